@@ -1,0 +1,102 @@
+"""The tolerance checker flags wrong results and accepts legal near-tie choices."""
+import numpy as np
+
+from oracle import check, propose
+
+
+def _case(seed=3, near_tie=False):
+    rng = np.random.default_rng(seed)
+    B, L, H, V, r, k = 3, 5, 16, 200, 4, 3
+    hidden = rng.standard_normal((B, L, H)).astype(np.float32)
+    W = rng.standard_normal((V, H)).astype(np.float32)
+    if near_tie:
+        W[7] = W[11] * np.float32(1.0 + 1e-4)   # rows 7 and 11 nearly equal
+    w1 = (rng.standard_normal((V, r)) * 0.3).astype(np.float32)
+    w2 = (rng.standard_normal((r, V)) * 0.3).astype(np.float32)
+    wc = rng.standard_normal(H).astype(np.float32)
+    anchors = rng.integers(0, V, B)
+    o = propose(hidden, anchors, W, w1, w2, L_in=L, sample_from_anchor=True, top_k=k,
+                conf_min=0.5, w_conf=wc, return_logits=True)
+    gpu = dict(draft=o["draft"].copy(), topk_ids=o["topk_ids"].copy(),
+               topk_vals=o["topk_vals"].astype(np.float32), conf=o["conf"].astype(np.float32),
+               n_draft=o["n_draft"].copy(), logits=o["logits"].astype(np.float32))
+    kw = dict(anchors=anchors, markov_w1=w1, markov_w2=w2, top_k=k, topk_markov=True,
+              conf_min=0.5, tol=2e-2)
+    return o, gpu, kw
+
+
+def test_exact_copy_passes():
+    o, gpu, kw = _case()
+    rep = check.check_propose(o, gpu=gpu, **kw)
+    assert rep["failures"] == []
+
+
+def test_wrong_token_flagged():
+    o, gpu, kw = _case()
+    gpu["draft"][1, 2] = (gpu["draft"][1, 2] + 1) % 200
+    assert check.check_propose(o, gpu=gpu, **kw)["failures"]
+
+
+def test_wrong_topk_flagged():
+    o, gpu, kw = _case()
+    gpu["topk_ids"][0, 1, [1, 2]] = gpu["topk_ids"][0, 1, [2, 1]]
+    gpu["topk_vals"][0, 1, [1, 2]] = gpu["topk_vals"][0, 1, [2, 1]]
+    rep = check.check_propose(o, gpu=gpu, **kw)
+    z = o["logits"][0, 1]
+    ids = o["topk_ids"][0, 1]
+    if abs(z[ids[1]] - z[ids[2]]) > 2e-2:
+        assert rep["failures"]
+
+
+def test_conf_and_ndraft_flagged():
+    o, gpu, kw = _case()
+    gpu["conf"][0, 0] += 0.1
+    assert check.check_propose(o, gpu=gpu, **kw)["failures"]
+    o, gpu, kw = _case()
+    gpu["n_draft"][2] = (gpu["n_draft"][2] + 1) % 6
+    assert check.check_propose(o, gpu=gpu, **kw)["failures"]
+
+
+def test_logits_flagged():
+    o, gpu, kw = _case()
+    gpu["logits"][2, 3, 17] += 0.05
+    assert check.check_propose(o, gpu=gpu, **kw)["failures"]
+
+
+def test_near_tie_alternative_accepted_and_chain_followed():
+    # force a near tie at one slot by construction: pick the GPU's token as the
+    # runner-up whenever the oracle margin is below tol
+    o, gpu, kw = _case()
+    z = o["logits"]
+    found = False
+    for b in range(z.shape[0]):
+        s = np.sort(z[b, 0])
+        if s[-1] - s[-2] < 5.0:
+            # pretend the tolerance is wide enough for this pair to be a near tie
+            kw2 = dict(kw, tol=float(s[-1] - s[-2]) + 1e-9)
+            alt = int(np.flatnonzero(z[b, 0] == s[-2])[0])
+            gpu2 = {k: (v.copy() if v is not None else None) for k, v in gpu.items()}
+            gpu2.pop("logits")
+            gpu2.pop("topk_ids")
+            gpu2.pop("topk_vals")
+            gpu2["draft"][b, 0] = alt
+            # the rest of the GPU chain follows the alternative token
+            from oracle import dspark_oracle as O
+            w2 = O.upcast(kw["markov_w2"])
+            prev = alt
+            for i in range(1, z.shape[1]):
+                zc = O.corrected_logits(o["base_logits"][b, i], kw["markov_w1"], w2, prev)
+                gpu2["draft"][b, i] = O.argmax_lowest(zc)
+                prev = gpu2["draft"][b, i]
+            rep = check.check_propose(o, gpu=gpu2, **kw2)
+            assert rep["failures"] == [], rep
+            found = True
+            break
+    assert found
+
+
+def test_verify_check():
+    d = np.array([[1, 2, 3]])
+    t = np.array([[1, 2, 0, 5]])
+    assert check.check_verify(d, [3], t, [2], [0]) == []
+    assert check.check_verify(d, [3], t, [3], [0])

@@ -1,0 +1,127 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that a pin fails.
+
+A pin set that a dropped term, a flipped sign, a wrong index or a transposed operand
+can slip through would not be evidence that the oracle is right.
+"""
+import contextlib
+
+import numpy as np
+import pytest
+
+import oracle_pins
+from oracle import dspark_oracle as O
+
+
+def _argmax_highest(row):
+    m = row.max()
+    return int(np.flatnonzero(row == m)[-1])
+
+
+def _chain_prev_always_anchor(z_b, w1, w2_f64, anchor, top_k=1, topk_markov=True):
+    N, V = z_b.shape
+    tok = np.empty(N, np.int64)
+    ids = np.empty((N, top_k), np.int64)
+    vals = np.empty((N, top_k))
+    zc = np.empty_like(z_b)
+    for i in range(N):
+        zc[i] = O.corrected_logits(z_b[i], w1, w2_f64, int(anchor))
+        tok[i] = O.argmax_lowest(zc[i])
+        ranked = zc[i] if topk_markov else z_b[i]
+        ids[i] = O.topk_sorted(ranked, top_k)
+        vals[i] = ranked[ids[i]]
+    return tok, ids, vals, zc
+
+
+def _chain_prev_is_own_slot(z_b, w1, w2_f64, anchor, top_k=1, topk_markov=True):
+    """prev(i) taken from the base argmax of slot i itself (an indexing slip)."""
+    N, V = z_b.shape
+    tok = np.empty(N, np.int64)
+    ids = np.empty((N, top_k), np.int64)
+    vals = np.empty((N, top_k))
+    zc = np.empty_like(z_b)
+    for i in range(N):
+        prev = int(anchor) if i == 0 else O.argmax_lowest(z_b[i])
+        zc[i] = O.corrected_logits(z_b[i], w1, w2_f64, prev)
+        tok[i] = O.argmax_lowest(zc[i])
+        ranked = zc[i] if topk_markov else z_b[i]
+        ids[i] = O.topk_sorted(ranked, top_k)
+        vals[i] = ranked[ids[i]]
+    return tok, ids, vals, zc
+
+
+def _verify_no_ndraft(draft, n_draft, target):
+    return _orig_verify(draft, np.full(len(draft), np.asarray(draft).shape[1]), target)
+
+
+def _verify_bonus_next(draft, n_draft, target):
+    a, b, e = _orig_verify(draft, n_draft, target)
+    t = np.asarray(target)
+    b2 = np.array([t[i, min(a[i] + 1, t.shape[1] - 1)] for i in range(len(a))])
+    e = e.copy()
+    for i in range(len(a)):
+        e[i, a[i]] = b2[i]
+    return a, b2, e
+
+
+_orig_verify = O.verify
+_orig_layout = O.block_layout
+_orig_base = O.base_logits
+_orig_conf = O.confidence
+
+
+MUTATIONS = {
+    "markov_dropped": ("corrected_logits", lambda z, w1, w2, prev: z),
+    "markov_sign": ("corrected_logits",
+                    lambda z, w1, w2, prev: z - O.markov_bias(w1, w2, prev)),
+    "markov_columns_reversed": ("markov_bias",
+                                lambda w1, w2, prev: O.upcast(np.asarray(w1)[prev]) @ w2[:, ::-1]),
+    "markov_rank_dropped": ("markov_bias",
+                            lambda w1, w2, prev: O.upcast(np.asarray(w1)[prev])[..., :-1] @ w2[:-1]),
+    "tie_to_highest": ("argmax_lowest", _argmax_highest),
+    "topk_ascending": ("topk_sorted",
+                       lambda row, k: np.lexsort((np.arange(row.shape[-1]), row))[:k]),
+    "prev_always_anchor": ("greedy_chain", _chain_prev_always_anchor),
+    "prev_from_own_slot": ("greedy_chain", _chain_prev_is_own_slot),
+    "truncate_le": ("truncation_length",
+                    lambda c, m: next((i for i in range(len(c)) if m > 0 and c[i] <= m), len(c))),
+    "conf_bias_dropped": ("confidence",
+                          lambda h, w, b, ifp, N: _orig_conf(h, w, 0.0, ifp, N)),
+    "conf_sign": ("confidence",
+                  lambda h, w, b, ifp, N: 1 - _orig_conf(h, w, b, ifp, N)),
+    "layout_bonus_ignored": ("block_layout", lambda L, sfa: (L, 0)),
+    "layout_wrong_offset": ("block_layout", lambda L, sfa: (L, 0) if sfa else (L - 1, 0)),
+    "lm_bias_dropped": ("base_logits",
+                        lambda h, W, bias, ifp, N, chunk=16384: _orig_base(h, W, None, ifp, N, chunk)),
+    "lm_head_transposed_rows": ("base_logits",
+                                lambda h, W, bias, ifp, N, chunk=16384:
+                                _orig_base(h, np.asarray(W)[:, ::-1], bias, ifp, N, chunk)),
+    "verify_ignores_ndraft": ("verify", _verify_no_ndraft),
+    "verify_bonus_off_by_one": ("verify", _verify_bonus_next),
+    "upcast_truncates": ("upcast",
+                         lambda a: (np.asarray(a).astype(np.float32).astype(np.float16).astype(np.float64)
+                                    if np.asarray(a).dtype != np.uint16 else
+                                    ((np.asarray(a).astype(np.uint32) << 16).view(np.float32) * 1.0078125).astype(np.float64))),
+}
+
+
+@contextlib.contextmanager
+def _planted(name, fn):
+    old = getattr(O, name)
+    setattr(O, name, fn)
+    try:
+        yield
+    finally:
+        setattr(O, name, old)
+
+
+@pytest.mark.parametrize("mutation", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(mutation):
+    name, fn = MUTATIONS[mutation]
+    caught = []
+    with _planted(name, fn), np.errstate(all="ignore"):
+        for pin in oracle_pins.ALL_PINS:
+            try:
+                pin()
+            except (AssertionError, IndexError, ValueError):
+                caught.append(pin.__name__)
+    assert caught, f"no pin catches the planted mistake {mutation}"
