@@ -1,0 +1,410 @@
+#!/usr/bin/env python3
+"""Benchmark: DSpark proposal head + greedy verify on one GB300 per process.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step is one full pass of the path over one batch: dspark_propose (confidence,
+base logits, Markov-corrected greedy chain, top-k, truncation) then dspark_verify.
+The default workload is the Qwen3-8B-shaped head at B=32 blocks of L=16 slots
+(H=4096, V=151936, r=256, top_k=8, conf_min=0.5).  Inputs are seeded and synthetic.
+
+Timing: W untimed warm-up steps, then K timed steps.  Before every timed step a 512 MB
+buffer is written (L2 flush, untimed); each step is bracketed by CUDA events on the
+launching stream, and the library records stage events inside dspark_propose_timed so
+the lm_head GEMM's own duration is known.  Under torchrun each rank runs an
+independent replica on its own batch (no collective on the data path: blocks are
+independent); the step time is the maximum over ranks and ``value`` counts the slots
+of all ranks.
+
+``--impl reference`` times the CPU oracle (float64 NumPy) on the host cores on a
+bounded sample of the same workload and prints the same JSON line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "drafted slots/sec (propose+verify) at B=32, V=151936"
+UNIT = "slots/s"
+FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["_source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["_source"] = "fallback"
+    return d
+
+
+def _algorithmic(wl, V_head):
+    """Algorithmic bytes and flops of one pass (all steps), and of the lm_head GEMM."""
+    es = 2 if wl.dtype == "bf16" else 4
+    M, H, r, B, N, k = wl.M, wl.H, wl.r, wl.B, wl.N, wl.top_k
+    gemm_bytes = V_head * H * es + M * H * es + M * V_head * 4 * 0   # W + hidden (+bias)
+    gemm_flops = 2.0 * M * H * V_head
+    markov_flops = 2.0 * M * r * V_head
+    bytes_all = (V_head * H * es + r * V_head * es + M * r * es + B * wl.L_in * H * es
+                 + H * es + (V_head * 4 if wl.n_emit else 0)
+                 + B * N * (4 + 4 + 8 * k) + B * (N + 1) * 4 + B * 16)
+    flops_all = gemm_flops + markov_flops + 2.0 * M * H
+    return dict(gemm_bytes=gemm_bytes, gemm_flops=gemm_flops, bytes=bytes_all,
+                flops=flops_all)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].isdigit():
+                    rows.append(parts)
+        if not rows:
+            return None
+        sm = [int(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_pass(wl, hd, bt, blocks):
+    """One propose + verify of the oracle on the first ``blocks`` blocks."""
+    from oracle import propose, verify
+    from workloads import make_target
+    sub = {k: v[:blocks] for k, v in bt.items()}
+    o = propose(sub["hidden"], sub["anchors"], hd["lm_head"], hd["markov_w1"],
+                hd["markov_w2"], L_in=wl.L_in, sample_from_anchor=wl.sample_from_anchor,
+                top_k=wl.top_k, conf_min=wl.conf_min, lm_bias=hd.get("lm_bias"),
+                w_conf=hd.get("w_conf"), b_conf=hd.get("b_conf", 0.0),
+                topk_markov=wl.topk_markov)
+    target = make_target(wl, o["draft"])
+    verify(o["draft"], o["n_draft"], target)
+    return o
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, hd, bt, budget_s=20.0, blocks=4):
+    """Time the oracle as it stands on a bounded sample; returns the JSON object."""
+    times = []
+    t_end = time.time() + budget_s
+    while True:
+        t0 = time.perf_counter()
+        oracle_pass(wl, hd, bt, blocks)
+        times.append(time.perf_counter() - t0)
+        if time.time() + times[-1] > t_end or len(times) >= 5:
+            break
+    t = statistics.median(times)
+    return {"value": blocks * wl.N / t, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": f"{blocks} of {wl.B} blocks x {wl.N} slots, full vocabulary "
+                      f"(V={wl.V}), propose + verify, float64 NumPy; median of "
+                      f"{len(times)} passes ({t:.2f} s each)"}
+
+
+def run_reference(args):
+    rank, world, local = _dist()
+    if rank != 0:
+        return 0
+    from workloads import WORKLOADS, make_batch, make_head
+    wl = WORKLOADS[args.workload]
+    hd, bt = make_head(wl), make_batch(wl)
+    blocks = 1
+    for _ in range(args.warmup):
+        oracle_pass(wl, hd, bt, blocks)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_pass(wl, hd, bt, blocks)
+        times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    v = blocks * wl.N / t
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": _config(wl, "host cores, no L2 flush (CPU)"),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                             "sample": f"{blocks} of {wl.B} blocks per step, all {wl.N} "
+                                       f"slots, full vocabulary, propose + verify"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(wl, l2):
+    return {"workload": wl.name, "B": wl.B, "L": wl.L_in, "N": wl.N, "H": wl.H, "V": wl.V,
+            "r": wl.r, "top_k": wl.top_k, "conf_min": wl.conf_min,
+            "layout": "anchor-first" if wl.sample_from_anchor else "1+N bonus anchor",
+            "n_emit": wl.n_emit, "l2": l2, "parallelism": "replicas (blocks per GPU)"}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from dspark_block_drafter_gb300 import _abi
+    from dspark_block_drafter_gb300 import torch_io as tio
+    from workloads import WORKLOADS, make_batch, make_head, make_target
+
+    wl = WORKLOADS[args.workload]
+    hd = make_head(wl)
+    bt = make_batch(wl, batch_index=rank)           # each replica drafts its own batch
+    form = "d2t" if wl.n_emit else "full"
+    head = tio.head_to_device(hd, form, dev)
+    cfg = tio.make_config(wl.B, wl.L_in, wl.H, wl.V, wl.r, wl.top_k, wl.sample_from_anchor,
+                          wl.conf_min, wl.dtype, wl.topk_markov)
+    hidden = tio.to_device(bt["hidden"], dev)
+    anchors = tio.to_device(bt["anchors"], dev)
+    out = tio.Outputs.allocate(wl.B, wl.N, wl.top_k, head.V_head, dev, topk=True, conf=True)
+    ws = tio.workspace_for(cfg, head, dev)
+    stream = torch.cuda.current_stream(dev)
+    acc = torch.empty(wl.B, dtype=torch.int32, device=dev)
+    bonus = torch.empty(wl.B, dtype=torch.int32, device=dev)
+    emitted = torch.empty(wl.B, wl.N + 1, dtype=torch.int32, device=dev)
+
+    # target tokens: agree with this replica's draft for a seeded geometric prefix
+    tio.propose(cfg, head, hidden, anchors, out, ws, stream)
+    torch.cuda.synchronize()
+    target = tio.to_device(make_target(wl, out.draft.cpu().numpy(), rank), dev)
+
+    def step(events=None):
+        if events is None:
+            tio.propose(cfg, head, hidden, anchors, out, ws, stream)
+        else:
+            _abi.check(_abi.dspark_propose_timed(
+                cfg, head.struct(), hidden.data_ptr(), anchors.data_ptr(), out.struct(),
+                ws.data_ptr(), ws.numel(), stream.cuda_stream, [e.cuda_event for e in events]))
+        tio.verify(out.draft, out.n_draft, target, acc, bonus, emitted, stream)
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert tio.device_status(ws, stream) == 0
+
+    K = args.steps
+    ns = _abi.DSPARK_NUM_STAGES
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    ev_stage = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(K)]
+    for evs in ev_stage:          # materialise the handles the library records into
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for s in range(K):
+        flush.zero_()                                   # untimed L2 flush
+        ev_step[s][0].record(stream)
+        step(ev_stage[s])
+        ev_step[s][1].record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    assert tio.device_status(ws, stream) == 0
+
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    stage_ms = {name: statistics.mean(ev_stage[s][i].elapsed_time(ev_stage[s][i + 1])
+                                      for s in range(K))
+                for i, name in enumerate(_abi.STAGE_NAMES)}
+    ms = statistics.mean(step_ms)
+    ms_max = _max_over_ranks(ms, world, dev)
+    slots = wl.B * wl.N * world
+    value = slots / (ms_max / 1e3)
+
+    # end to end through the host-buffer entry point (copies inside the timed region)
+    e2e = e2e_host(cfg, head, wl, bt, target, dev, stream, flush, K, args.warmup, world)
+
+    peaks = _peaks()
+    alg = _algorithmic(wl, head.V_head)
+    gemm_ms = stage_ms["logits"]
+    peak_tf = peaks["bf16_tflops"] if wl.dtype == "bf16" else peaks["bf16_tflops"] / 4
+    achieved = alg["gemm_flops"] / (gemm_ms / 1e3) / 1e12
+    t_roof = max(alg["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                 alg["flops"] / (peaks["bf16_tflops"] * 1e12))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": _config(wl, f"flushed: {FLUSH_BYTES >> 20} MB written before each timed "
+                              "step (untimed)"),
+        "verified_blocks_per_s": wl.B * world / (ms_max / 1e3),
+        "t_pass_us": ms_max * 1e3,
+        "stage_us": {k: v * 1e3 for k, v in stage_ms.items()},
+        "pass_roofline": {"t_roof_us": t_roof * 1e6, "frac": t_roof / (ms_max / 1e3),
+                          "bytes": alg["bytes"], "flops": alg["flops"],
+                          "peaks": peaks["_source"]},
+        "roofline": {"kernel": "base logits (lm_head GEMM)", "bound": "tensor",
+                     "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": None,
+                     "peak_source": f"{peaks['_source']} bf16 burst"},
+        "e2e": e2e,
+        "gpu_launches": K * (_abi.dspark_propose_kernel_count(cfg, head.struct()) + 1),
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, hd, bt)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_host(cfg, head, wl, bt, target_dev, dev, stream, flush, K, W, world):
+    """Same metric through dspark_step_host with page-locked host buffers."""
+    import torch
+    from dspark_block_drafter_gb300 import _abi
+    from dspark_block_drafter_gb300 import torch_io as tio
+    hidden_h = tio.to_device(bt["hidden"], "cpu").pin_memory()
+    anchors_h = torch.from_numpy(bt["anchors"]).pin_memory()
+    target_h = target_dev.cpu().pin_memory()
+    B, N, k = wl.B, wl.N, wl.top_k
+    i32 = dict(dtype=torch.int32, pin_memory=True)
+    draft_h, nd_h = torch.empty(B, N, **i32), torch.empty(B, **i32)
+    acc_h, bon_h = torch.empty(B, **i32), torch.empty(B, **i32)
+    tki_h = torch.empty(B, N, k, **i32)
+    tkv_h = torch.empty(B, N, k, dtype=torch.float32, pin_memory=True)
+    n = _abi.dspark_step_host_workspace_size(cfg, head.struct())
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+
+    def go():
+        _abi.check(_abi.dspark_step_host(cfg, head.struct(), hidden_h.data_ptr(),
+                                         anchors_h.data_ptr(), target_h.data_ptr(),
+                                         draft_h.data_ptr(), nd_h.data_ptr(), acc_h.data_ptr(),
+                                         bon_h.data_ptr(), tki_h.data_ptr(), tkv_h.data_ptr(),
+                                         ws.data_ptr(), n, stream.cuda_stream))
+    for _ in range(W):
+        flush.zero_()
+        go()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(K):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        go()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = _max_over_ranks(statistics.mean(times), world, dev)
+    h2d = hidden_h.numel() * hidden_h.element_size() + 4 * B + 4 * B * (N + 1)
+    d2h = 4 * (B * N + 3 * B) + 8 * B * N * k
+    return {"value": B * N * world / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "api": "dspark_step_host (page-locked host buffers)"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_8b_b32")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,320 @@
+// The C ABI: argument validation, workspace carve-up and kernel dispatch.
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/dspark.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dspark {
+
+static thread_local std::string g_last_error;
+
+static dspark_status fail(dspark_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+static dspark_status cuda_fail(cudaError_t e, const char* where) {
+  g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
+  return DSPARK_ERR_CUDA;
+}
+
+static constexpr size_t kAlign = 256;
+static constexpr size_t kCtrlBytes = 4096;
+
+WorkspaceLayout plan_workspace(int B, int N, int Vh) {
+  WorkspaceLayout w{};
+  w.ldz = align_up((size_t)Vh, 64);
+  size_t off = 0;
+  w.ctrl = off;
+  off += kCtrlBytes;
+  w.z = off;
+  off = align_up(off + sizeof(float) * (size_t)N * B * w.ldz, kAlign);
+  w.zc = off;
+  off = align_up(off + sizeof(float) * (size_t)B * w.ldz, kAlign);
+  w.prev = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)B, kAlign);
+  w.conf = off;
+  off = align_up(off + sizeof(float) * (size_t)B * N, kAlign);
+  w.total = off;
+  return w;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Host-side checks; on success fills N and i_first_pred.
+static dspark_status validate(const dspark_config* c, const dspark_head* h, int* N,
+                              int* ifp) {
+  if (!c) return fail(DSPARK_ERR_INVALID_ARG, "config is NULL");
+  if (!h) return fail(DSPARK_ERR_INVALID_ARG, "head is NULL");
+  if (c->B < 1 || c->L_in < 1 || c->H < 1 || c->V < 1 || c->r < 1)
+    return fail(DSPARK_ERR_INVALID_ARG, "B, L_in, H, V and r must all be >= 1");
+  if (c->sample_from_anchor != 0 && c->sample_from_anchor != 1)
+    return fail(DSPARK_ERR_INVALID_ARG, "sample_from_anchor must be 0 or 1");
+  if (c->topk_markov != 0 && c->topk_markov != 1)
+    return fail(DSPARK_ERR_INVALID_ARG, "topk_markov must be 0 or 1");
+  if (c->dtype != DSPARK_F32 && c->dtype != DSPARK_BF16)
+    return fail(DSPARK_ERR_INVALID_ARG, "dtype must be DSPARK_F32 or DSPARK_BF16");
+  if (!c->sample_from_anchor && c->L_in < 2)
+    return fail(DSPARK_ERR_INVALID_ARG, "the 1+N bonus-anchor layout needs L_in >= 2");
+  if (!(c->conf_min == c->conf_min))
+    return fail(DSPARK_ERR_INVALID_ARG, "conf_min is NaN");
+  if (!h->lm_head || !h->markov_w1 || !h->markov_w2)
+    return fail(DSPARK_ERR_INVALID_ARG, "lm_head, markov_w1 and markov_w2 are required");
+  if (h->V_head < 1 || h->V_head > c->V)
+    return fail(DSPARK_ERR_INVALID_ARG, "V_head must be in [1, V]");
+  if (!h->d2t && h->V_head != c->V)
+    return fail(DSPARK_ERR_INVALID_ARG, "without d2t, V_head must equal V");
+  if (c->top_k < 1 || c->top_k > 32 || c->top_k > h->V_head)
+    return fail(DSPARK_ERR_INVALID_ARG, "top_k must be in [1, min(32, V_head)]");
+  if (c->r > 4096) return fail(DSPARK_ERR_UNSUPPORTED, "Markov rank above 4096");
+  if ((long long)c->B * c->L_in > (1ll << 30) || (long long)c->V * c->r > (1ll << 40))
+    return fail(DSPARK_ERR_UNSUPPORTED, "sizes too large");
+  if (c->dtype == DSPARK_BF16) {
+    if (c->H % 8 != 0)
+      return fail(DSPARK_ERR_UNSUPPORTED, "bf16 path needs H % 8 == 0 (16-byte rows)");
+    if (h->V_head % 8 != 0)
+      return fail(DSPARK_ERR_UNSUPPORTED, "bf16 path needs V_head % 8 == 0 (16-byte rows)");
+    if (!aligned(h->lm_head, 16) || !aligned(h->markov_w2, 16) || !aligned(h->markov_w1, 16))
+      return fail(DSPARK_ERR_INVALID_ARG, "bf16 weights must be 16-byte aligned");
+  }
+  *N = c->sample_from_anchor ? c->L_in : c->L_in - 1;
+  *ifp = c->sample_from_anchor ? 0 : 1;
+  return DSPARK_OK;
+}
+
+}  // namespace dspark
+
+using namespace dspark;
+
+static_assert(sizeof(dspark_config) == 40, "dspark_config layout");
+static_assert(sizeof(dspark_head) == 64, "dspark_head layout");
+static_assert(sizeof(dspark_outputs) == 48, "dspark_outputs layout");
+
+extern "C" {
+
+int32_t dspark_num_slots(const dspark_config* cfg) {
+  if (!cfg || cfg->L_in < 1) return 0;
+  if (cfg->sample_from_anchor) return cfg->L_in;
+  return cfg->L_in >= 2 ? cfg->L_in - 1 : 0;
+}
+
+size_t dspark_propose_workspace_size(const dspark_config* cfg, const dspark_head* head) {
+  int N, ifp;
+  if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return 0;
+  return plan_workspace(cfg->B, N, head->V_head).total;
+}
+
+static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* head,
+                                  const void* hidden, const int32_t* anchors,
+                                  const dspark_outputs* out, void* workspace,
+                                  size_t workspace_bytes, void* stream,
+                                  void* const* events) {
+  int N, ifp;
+  dspark_status st = validate(cfg, head, &N, &ifp);
+  if (st != DSPARK_OK) return st;
+  if (!hidden || !anchors) return fail(DSPARK_ERR_INVALID_ARG, "hidden and anchors are required");
+  if (!out || !out->draft || !out->n_draft)
+    return fail(DSPARK_ERR_INVALID_ARG, "outputs draft and n_draft are required");
+  if (cfg->dtype == DSPARK_BF16 && !aligned(hidden, 16))
+    return fail(DSPARK_ERR_INVALID_ARG, "bf16 hidden must be 16-byte aligned");
+  WorkspaceLayout wl = plan_workspace(cfg->B, N, head->V_head);
+  if (!workspace || !aligned(workspace, 256))
+    return fail(DSPARK_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+  if (workspace_bytes < wl.total)
+    return fail(DSPARK_ERR_WORKSPACE, "workspace too small: need " +
+                                          std::to_string(wl.total) + " bytes");
+
+  char* ws = (char*)workspace;
+  ProposePlan p{};
+  p.B = cfg->B; p.L_in = cfg->L_in; p.N = N; p.ifp = ifp; p.H = cfg->H; p.V = cfg->V;
+  p.Vh = head->V_head; p.r = cfg->r; p.k = cfg->top_k; p.topk_markov = cfg->topk_markov;
+  p.dtype = cfg->dtype; p.conf_min = cfg->conf_min; p.b_conf = head->b_conf;
+  p.hidden = hidden; p.anchors = anchors; p.lm_head = head->lm_head;
+  p.lm_bias = head->lm_bias; p.d2t = head->d2t; p.w1 = head->markov_w1;
+  p.w2 = head->markov_w2; p.w_conf = head->w_conf;
+  p.draft = out->draft; p.n_draft = out->n_draft; p.topk_ids = out->topk_ids;
+  p.topk_vals = out->topk_vals; p.conf = head->w_conf ? out->conf : nullptr;
+  p.logits = out->logits;
+  p.ctrl = (uint32_t*)(ws + wl.ctrl);
+  p.z = (float*)(ws + wl.z);
+  p.ldz = wl.ldz;
+  p.zc = (float*)(ws + wl.zc);
+  p.prev = (int32_t*)(ws + wl.prev);
+  p.conf_ws = (float*)(ws + wl.conf);
+  p.stream = (cudaStream_t)stream;
+
+  cudaError_t e;
+  auto mark = [&](int s) -> cudaError_t {
+    return events ? cudaEventRecord((cudaEvent_t)events[s], p.stream) : cudaSuccess;
+  };
+  // the control block (error word included) starts from zero on every call
+  e = cudaMemsetAsync(ws + wl.ctrl, 0, kCtrlBytes, p.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "control reset");
+  if ((e = mark(DSPARK_STAGE_CONF)) != cudaSuccess) return cuda_fail(e, "event record");
+  if ((e = launch_conf(p)) != cudaSuccess) return cuda_fail(e, "confidence kernel");
+  if ((e = mark(DSPARK_STAGE_LOGITS)) != cudaSuccess) return cuda_fail(e, "event record");
+  if ((e = launch_base_logits_simt(p)) != cudaSuccess) return cuda_fail(e, "base logits");
+  if ((e = mark(DSPARK_STAGE_CHAIN)) != cudaSuccess) return cuda_fail(e, "event record");
+  if ((e = launch_chain_simt(p)) != cudaSuccess) return cuda_fail(e, "chain");
+  if ((e = mark(DSPARK_STAGE_TOPK)) != cudaSuccess) return cuda_fail(e, "event record");
+  if ((e = mark(DSPARK_NUM_STAGES)) != cudaSuccess) return cuda_fail(e, "event record");
+  return DSPARK_OK;
+}
+
+dspark_status dspark_propose(const dspark_config* cfg, const dspark_head* head,
+                             const void* hidden, const int32_t* anchors,
+                             const dspark_outputs* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return propose_impl(cfg, head, hidden, anchors, out, workspace, workspace_bytes, stream,
+                      nullptr);
+}
+
+dspark_status dspark_propose_timed(const dspark_config* cfg, const dspark_head* head,
+                                   const void* hidden, const int32_t* anchors,
+                                   const dspark_outputs* out, void* workspace,
+                                   size_t workspace_bytes, void* stream,
+                                   void* const* events) {
+  if (!events) return fail(DSPARK_ERR_INVALID_ARG, "events is NULL");
+  for (int s = 0; s <= DSPARK_NUM_STAGES; ++s)
+    if (!events[s]) return fail(DSPARK_ERR_INVALID_ARG, "an event is NULL");
+  return propose_impl(cfg, head, hidden, anchors, out, workspace, workspace_bytes, stream,
+                      events);
+}
+
+int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head* head) {
+  int N, ifp;
+  if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return -1;
+  return 1 /* confidence */ + 1 /* base logits */ + 2 * N /* chain steps */;
+}
+
+// staging for dspark_step_host, placed after dspark_propose's workspace
+struct StageLayout {
+  size_t hidden, anchors, target, draft, n_draft, accepted, bonus, tk_ids, tk_vals, total;
+};
+static StageLayout plan_stage(const dspark_config* c, int N, size_t base) {
+  StageLayout s{};
+  size_t es = c->dtype == DSPARK_BF16 ? 2 : 4;
+  size_t off = base;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, kAlign); return o; };
+  s.hidden = take(es * (size_t)c->B * c->L_in * c->H);
+  s.anchors = take(4 * (size_t)c->B);
+  s.target = take(4 * (size_t)c->B * (N + 1));
+  s.draft = take(4 * (size_t)c->B * N);
+  s.n_draft = take(4 * (size_t)c->B);
+  s.accepted = take(4 * (size_t)c->B);
+  s.bonus = take(4 * (size_t)c->B);
+  s.tk_ids = take(4 * (size_t)c->B * N * c->top_k);
+  s.tk_vals = take(4 * (size_t)c->B * N * c->top_k);
+  s.total = off;
+  return s;
+}
+
+size_t dspark_step_host_workspace_size(const dspark_config* cfg, const dspark_head* head) {
+  int N, ifp;
+  if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return 0;
+  return plan_stage(cfg, N, plan_workspace(cfg->B, N, head->V_head).total).total;
+}
+
+dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head,
+                               const void* hidden_h, const int32_t* anchors_h,
+                               const int32_t* target_h, int32_t* draft_h,
+                               int32_t* n_draft_h, int32_t* accepted_h, int32_t* bonus_h,
+                               int32_t* topk_ids_h, float* topk_vals_h,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  int N, ifp;
+  dspark_status st = validate(cfg, head, &N, &ifp);
+  if (st != DSPARK_OK) return st;
+  if (!hidden_h || !anchors_h || !target_h || !draft_h || !n_draft_h || !accepted_h || !bonus_h)
+    return fail(DSPARK_ERR_INVALID_ARG, "a required host buffer is NULL");
+  size_t base = plan_workspace(cfg->B, N, head->V_head).total;
+  StageLayout s = plan_stage(cfg, N, base);
+  if (!workspace || !aligned(workspace, 256))
+    return fail(DSPARK_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+  if (workspace_bytes < s.total)
+    return fail(DSPARK_ERR_WORKSPACE, "workspace too small: need " + std::to_string(s.total) +
+                                          " bytes");
+  char* ws = (char*)workspace;
+  cudaStream_t cs = (cudaStream_t)stream;
+  const size_t es = cfg->dtype == DSPARK_BF16 ? 2 : 4;
+  const size_t B = cfg->B, k = cfg->top_k;
+  cudaError_t e;
+  auto h2d = [&](size_t off, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(ws + off, src, bytes, cudaMemcpyHostToDevice, cs);
+  };
+  auto d2h = [&](void* dst, size_t off, size_t bytes) {
+    return cudaMemcpyAsync(dst, ws + off, bytes, cudaMemcpyDeviceToHost, cs);
+  };
+  if ((e = h2d(s.hidden, hidden_h, es * B * cfg->L_in * cfg->H)) != cudaSuccess ||
+      (e = h2d(s.anchors, anchors_h, 4 * B)) != cudaSuccess ||
+      (e = h2d(s.target, target_h, 4 * B * (N + 1))) != cudaSuccess)
+    return cuda_fail(e, "host-to-device copy");
+  dspark_outputs o{};
+  o.draft = (int32_t*)(ws + s.draft);
+  o.n_draft = (int32_t*)(ws + s.n_draft);
+  o.topk_ids = topk_ids_h ? (int32_t*)(ws + s.tk_ids) : nullptr;
+  o.topk_vals = topk_vals_h ? (float*)(ws + s.tk_vals) : nullptr;
+  st = propose_impl(cfg, head, ws + s.hidden, (const int32_t*)(ws + s.anchors), &o, workspace,
+                    base, stream, nullptr);
+  if (st != DSPARK_OK) return st;
+  st = dspark_verify(cfg->B, N, o.draft, o.n_draft, (const int32_t*)(ws + s.target),
+                     (int32_t*)(ws + s.accepted), (int32_t*)(ws + s.bonus), nullptr, stream);
+  if (st != DSPARK_OK) return st;
+  if ((e = d2h(draft_h, s.draft, 4 * B * N)) != cudaSuccess ||
+      (e = d2h(n_draft_h, s.n_draft, 4 * B)) != cudaSuccess ||
+      (e = d2h(accepted_h, s.accepted, 4 * B)) != cudaSuccess ||
+      (e = d2h(bonus_h, s.bonus, 4 * B)) != cudaSuccess)
+    return cuda_fail(e, "device-to-host copy");
+  if (topk_ids_h && (e = d2h(topk_ids_h, s.tk_ids, 4 * B * N * k)) != cudaSuccess)
+    return cuda_fail(e, "device-to-host copy");
+  if (topk_vals_h && (e = d2h(topk_vals_h, s.tk_vals, 4 * B * N * k)) != cudaSuccess)
+    return cuda_fail(e, "device-to-host copy");
+  return DSPARK_OK;
+}
+
+dspark_status dspark_verify(int32_t B, int32_t N, const int32_t* draft,
+                            const int32_t* n_draft, const int32_t* target,
+                            int32_t* accepted, int32_t* bonus, int32_t* emitted,
+                            void* stream) {
+  if (B < 1 || N < 1) return fail(DSPARK_ERR_INVALID_ARG, "B and N must be >= 1");
+  if (!draft || !n_draft || !target || !accepted || !bonus)
+    return fail(DSPARK_ERR_INVALID_ARG, "draft, n_draft, target, accepted, bonus are required");
+  cudaError_t e = launch_verify(B, N, draft, n_draft, target, accepted, bonus, emitted,
+                                (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "verify kernel");
+  return DSPARK_OK;
+}
+
+dspark_status dspark_device_status(void* workspace, void* stream) {
+  if (!workspace) return fail(DSPARK_ERR_INVALID_ARG, "workspace is NULL");
+  uint32_t word = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (word == 0) return DSPARK_OK;
+  e = cudaMemsetAsync(workspace, 0, sizeof(word), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  if (word & kErrTimeout) return fail(DSPARK_ERR_TIMEOUT, "a device-side wait timed out");
+  return fail(DSPARK_ERR_DEVICE, "a kernel saw a token outside [0, V)");
+}
+
+const char* dspark_status_string(int32_t s) {
+  switch (s) {
+    case DSPARK_OK: return "ok";
+    case DSPARK_ERR_INVALID_ARG: return "invalid argument";
+    case DSPARK_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DSPARK_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DSPARK_ERR_CUDA: return "CUDA runtime error";
+    case DSPARK_ERR_DEVICE: return "device-side data error";
+    case DSPARK_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* dspark_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

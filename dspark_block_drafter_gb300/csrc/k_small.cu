@@ -1,0 +1,103 @@
+// Small kernels of the path: the confidence head with the truncation length, and the
+// greedy verify/accept step.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dspark {
+
+namespace {
+
+// conf[b, i] = sigmoid(h[b, ifp + i] . w_conf + b_conf) and n_draft[b] = the first slot
+// with conf < conf_min, else N (llama.cpp commit 6fed9f6, "spec: add confidence-based
+// draft pruning for DSpark": truncate at the first position below the threshold, 0
+// disables).  One CTA per block; warps take slots round-robin.
+template <typename T>
+__global__ void __launch_bounds__(256)
+conf_truncate(const T* __restrict__ hidden, const T* __restrict__ w_conf, float b_conf,
+              int L_in, int N, int ifp, int H, float conf_min, float* __restrict__ conf,
+              int32_t* __restrict__ n_draft) {
+  extern __shared__ float sconf[];  // [N]
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
+  if (w_conf) {
+    for (int i = warp; i < N; i += nw) {
+      const T* h = hidden + ((size_t)b * L_in + ifp + i) * H;
+      float acc = 0.f;
+      for (int c = lane; c < H; c += 32) acc = fmaf(to_f32(h[c]), to_f32(w_conf[c]), acc);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+      if (lane == 0) {
+        float c = 1.f / (1.f + expf(-(acc + b_conf)));
+        sconf[i] = c;
+        conf[(size_t)b * N + i] = c;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int n = N;
+    if (w_conf && conf_min > 0.f) {
+      for (int i = 0; i < N; ++i)
+        if (sconf[i] < conf_min) { n = i; break; }
+    }
+    n_draft[b] = n;
+  }
+}
+
+// Greedy verify/accept, unchanged from DFlash (llama.cpp commit 6fed9f6: "verify
+// unchanged, same as DFlash"; greedy stays lossless).  One warp per block: a ballot over
+// the slot comparisons finds the first mismatch.
+__global__ void __launch_bounds__(256)
+verify_kernel(int B, int N, const int32_t* __restrict__ draft,
+              const int32_t* __restrict__ n_draft, const int32_t* __restrict__ target,
+              int32_t* __restrict__ accepted, int32_t* __restrict__ bonus,
+              int32_t* __restrict__ emitted) {
+  const int b = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (b >= B) return;
+  const int nd = min(max(n_draft[b], 0), N);
+  const int32_t* d = draft + (size_t)b * N;
+  const int32_t* t = target + (size_t)b * (N + 1);
+  int a = nd;
+  for (int j0 = 0; j0 < nd; j0 += 32) {
+    const int j = j0 + lane;
+    const bool mismatch = j < nd && d[j] != t[j];
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, mismatch);
+    if (m) { a = j0 + __ffs(m) - 1; break; }
+  }
+  const int bo = t[a];
+  if (lane == 0) {
+    accepted[b] = a;
+    bonus[b] = bo;
+  }
+  if (emitted)
+    for (int j = lane; j <= N; j += 32)
+      emitted[(size_t)b * (N + 1) + j] = j < a ? d[j] : (j == a ? bo : -1);
+}
+
+}  // namespace
+
+cudaError_t launch_conf(const ProposePlan& p) {
+  float* conf = p.conf ? p.conf : p.conf_ws;
+  size_t smem = sizeof(float) * (size_t)p.N;
+  if (p.dtype == 0)
+    conf_truncate<float><<<p.B, 256, smem, p.stream>>>(
+        (const float*)p.hidden, (const float*)p.w_conf, p.b_conf, p.L_in, p.N, p.ifp, p.H,
+        p.conf_min, conf, p.n_draft);
+  else
+    conf_truncate<__nv_bfloat16><<<p.B, 256, smem, p.stream>>>(
+        (const __nv_bfloat16*)p.hidden, (const __nv_bfloat16*)p.w_conf, p.b_conf, p.L_in,
+        p.N, p.ifp, p.H, p.conf_min, conf, p.n_draft);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify(int B, int N, const int32_t* draft, const int32_t* n_draft,
+                          const int32_t* target, int32_t* accepted, int32_t* bonus,
+                          int32_t* emitted, cudaStream_t stream) {
+  const int warps_per_cta = 8;
+  verify_kernel<<<(B + warps_per_cta - 1) / warps_per_cta, 32 * warps_per_cta, 0, stream>>>(
+      B, N, draft, n_draft, target, accepted, bonus, emitted);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -1,0 +1,55 @@
+// Internal launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dspark {
+
+// Everything a proposal launch needs, resolved by the ABI layer.
+struct ProposePlan {
+  // sizes
+  int B, L_in, N, ifp, H, V, Vh, r, k, topk_markov, dtype;
+  float conf_min, b_conf;
+  // inputs
+  const void* hidden;
+  const int32_t* anchors;
+  const void* lm_head;
+  const float* lm_bias;
+  const int32_t* d2t;
+  const void* w1;
+  const void* w2;
+  const void* w_conf;
+  // outputs
+  int32_t* draft;
+  int32_t* n_draft;
+  int32_t* topk_ids;
+  float* topk_vals;
+  float* conf;
+  float* logits;
+  // workspace pieces
+  uint32_t* ctrl;       // [0] = error word, the rest control words of the chain
+  float* z;             // base logits [N][B][ldz]
+  size_t ldz;
+  float* zc;            // corrected logits of the current slot [B][ldz]
+  int32_t* prev;        // previous tokens [B]
+  float* conf_ws;       // confidences when the caller did not ask for them [B][N]
+  cudaStream_t stream;
+};
+
+// Workspace carve-up shared by the size query and the launch.
+struct WorkspaceLayout {
+  size_t ctrl, z, zc, prev, conf, total;
+  size_t ldz;
+};
+WorkspaceLayout plan_workspace(int B, int N, int Vh);
+
+cudaError_t launch_conf(const ProposePlan& p);
+cudaError_t launch_base_logits_simt(const ProposePlan& p);
+cudaError_t launch_chain_simt(const ProposePlan& p);
+cudaError_t launch_verify(int B, int N, const int32_t* draft, const int32_t* n_draft,
+                          const int32_t* target, int32_t* accepted, int32_t* bonus,
+                          int32_t* emitted, cudaStream_t stream);
+
+}  // namespace dspark

@@ -1,0 +1,220 @@
+/*
+ * dspark.h -- C ABI of the DSpark proposal head and the greedy verify step.
+ *
+ * The method (llama.cpp commit 6fed9f6, src/models/dflash.cpp, squash log of
+ * "spec: add DSpark speculative decoding", the proposal formula):
+ *
+ *   logits(i)  = h[b, i] . lm_head^T (+ lm_bias)
+ *   logits'(i) = logits(i) + markov_w2^T . markov_w1[prev(i)]
+ *   prev(0)    = the block's anchor token,  prev(i > 0) = argmax logits'(i - 1)
+ *
+ * run greedily over the slots of a block and in parallel over the blocks of a batch,
+ * followed by DFlash's unchanged greedy verify/accept.  The confidence head
+ * conf = sigmoid(h . w_conf + b_conf) truncates each block at its first slot below
+ * conf_min ("spec: add confidence-based draft pruning for DSpark").  Block layouts:
+ * anchor-first (every slot predicts) and the 1+N bonus-anchor layout of
+ * speculators-format drafts (llama.cpp PR #26275, "Format differences": slot 0 holds
+ * the bonus token and is not a prediction slot).  Reduced draft vocabularies come in
+ * the two forms PR #26275 describes: an lm_head expanded to the full vocabulary with a
+ * -1e9 bias on rows the draft cannot emit, or a compact head plus a d2t table of
+ * absolute target ids.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named "device" must point to device memory of the current device;
+ *     "host" pointers to host memory.  The caller owns every buffer; the library keeps
+ *     no pointer after a call returns and allocates no device memory.
+ *   - Arrays are dense and row-major with the shapes given; element types are the
+ *     config's dtype for the tensors marked "dtype", int32 / fp32 otherwise.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) unless stated otherwise.
+ *   - Argument errors detectable on the host return before anything is launched and
+ *     leave every output untouched.  Problems only the device can see (an anchor
+ *     outside [0, V), a bounded wait that gave up) set a sticky error word in the
+ *     workspace; read it with dspark_device_status().
+ *   - dspark_last_error() returns a message for the calling thread's last failure.
+ */
+#ifndef DSPARK_H_
+#define DSPARK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dspark_status {
+  DSPARK_OK = 0,
+  DSPARK_ERR_INVALID_ARG = 1,  /* a NULL required pointer, a bad size, a bad flag */
+  DSPARK_ERR_UNSUPPORTED = 2,  /* valid in principle but outside what the kernels take */
+  DSPARK_ERR_WORKSPACE = 3,    /* workspace NULL, misaligned or too small */
+  DSPARK_ERR_CUDA = 4,         /* a CUDA runtime call failed (message has the details) */
+  DSPARK_ERR_DEVICE = 5,       /* a kernel saw bad data (e.g. an anchor outside [0, V)) */
+  DSPARK_ERR_TIMEOUT = 6       /* a bounded device-side wait gave up */
+} dspark_status;
+
+typedef enum dspark_dtype {
+  DSPARK_F32 = 0,   /* fp32 operands, fp32 FMA arithmetic */
+  DSPARK_BF16 = 1   /* bf16 operands, fp32 accumulation on the tensor cores */
+} dspark_dtype;
+
+/* Sizes and knobs of one call. */
+typedef struct dspark_config {
+  int32_t B;                  /* blocks in the batch, >= 1 */
+  int32_t L_in;               /* slots per block in `hidden`, >= 1 (>= 2 for 1+N) */
+  int32_t H;                  /* hidden size, >= 1 (multiple of 8 for bf16) */
+  int32_t V;                  /* vocabulary: token ids are in [0, V) */
+  int32_t r;                  /* Markov rank, >= 1 */
+  int32_t top_k;              /* candidates kept per slot, 1 .. min(32, V_head) */
+  int32_t sample_from_anchor; /* 1: anchor-first, N = L_in prediction slots reading
+                                 hidden rows 0..L_in-1;
+                                 0: 1+N bonus anchor, N = L_in - 1 slots reading
+                                 hidden rows 1..L_in-1 (row 0 is the bonus token) */
+  int32_t topk_markov;        /* 1: top-k ranks the corrected logits (the lattice
+                                 candidates get the Markov bias, lucebox PR #626);
+                                 0: top-k ranks the base logits */
+  float conf_min;             /* truncate at the first slot with conf < conf_min;
+                                 <= 0 disables truncation (n_draft = N) */
+  int32_t dtype;              /* dspark_dtype of hidden, lm_head, markov_w1/w2, w_conf */
+} dspark_config;
+
+/* The drafter head's weights (device memory, not modified). */
+typedef struct dspark_head {
+  const void* lm_head;        /* device [V_head, H], dtype */
+  const float* lm_bias;       /* device [V_head] fp32, or NULL.  A bias <= -1e8 marks a
+                                 row the draft cannot emit (never chosen while any
+                                 other row is finite) */
+  const int32_t* d2t;         /* device [V_head] int32, strictly increasing token ids in
+                                 [0, V): row j of lm_head / column j of markov_w2 is
+                                 token d2t[j].  NULL: row j is token j and V_head == V */
+  int32_t V_head;             /* rows of lm_head = columns of markov_w2 (multiple of 8
+                                 for bf16) */
+  const void* markov_w1;      /* device [V, r], dtype; row p is gathered for prev = p */
+  const void* markov_w2;      /* device [r, V_head], dtype */
+  const void* w_conf;         /* device [H], dtype, or NULL (no confidence head:
+                                 conf output is not written, n_draft = N) */
+  float b_conf;
+} dspark_head;
+
+/* Outputs of dspark_propose (device memory).  N = dspark_num_slots(cfg). */
+typedef struct dspark_outputs {
+  int32_t* draft;             /* required [B, N]: the greedy chain's tokens; all N slots
+                                 are filled, truncation only sets n_draft */
+  int32_t* n_draft;           /* required [B]: truncated draft length, 0..N */
+  int32_t* topk_ids;          /* [B, N, top_k] token ids by value descending, ties to
+                                 the lower id; or NULL */
+  float* topk_vals;           /* [B, N, top_k] the ranked logits of topk_ids; or NULL */
+  float* conf;                /* [B, N] confidences; or NULL */
+  float* logits;              /* [B, N, V_head] corrected logits (column j = head row
+                                 j); or NULL.  Costs a full write; meant for tests */
+} dspark_outputs;
+
+/* N, the prediction slots per block (L_in or L_in - 1); 0 on invalid input. */
+int32_t dspark_num_slots(const dspark_config* cfg);
+
+/* Bytes of device workspace dspark_propose needs for this config and head; 0 on
+   invalid input.  The workspace must be 256-byte aligned.  Its contents need no
+   initialisation and are scratch between calls; each call clears the error word that
+   dspark_device_status() reads, so that word describes the latest call. */
+size_t dspark_propose_workspace_size(const dspark_config* cfg, const dspark_head* head);
+
+/*
+ * dspark_propose -- the whole proposal of one batch.
+ *
+ * hidden  device [B, L_in, H] dtype: the drafter's final hidden states
+ * anchors device [B] int32: token 0 of every block (the dedicated anchor input of the
+ *         llama.cpp squash log; in the 1+N layout the bonus token), each in [0, V)
+ * out     the outputs above
+ *
+ * Steps, all on the device: (a) emittable-row handling from lm_bias / d2t;
+ * (b) base logits of every prediction slot over the head's rows; (c) the confidence
+ * head and the truncation length; (d) the Markov-corrected greedy chain over the N
+ * slots, vectorised over blocks; (e) top-k per slot.  Not reentrant on one workspace:
+ * calls that share a workspace must be ordered on the GPU.
+ */
+dspark_status dspark_propose(const dspark_config* cfg, const dspark_head* head,
+                             const void* hidden, const int32_t* anchors,
+                             const dspark_outputs* out,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dspark_verify -- DFlash's greedy verify/accept (unchanged by DSpark).
+ *
+ * draft    device [B, N] int32      n_draft device [B] int32 (values outside [0, N] are
+ *                                    clamped to that range)
+ * target   device [B, N + 1] int32: the target model's argmax after the anchor and after
+ *          each drafted slot
+ * accepted device [B] int32: a = the longest prefix j <= n_draft[b] with
+ *          draft[b, 0..j-1] == target[b, 0..j-1]
+ * bonus    device [B] int32: target[b, a]
+ * emitted  device [B, N + 1] int32 or NULL: draft[b, 0..a-1], then the bonus token, then
+ *          -1; with greedy decoding this equals the target's own argmax sequence.
+ */
+dspark_status dspark_verify(int32_t B, int32_t N, const int32_t* draft,
+                            const int32_t* n_draft, const int32_t* target,
+                            int32_t* accepted, int32_t* bonus, int32_t* emitted,
+                            void* stream);
+
+/* Stages of dspark_propose, in launch order, for dspark_propose_timed(). */
+enum {
+  DSPARK_STAGE_CONF = 0,    /* confidence head + truncation length */
+  DSPARK_STAGE_LOGITS = 1,  /* base logits of every prediction slot (the lm_head GEMM) */
+  DSPARK_STAGE_CHAIN = 2,   /* Markov-corrected greedy chain and per-slot candidates */
+  DSPARK_STAGE_TOPK = 3,    /* final top-k ordering */
+  DSPARK_NUM_STAGES = 4
+};
+
+/* dspark_propose that also records events[s] (cudaEvent_t, created by the caller) on
+   `stream` as stage s begins, and events[DSPARK_NUM_STAGES] after the last stage.
+   A stage with no kernel for this config records its event right before the next
+   one's.  The work done is identical to dspark_propose's. */
+dspark_status dspark_propose_timed(const dspark_config* cfg, const dspark_head* head,
+                                   const void* hidden, const int32_t* anchors,
+                                   const dspark_outputs* out, void* workspace,
+                                   size_t workspace_bytes, void* stream,
+                                   void* const* events);
+
+/* Number of kernels one dspark_propose call launches for this config and head (the
+   workspace reset is a memset node, not counted); -1 on invalid input. */
+int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head* head);
+
+/* Bytes of device workspace dspark_step_host needs: dspark_propose's plus staging for
+   the host inputs and outputs.  256-byte aligned; 0 on invalid input. */
+size_t dspark_step_host_workspace_size(const dspark_config* cfg, const dspark_head* head);
+
+/*
+ * dspark_step_host -- one draft step from and to HOST memory: copies hidden, anchors
+ * and target in, runs dspark_propose and dspark_verify, copies the results out.
+ *
+ * hidden_h  host [B, L_in, H] dtype      anchors_h host [B] int32
+ * target_h  host [B, N + 1] int32 (the target's argmax tokens for the verify step)
+ * draft_h   host [B, N] int32            n_draft_h host [B] int32
+ * accepted_h, bonus_h host [B] int32
+ * topk_ids_h / topk_vals_h host [B, N, top_k] or NULL
+ *
+ * All copies are cudaMemcpyAsync on `stream`; for them to overlap, the host buffers
+ * should be page-locked.  The call returns once everything is queued: synchronise
+ * `stream` before reading the outputs.
+ */
+dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head,
+                               const void* hidden_h, const int32_t* anchors_h,
+                               const int32_t* target_h, int32_t* draft_h,
+                               int32_t* n_draft_h, int32_t* accepted_h, int32_t* bonus_h,
+                               int32_t* topk_ids_h, float* topk_vals_h,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, reads the sticky device error word of a workspace used by
+   dspark_propose, and clears it.  DSPARK_OK when no kernel flagged anything. */
+dspark_status dspark_device_status(void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* dspark_status_string(int32_t status);
+
+/* Message describing the calling thread's most recent failed call ("" if none). */
+const char* dspark_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H_ */

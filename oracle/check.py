@@ -63,7 +63,7 @@ def check_propose(oracle_out: dict, *, anchors, markov_w1, markov_w2, top_k: int
                 fail(f"draft[{b},{i}]={g} out of range")
                 break
             best = argmax_lowest(zc)
-            top2 = np.sort(zc)[-2:] if V >= 2 else np.array([zc[0], -np.inf])
+            top2 = np.partition(zc, V - 2)[-2:] if V >= 2 else np.array([-np.inf, zc[0]])
             margin = top2[1] - top2[0]
             if margin > tol:
                 if g != best:

@@ -70,7 +70,7 @@ def block_layout(L_in: int, sample_from_anchor: bool) -> tuple[int, int]:
 
 
 def base_logits(hidden, lm_head, lm_bias, i_first_pred: int, N: int,
-                chunk: int = 16384) -> np.ndarray:
+                chunk: int = 8192) -> np.ndarray:
     """logits(i) = h[b, i_first_pred + i] . lm_head^T (+ lm_bias), shape [B, N, V].
 
     [dflash-log], the proposal formula: logits(i) is the plain lm_head projection of
@@ -83,11 +83,18 @@ def base_logits(hidden, lm_head, lm_bias, i_first_pred: int, N: int,
     h = upcast(hidden)                                   # [B, L_in, H]
     B, _, H = h.shape
     rows = h[:, i_first_pred:i_first_pred + N, :].reshape(B * N, H)
-    V = np.asarray(lm_head).shape[0]
+    lm_head = np.asarray(lm_head)
+    V = lm_head.shape[0]
     z = np.empty((B * N, V), np.float64)
+    wbuf = np.empty((min(chunk, V), H), np.float64)     # reused: avoids page faults
     for v0 in range(0, V, chunk):
         v1 = min(V, v0 + chunk)
-        z[:, v0:v1] = rows @ upcast(lm_head[v0:v1]).T
+        w = wbuf[:v1 - v0]
+        if lm_head.dtype == np.uint16:
+            w[...] = np.left_shift(lm_head[v0:v1], 16, dtype=np.uint32).view(np.float32)
+        else:
+            w[...] = lm_head[v0:v1]
+        z[:, v0:v1] = rows @ w.T
     if lm_bias is not None:
         z += upcast(lm_bias)[None, :]
     return z.reshape(B, N, V)
@@ -121,9 +128,15 @@ def topk_sorted(row: np.ndarray, k: int) -> np.ndarray:
     [ort-pr]: dspark_top_k is the number of candidates the lattice keeps per block
     slot; the order is this oracle's reading.
     """
-    idx = np.arange(row.shape[-1])
-    order = np.lexsort((idx, -row))
-    return order[:k]
+    n = row.shape[-1]
+    if k < n:
+        # every member of the top k is >= the k-th largest value; sort only those
+        kth = np.partition(row, n - k)[n - k]
+        cand = np.flatnonzero(row >= kth)
+    else:
+        cand = np.arange(n)
+    order = np.lexsort((cand, -row[cand]))
+    return cand[order[:k]]
 
 
 def confidence(hidden, w_conf, b_conf: float, i_first_pred: int, N: int) -> np.ndarray:

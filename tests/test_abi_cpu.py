@@ -1,0 +1,115 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and its
+host-side validation answers with status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dspark_block_drafter_gb300 as ds
+from dspark_block_drafter_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(dspark_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_abi.LIB_PATH):
+        from dspark_block_drafter_gb300 import build
+        build.build()
+    return ds.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert "dspark_propose" in names and "dspark_verify" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+        assert n in _abi.SIGNATURES, f"{n} has no Python binding"
+
+
+def _cfg(**kw):
+    c = dict(B=2, L_in=4, H=64, V=1000, r=8, top_k=4, sample_from_anchor=1, topk_markov=1,
+             conf_min=0.0, dtype=_abi.DSPARK_F32)
+    c.update(kw)
+    return _abi.dspark_config(**c)
+
+
+def _head(**kw):
+    h = dict(lm_head=0x1000, lm_bias=None, d2t=None, V_head=1000, markov_w1=0x2000,
+             markov_w2=0x3000, w_conf=None, b_conf=0.0)
+    h.update(kw)
+    return _abi.dspark_head(**h)
+
+
+def test_num_slots(lib):
+    assert ds.dspark_num_slots(_cfg(L_in=7, sample_from_anchor=1)) == 7
+    assert ds.dspark_num_slots(_cfg(L_in=7, sample_from_anchor=0)) == 6
+    assert ds.dspark_num_slots(_cfg(L_in=1, sample_from_anchor=0)) == 0
+
+
+def test_workspace_size_and_validation(lib):
+    n = ds.dspark_propose_workspace_size(_cfg(), _head())
+    assert n > 0 and n % 256 == 0
+    # the workspace holds at least the fp32 base logits of every prediction slot
+    assert n >= 4 * 2 * 4 * 1000
+    bad = [
+        _cfg(B=0), _cfg(top_k=0), _cfg(top_k=33), _cfg(L_in=1, sample_from_anchor=0),
+        _cfg(dtype=7), _cfg(sample_from_anchor=2), _cfg(conf_min=float("nan")),
+    ]
+    for c in bad:
+        assert ds.dspark_propose_workspace_size(c, _head()) == 0
+    assert ds.dspark_propose_workspace_size(_cfg(), _head(V_head=999)) == 0   # no d2t
+    assert ds.dspark_propose_workspace_size(_cfg(), _head(lm_head=None)) == 0
+    assert ds.dspark_propose_workspace_size(_cfg(top_k=5), _head(V_head=4, d2t=0x10)) == 0
+    # bf16 alignment / size rules
+    assert ds.dspark_propose_workspace_size(_cfg(dtype=1, H=60), _head()) == 0
+    assert ds.dspark_propose_workspace_size(_cfg(dtype=1), _head(lm_head=0x1002)) == 0
+    assert ds.dspark_propose_workspace_size(_cfg(dtype=1), _head()) > 0
+
+
+def test_propose_rejects_before_launch(lib):
+    out = _abi.dspark_outputs(draft=0x100, n_draft=0x200)
+    cfg, head = _cfg(), _head()
+    need = ds.dspark_propose_workspace_size(cfg, head)
+    st = ds.dspark_propose(cfg, head, 0x4000, 0x5000, out, 0x10000, need - 1, 0)
+    assert st == _abi.DSPARK_ERR_WORKSPACE
+    assert "too small" in ds.dspark_last_error()
+    st = ds.dspark_propose(cfg, head, 0x4000, 0x5000, out, 0x10010, need, 0)
+    assert st == _abi.DSPARK_ERR_WORKSPACE                      # misaligned
+    st = ds.dspark_propose(cfg, head, None, 0x5000, out, 0x10000, need, 0)
+    assert st == _abi.DSPARK_ERR_INVALID_ARG
+    st = ds.dspark_propose(cfg, head, 0x4000, 0x5000, _abi.dspark_outputs(draft=0x100),
+                           0x10000, need, 0)
+    assert st == _abi.DSPARK_ERR_INVALID_ARG
+    st = ds.dspark_propose(_cfg(B=-1), head, 0x4000, 0x5000, out, 0x10000, need, 0)
+    assert st == _abi.DSPARK_ERR_INVALID_ARG
+
+
+def test_verify_rejects_before_launch(lib):
+    assert ds.dspark_verify(0, 4, 1, 1, 1, 1, 1, None, 0) == _abi.DSPARK_ERR_INVALID_ARG
+    assert ds.dspark_verify(2, 4, None, 1, 1, 1, 1, None, 0) == _abi.DSPARK_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert ds.dspark_status_string(s)
+    assert ds.dspark_status_string(99) == "unknown status"
+
+
+def test_struct_layouts_match_c():
+    # pointer-sized fields are 8 bytes on both hosts; the int/float fields pack as in C
+    assert ctypes.sizeof(_abi.dspark_config) == 40
+    assert ctypes.sizeof(_abi.dspark_head) == 64
+    assert ctypes.sizeof(_abi.dspark_outputs) == 48

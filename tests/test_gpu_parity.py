@@ -1,0 +1,131 @@
+"""GPU path (through the C ABI) against the oracle on the same seeded inputs.
+
+Small cases span several tiles and a ragged vocabulary tail; the five named workloads
+run at their full sizes.
+"""
+import numpy as np
+import pytest
+
+from workloads import WORKLOADS, Workload, make_batch, make_head
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from gpu_cases import TOL, compare, gpu_propose, oracle_run, run_case  # noqa: E402
+
+
+def _small(**kw):
+    base = dict(name="small", B=3, L_in=5, H=200, V=1000, r=24, top_k=5,
+                sample_from_anchor=True, conf_min=0.5, dtype="bf16", weight_std=0.2,
+                conf_std=0.05, seed=4242)
+    base.update(kw)
+    return Workload(**base)
+
+
+def test_tiny_fp32_workload():
+    g, o, rep = run_case(WORKLOADS["tiny_fp32"])
+    assert rep["slots"] == 8
+
+
+@pytest.mark.parametrize("sfa", [True, False])
+@pytest.mark.parametrize("topk_markov", [True, False])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_small_dense(sfa, topk_markov, dtype):
+    run_case(_small(sample_from_anchor=sfa, topk_markov=topk_markov, dtype=dtype))
+
+
+@pytest.mark.parametrize("form", ["full", "d2t"])
+@pytest.mark.parametrize("sfa", [True, False])
+def test_small_reduced_vocab(form, sfa):
+    wl = _small(n_emit=304, sample_from_anchor=sfa, V=1024)
+    g, o, rep = run_case(wl, form)
+    emit = set(make_head(wl)["emit_rows"].tolist())
+    assert set(g["draft"].ravel().tolist()) <= emit
+    assert set(g["topk_ids"].ravel().tolist()) <= emit
+
+
+def test_single_block_single_slot():
+    run_case(_small(B=1, L_in=1, top_k=3))
+
+
+def test_topk_equals_head_rows():
+    # k = V_head: every row is a candidate; ragged tiny vocabulary
+    wl = _small(V=1000, n_emit=32, top_k=32, L_in=3)
+    run_case(wl, "d2t")
+
+
+def test_large_rank_and_many_blocks():
+    run_case(_small(B=40, L_in=3, r=300, H=136, V=520, top_k=2))
+
+
+def test_anchor_is_last_token():
+    wl = _small()
+    hd, bt = make_head(wl), make_batch(wl)
+    bt["anchors"][:] = wl.V - 1
+    run_case(wl, hd=hd, bt=bt)
+
+
+def test_confidence_at_threshold_keeps_slot():
+    # w_conf = 0, b_conf = 0 gives conf = 0.5 exactly on both sides
+    wl = _small(conf_min=0.5)
+    hd, bt = make_head(wl), make_batch(wl)
+    hd["w_conf"] = np.zeros_like(hd["w_conf"])
+    g, o, rep = run_case(wl, hd=hd, bt=bt)
+    assert np.all(g["conf"] == 0.5)
+    assert np.all(g["n_draft"] == wl.N)
+
+
+def test_truncation_everywhere():
+    # strong confidence head: truncation lands on many different slots
+    wl = _small(B=24, L_in=8, conf_std=0.3, conf_min=0.5)
+    g, o, rep = run_case(wl)
+    assert len(set(g["n_draft"].tolist())) > 2
+
+
+def test_zero_markov_is_plain_argmax():
+    wl = _small()
+    hd, bt = make_head(wl), make_batch(wl)
+    hd["markov_w1"] = np.zeros_like(hd["markov_w1"])
+    g, o, rep = run_case(wl, hd=hd, bt=bt)
+
+
+def test_bad_anchor_sets_device_status():
+    import dspark_block_drafter_gb300 as ds
+    from dspark_block_drafter_gb300 import torch_io as tio
+    wl = _small()
+    hd, bt = make_head(wl), make_batch(wl)
+    bt["anchors"][1] = wl.V + 5
+    cfg = tio.make_config(wl.B, wl.L_in, wl.H, wl.V, wl.r, wl.top_k, True, wl.conf_min, "bf16")
+    head = tio.head_to_device(hd)
+    out = tio.Outputs.allocate(wl.B, wl.N, wl.top_k, wl.V)
+    ws = tio.workspace_for(cfg, head)
+    tio.propose(cfg, head, tio.to_device(bt["hidden"]), tio.to_device(bt["anchors"]), out, ws)
+    assert tio.device_status(ws) == ds._abi.DSPARK_ERR_DEVICE
+    assert tio.device_status(ws) == 0          # the word is cleared once read
+
+
+def test_repeat_calls_same_workspace_identical():
+    wl = _small()
+    hd, bt = make_head(wl), make_batch(wl)
+    g1, ws = gpu_propose(wl, hd, bt)
+    g2, _ = gpu_propose(wl, hd, bt)
+    for k in ("draft", "topk_ids", "n_draft"):
+        assert np.array_equal(g1[k], g2[k])
+    assert np.array_equal(g1["topk_vals"], g2["topk_vals"])
+
+
+# ------------------------------------------------------------------ full sizes
+@pytest.mark.parametrize("name", ["qwen3_8b_b1", "qwen3_8b_b32", "qwen38_27b_b8",
+                                  "gemma4_bonus_b64"])
+def test_full_size_workload(name):
+    wl = WORKLOADS[name]
+    hd, bt = make_head(wl), make_batch(wl)
+    forms = ["full", "d2t"] if wl.n_emit else ["full"]
+    o = oracle_run(wl, hd, bt)
+    for form in forms:
+        g, _ = gpu_propose(wl, hd, bt, form)
+        rep = compare(wl, hd, bt, o, g, form)
+        assert rep["failures"] == [], (form, rep)
