@@ -332,7 +332,8 @@ def run_ours(args):
                      "frac": achieved / peak_tf, "traffic": None,
                      "peak_source": f"{peaks['_source']} bf16 burst"},
         "e2e": e2e,
-        "gpu_launches": K * (_abi.dspark_propose_kernel_count(cfg, head.struct()) + 1),
+        "gpu_launches": K * (_abi.dspark_propose_kernel_count(cfg, head.struct(),
+                                                              out.struct()) + 1),
         "clocks": clk,
         "wall_s_timed_region": t_wall,
     }

@@ -65,7 +65,8 @@ SIGNATURES = {
                                      ctypes.POINTER(dspark_outputs), c_ptr, ctypes.c_size_t,
                                      c_ptr, ctypes.POINTER(c_ptr)]),
     "dspark_propose_kernel_count": (c_i32, [ctypes.POINTER(dspark_config),
-                                            ctypes.POINTER(dspark_head)]),
+                                            ctypes.POINTER(dspark_head),
+                                            ctypes.POINTER(dspark_outputs)]),
     "dspark_step_host_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(dspark_config),
                                                           ctypes.POINTER(dspark_head)]),
     "dspark_step_host": (c_i32, [ctypes.POINTER(dspark_config), ctypes.POINTER(dspark_head),
@@ -131,8 +132,10 @@ def dspark_propose_timed(cfg: dspark_config, head: dspark_head, hidden: int, anc
                                       arr)
 
 
-def dspark_propose_kernel_count(cfg: dspark_config, head: dspark_head) -> int:
-    return lib().dspark_propose_kernel_count(ctypes.byref(cfg), ctypes.byref(head))
+def dspark_propose_kernel_count(cfg: dspark_config, head: dspark_head,
+                                out: dspark_outputs) -> int:
+    return lib().dspark_propose_kernel_count(ctypes.byref(cfg), ctypes.byref(head),
+                                             ctypes.byref(out))
 
 
 def dspark_step_host_workspace_size(cfg: dspark_config, head: dspark_head) -> int:

@@ -22,22 +22,29 @@ static dspark_status cuda_fail(cudaError_t e, const char* where) {
 }
 
 static constexpr size_t kAlign = 256;
-static constexpr size_t kCtrlBytes = 4096;
 
-WorkspaceLayout plan_workspace(int B, int N, int Vh) {
+WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype) {
   WorkspaceLayout w{};
   w.ldz = align_up((size_t)Vh, 64);
   size_t off = 0;
-  w.ctrl = off;
-  off += kCtrlBytes;
-  w.z = off;
-  off = align_up(off + sizeof(float) * (size_t)N * B * w.ldz, kAlign);
-  w.zc = off;
-  off = align_up(off + sizeof(float) * (size_t)B * w.ldz, kAlign);
-  w.prev = off;
-  off = align_up(off + sizeof(int32_t) * (size_t)B, kAlign);
-  w.conf = off;
-  off = align_up(off + sizeof(float) * (size_t)B * N, kAlign);
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  w.ctrl = take(256);
+  w.bar = take(sizeof(unsigned) * (size_t)((B + 63) / 64));
+  w.keys = take(sizeof(unsigned long long) * (size_t)N * B);
+  w.zero_end = off;
+  w.z = take(sizeof(float) * (size_t)N * B * w.ldz);
+  if (dtype == DSPARK_F32) {          // the CUDA-core chain keeps one corrected row per block
+    w.zc = take(sizeof(float) * (size_t)B * w.ldz);
+    w.prev = take(sizeof(int32_t) * (size_t)B);
+  } else {                            // the tensor-core chain keeps per-CTA top-k partials
+    w.part_val = take(sizeof(float) * (size_t)N * B * kChainMaxCtas * k);
+    w.part_id = take(sizeof(int32_t) * (size_t)N * B * kChainMaxCtas * k);
+  }
+  w.conf = take(sizeof(float) * (size_t)B * N);
   w.total = off;
   return w;
 }
@@ -80,6 +87,10 @@ static dspark_status validate(const dspark_config* c, const dspark_head* h, int*
     if (!aligned(h->lm_head, 16) || !aligned(h->markov_w2, 16) || !aligned(h->markov_w1, 16))
       return fail(DSPARK_ERR_INVALID_ARG, "bf16 weights must be 16-byte aligned");
   }
+  if (c->dtype == DSPARK_BF16 && (c->sample_from_anchor ? c->L_in : c->L_in - 1) > 256)
+    return fail(DSPARK_ERR_UNSUPPORTED, "bf16 path takes at most 256 prediction slots");
+  if (c->dtype == DSPARK_BF16 && c->r > 512)
+    return fail(DSPARK_ERR_UNSUPPORTED, "bf16 path takes a Markov rank of at most 512");
   *N = c->sample_from_anchor ? c->L_in : c->L_in - 1;
   *ifp = c->sample_from_anchor ? 0 : 1;
   return DSPARK_OK;
@@ -104,7 +115,7 @@ int32_t dspark_num_slots(const dspark_config* cfg) {
 size_t dspark_propose_workspace_size(const dspark_config* cfg, const dspark_head* head) {
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return 0;
-  return plan_workspace(cfg->B, N, head->V_head).total;
+  return plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype).total;
 }
 
 static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* head,
@@ -120,7 +131,7 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
     return fail(DSPARK_ERR_INVALID_ARG, "outputs draft and n_draft are required");
   if (cfg->dtype == DSPARK_BF16 && !aligned(hidden, 16))
     return fail(DSPARK_ERR_INVALID_ARG, "bf16 hidden must be 16-byte aligned");
-  WorkspaceLayout wl = plan_workspace(cfg->B, N, head->V_head);
+  WorkspaceLayout wl = plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype);
   if (!workspace || !aligned(workspace, 256))
     return fail(DSPARK_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
   if (workspace_bytes < wl.total)
@@ -139,10 +150,14 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   p.topk_vals = out->topk_vals; p.conf = head->w_conf ? out->conf : nullptr;
   p.logits = out->logits;
   p.ctrl = (uint32_t*)(ws + wl.ctrl);
+  p.bar = (unsigned*)(ws + wl.bar);
+  p.keys = (unsigned long long*)(ws + wl.keys);
   p.z = (float*)(ws + wl.z);
   p.ldz = wl.ldz;
   p.zc = (float*)(ws + wl.zc);
   p.prev = (int32_t*)(ws + wl.prev);
+  p.part_val = (float*)(ws + wl.part_val);
+  p.part_id = (int32_t*)(ws + wl.part_id);
   p.conf_ws = (float*)(ws + wl.conf);
   p.stream = (cudaStream_t)stream;
 
@@ -150,15 +165,17 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   auto mark = [&](int s) -> cudaError_t {
     return events ? cudaEventRecord((cudaEvent_t)events[s], p.stream) : cudaSuccess;
   };
-  // the control block (error word included) starts from zero on every call
-  e = cudaMemsetAsync(ws + wl.ctrl, 0, kCtrlBytes, p.stream);
+  // the control words (error word, barrier counters, winner keys) start from zero
+  e = cudaMemsetAsync(ws + wl.ctrl, 0, wl.zero_end - wl.ctrl, p.stream);
   if (e != cudaSuccess) return cuda_fail(e, "control reset");
   if ((e = mark(DSPARK_STAGE_CONF)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = launch_conf(p)) != cudaSuccess) return cuda_fail(e, "confidence kernel");
   if ((e = mark(DSPARK_STAGE_LOGITS)) != cudaSuccess) return cuda_fail(e, "event record");
-  if ((e = launch_base_logits_simt(p)) != cudaSuccess) return cuda_fail(e, "base logits");
+  e = p.dtype == DSPARK_BF16 ? launch_base_logits_tc(p) : launch_base_logits_simt(p);
+  if (e != cudaSuccess) return cuda_fail(e, "base logits");
   if ((e = mark(DSPARK_STAGE_CHAIN)) != cudaSuccess) return cuda_fail(e, "event record");
-  if ((e = launch_chain_simt(p)) != cudaSuccess) return cuda_fail(e, "chain");
+  e = p.dtype == DSPARK_BF16 ? launch_chain_tc(p) : launch_chain_simt(p);
+  if (e != cudaSuccess) return cuda_fail(e, "chain");
   if ((e = mark(DSPARK_STAGE_TOPK)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = mark(DSPARK_NUM_STAGES)) != cudaSuccess) return cuda_fail(e, "event record");
   return DSPARK_OK;
@@ -184,10 +201,13 @@ dspark_status dspark_propose_timed(const dspark_config* cfg, const dspark_head* 
                       events);
 }
 
-int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head* head) {
+int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head* head,
+                                    const dspark_outputs* out) {
   int N, ifp;
-  if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return -1;
-  return 1 /* confidence */ + 1 /* base logits */ + 2 * N /* chain steps */;
+  if (validate(cfg, head, &N, &ifp) != DSPARK_OK || !out) return -1;
+  if (cfg->dtype == DSPARK_F32) return 1 + 1 + 2 * N;   // confidence, GEMM, 2 per slot
+  const bool topk = out->topk_ids || out->topk_vals;
+  return 1 /* confidence */ + 1 /* GEMM */ + (cfg->B + 63) / 64 /* chain */ + (topk ? 1 : 0);
 }
 
 // staging for dspark_step_host, placed after dspark_propose's workspace
@@ -215,7 +235,8 @@ static StageLayout plan_stage(const dspark_config* c, int N, size_t base) {
 size_t dspark_step_host_workspace_size(const dspark_config* cfg, const dspark_head* head) {
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return 0;
-  return plan_stage(cfg, N, plan_workspace(cfg->B, N, head->V_head).total).total;
+  return plan_stage(cfg, N, plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype).total)
+      .total;
 }
 
 dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head,
@@ -229,7 +250,7 @@ dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head
   if (st != DSPARK_OK) return st;
   if (!hidden_h || !anchors_h || !target_h || !draft_h || !n_draft_h || !accepted_h || !bonus_h)
     return fail(DSPARK_ERR_INVALID_ARG, "a required host buffer is NULL");
-  size_t base = plan_workspace(cfg->B, N, head->V_head).total;
+  size_t base = plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype).total;
   StageLayout s = plan_stage(cfg, N, base);
   if (!workspace || !aligned(workspace, 256))
     return fail(DSPARK_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");

@@ -1,0 +1,309 @@
+// Base logits on the 5th-generation tensor cores (bf16 in, fp32 accumulate in TMEM).
+//
+//   z[i][b][v] = sum_h hidden[b, ifp + i, h] * lm_head[v, h] + lm_bias[v]
+//
+// (llama.cpp commit 6fed9f6, "spec: add DSpark speculative decoding": logits(i) of the
+// proposal formula.)  The GEMM runs "swap-AB": the MMA's M dimension is the vocabulary
+// (128 head rows per tile), its N dimension the prediction rows of whole blocks
+// (BB blocks x N slots, up to 256), so a small batch still fills the instruction.
+//
+// One persistent CTA per SM, warp-specialised:
+//   warp 4      TMA producer: lm_head tile [128 x 64] and hidden tile [BB, N, 64] per
+//               K-block into a ring of shared-memory stages (128-byte swizzle)
+//   warp 5      MMA issuer: 4 x tcgen05.mma (K = 16) per stage into a TMEM accumulator;
+//               tcgen05.commit frees the stage, and the accumulator when the tile ends
+//   warps 0-3   epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 head rows), + bias,
+//               coalesced fp32 stores of z (consecutive lanes = consecutive v)
+// Two TMEM accumulators alternate so that the epilogue of one tile overlaps the MMAs of
+// the next.  Tiles are ordered vocabulary-major: CTAs that run side by side share the
+// same lm_head tile through L2, so lm_head streams from HBM once.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kBlockV = 128;      // MMA M: head rows per tile
+constexpr int kBlockK = 64;       // one 128-byte swizzle row of bf16
+constexpr uint32_t kStageA = kBlockV * kBlockK * 2;   // 16 KB
+constexpr int kThreads = 192;
+constexpr long long kWaitBudget = 2000000000ll;       // ~1 s of SM clocks
+
+struct GemmArgs {
+  float* z;
+  size_t ldz;
+  const float* bias;
+  uint32_t* err;
+  int B, N, ifp, Vh;
+  int BB;          // blocks per N-tile
+  int bn_mma;      // MMA N (rows of the B operand per stage), multiple of 16
+  int acc_stride;  // TMEM columns between the two accumulators (multiple of 32)
+  int n_tiles, v_tiles, num_kb, stages;
+  uint32_t tmem_cols;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
+               const __grid_constant__ CUtensorMap tm_h, const GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t b_stage = (uint32_t)g.bn_mma * kBlockK * 2;
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + (size_t)g.stages * kStageA;
+  uint64_t* full = (uint64_t*)(sB + (size_t)g.stages * b_stage);
+  uint64_t* empty = full + g.stages;
+  uint64_t* acc_full = empty + g.stages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = (uint32_t*)(drain + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < g.stages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&acc_full[a], 1);
+      ptx::mbar_init(&acc_empty[a], 128);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 4 && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_w);
+    ptx::tma_prefetch_desc(&tm_h);
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(tmem_slot, g.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int num_tiles = g.v_tiles * g.n_tiles;
+
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    flag_error(g.err, kErrTimeout);
+  };
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint32_t tx = kStageA + (uint32_t)(g.BB * g.N) * kBlockK * 2;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int vt = tile / g.n_tiles, nt = tile % g.n_tiles;
+        for (int kb = 0; kb < g.num_kb; ++kb, ++it) {
+          const uint32_t s = it % g.stages, ph = (it / g.stages) & 1;
+          if (!ptx::mbar_wait(&empty[s], ph ^ 1, kWaitBudget, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&full[s], tx);
+          ptx::tma_load_2d(sA + (size_t)s * kStageA, &tm_w, &full[s], kb * kBlockK,
+                           vt * kBlockV);
+          ptx::tma_load_3d(sB + (size_t)s * b_stage, &tm_h, &full[s], kb * kBlockK, g.ifp,
+                           nt * g.BB);
+        }
+      }
+      if (!ok) {
+        give_up();
+        // let the copies already issued land before the CTA can exit
+        const uint32_t first = it > (uint32_t)g.stages ? it - g.stages : 0;
+        for (uint32_t j = first; j < it; ++j)
+          ptx::mbar_wait(&full[j % g.stages], (j / g.stages) & 1, kWaitBudget, nullptr);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+        const int nt = tile % g.n_tiles;
+        const int rows = min(g.BB, g.B - nt * g.BB) * g.N;
+        const int n_mma = (rows + 15) / 16 * 16;
+        const uint32_t idesc = ptx::idesc_bf16_f32(kBlockV, n_mma, 0, 0);
+        const uint32_t acc = local & 1, aph = (local >> 1) & 1;
+        if (!ptx::mbar_wait(&acc_empty[acc], aph ^ 1, kWaitBudget, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * (uint32_t)g.acc_stride;
+        for (int kb = 0; kb < g.num_kb; ++kb, ++it) {
+          const uint32_t s = it % g.stages, ph = (it / g.stages) & 1;
+          if (!ptx::mbar_wait(&full[s], ph, kWaitBudget, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_u32(sA + (size_t)s * kStageA);
+          const uint32_t b0 = ptx::smem_u32(sB + (size_t)s * b_stage);
+#pragma unroll
+          for (int k = 0; k < kBlockK / 16; ++k)
+            ptx::mma_f16(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
+                         ptx::desc_kmajor_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+          ptx::mma_commit(&empty[s]);
+        }
+        if (ok) ptx::mma_commit(&acc_full[acc]);
+      }
+      if (!ok) give_up();
+      // every MMA issued has finished once this commit lands
+      ptx::mma_commit(drain);
+      ptx::mbar_wait(drain, 0, kWaitBudget, nullptr);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    uint32_t local = 0;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int vt = tile / g.n_tiles, nt = tile % g.n_tiles;
+      const int rows = min(g.BB, g.B - nt * g.BB) * g.N;
+      const uint32_t acc = local & 1, aph = (local >> 1) & 1;
+      // the warp leaves together: tcgen05.ld below is a warp-collective instruction
+      const bool ok = __all_sync(0xFFFFFFFFu,
+                                 ptx::mbar_wait(&acc_full[acc], aph, kWaitBudget, abort_flag));
+      if (!ok) {
+        give_up();
+        break;
+      }
+      ptx::tc_fence_after();
+      const int v = vt * kBlockV + warp * 32 + lane;
+      const bool live = v < g.Vh;
+      const float bias_v = (g.bias && live) ? g.bias[v] : 0.f;
+      const int b_first = nt * g.BB;
+      for (int c0 = 0; c0 < rows; c0 += 32) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(tmem + lane_base + acc * (uint32_t)g.acc_stride + c0, r);
+        ptx::tmem_ld_wait();
+        int bl = c0 / g.N, il = c0 % g.N;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (live && c0 + j < rows)
+            g.z[((size_t)il * g.B + b_first + bl) * g.ldz + v] = __uint_as_float(r[j]) + bias_v;
+          if (++il == g.N) { il = 0; ++bl; }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&acc_empty[acc]);
+    }
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, g.tmem_cols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  });
+  return fn;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+// Tile plan of the lm_head GEMM for B blocks of N prediction slots.
+GemmTilePlan plan_logits_gemm(int B, int N) {
+  GemmTilePlan t{};
+  const int bb_max = 256 / N;
+  t.n_tiles = (B + bb_max - 1) / bb_max;
+  t.BB = (B + t.n_tiles - 1) / t.n_tiles;
+  t.bn_mma = (t.BB * N + 15) / 16 * 16;
+  return t;
+}
+
+cudaError_t launch_base_logits_tc(const ProposePlan& p) {
+  auto encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  const GemmTilePlan tp = plan_logits_gemm(p.B, p.N);
+  GemmArgs g{};
+  g.z = p.z;
+  g.ldz = p.ldz;
+  g.bias = p.lm_bias;
+  g.err = p.ctrl;
+  g.B = p.B;
+  g.N = p.N;
+  g.ifp = p.ifp;
+  g.Vh = p.Vh;
+  g.BB = tp.BB;
+  g.bn_mma = tp.bn_mma;
+  g.n_tiles = tp.n_tiles;
+  g.v_tiles = (p.Vh + kBlockV - 1) / kBlockV;
+  g.num_kb = (p.H + kBlockK - 1) / kBlockK;
+  const uint32_t stage_bytes = kStageA + (uint32_t)g.bn_mma * kBlockK * 2;
+  const size_t smem_budget = 220 * 1024;
+  g.stages = (int)std::min<size_t>(8, (smem_budget - 1024 - 256) / stage_bytes);
+  // 32-column TMEM loads may run past the last valid column of an accumulator, so
+  // each accumulator owns a multiple of 32 columns
+  g.acc_stride = (g.bn_mma + 31) / 32 * 32;
+  uint32_t cols = 32;
+  while (cols < 2u * (uint32_t)g.acc_stride) cols <<= 1;
+  g.tmem_cols = cols;
+  const size_t smem = 1024 + (size_t)g.stages * stage_bytes + 256;
+
+  CUtensorMap tm_w, tm_h;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)p.H, (cuuint64_t)p.Vh};
+    cuuint64_t strides[1] = {(cuuint64_t)p.H * 2};
+    cuuint32_t box[2] = {kBlockK, kBlockV};
+    cuuint32_t es[2] = {1, 1};
+    if (encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)p.lm_head, dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)p.H, (cuuint64_t)p.L_in, (cuuint64_t)p.B};
+    cuuint64_t strides[2] = {(cuuint64_t)p.H * 2, (cuuint64_t)p.L_in * p.H * 2};
+    cuuint32_t box[3] = {kBlockK, (cuuint32_t)p.N, (cuuint32_t)g.BB};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)p.hidden, dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(logits_gemm_tc,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = g.v_tiles * g.n_tiles;
+  const int grid = std::min(tiles, sm_count());
+  logits_gemm_tc<<<grid, kThreads, smem, p.stream>>>(tm_w, tm_h, g);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

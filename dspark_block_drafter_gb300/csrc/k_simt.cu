@@ -1,6 +1,6 @@
-// CUDA-core (FMA) kernels of the proposal: base logits, and the Markov-corrected
-// greedy chain one slot at a time.  These carry the fp32 operand type; every sum is
-// accumulated in fp32.
+// CUDA-core (FMA) kernels of the proposal: base logits of the fp32 operand type, and
+// the Markov-corrected greedy chain one slot at a time.  Every sum is accumulated in
+// fp32.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -187,7 +187,7 @@ cudaError_t chain_t(const ProposePlan& p) {
 }  // namespace
 
 cudaError_t launch_base_logits_simt(const ProposePlan& p) {
-  return p.dtype == 0 ? base_logits_t<float>(p) : base_logits_t<__nv_bfloat16>(p);
+  return base_logits_t<float>(p);   // the bf16 operand type runs on the tensor cores
 }
 
 cudaError_t launch_chain_simt(const ProposePlan& p) {

@@ -29,7 +29,11 @@ struct ProposePlan {
   float* conf;
   float* logits;
   // workspace pieces
-  uint32_t* ctrl;       // [0] = error word, the rest control words of the chain
+  uint32_t* ctrl;       // [0] = error word
+  unsigned int* bar;    // grid-barrier counters of the chain, one per group of 64 blocks
+  unsigned long long* keys;  // [N][B] order keys of each slot's winner
+  float* part_val;      // [N][B][kChainMaxCtas][k] per-CTA top-k partials
+  int32_t* part_id;
   float* z;             // base logits [N][B][ldz]
   size_t ldz;
   float* zc;            // corrected logits of the current slot [B][ldz]
@@ -38,16 +42,29 @@ struct ProposePlan {
   cudaStream_t stream;
 };
 
-// Workspace carve-up shared by the size query and the launch.
+// Upper bound on the chain kernel's grid (one CTA per SM).
+constexpr int kChainMaxCtas = 256;
+
+// Workspace carve-up shared by the size query and the launch.  [ctrl, zero_end) is
+// cleared at the start of every call.
 struct WorkspaceLayout {
-  size_t ctrl, z, zc, prev, conf, total;
+  size_t ctrl, bar, keys, zero_end, z, zc, prev, conf, part_val, part_id, total;
   size_t ldz;
 };
-WorkspaceLayout plan_workspace(int B, int N, int Vh);
+WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype);
+
+// Blocking of the lm_head GEMM's N dimension: BB whole blocks (BB * N prediction rows,
+// padded to bn_mma, a multiple of 16 and at most 256) per tile, n_tiles tiles.
+struct GemmTilePlan {
+  int BB, bn_mma, n_tiles;
+};
+GemmTilePlan plan_logits_gemm(int B, int N);
 
 cudaError_t launch_conf(const ProposePlan& p);
+cudaError_t launch_base_logits_tc(const ProposePlan& p);
 cudaError_t launch_base_logits_simt(const ProposePlan& p);
 cudaError_t launch_chain_simt(const ProposePlan& p);
+cudaError_t launch_chain_tc(const ProposePlan& p);
 cudaError_t launch_verify(int B, int N, const int32_t* draft, const int32_t* n_draft,
                           const int32_t* target, int32_t* accepted, int32_t* bonus,
                           int32_t* emitted, cudaStream_t stream);

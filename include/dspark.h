@@ -174,9 +174,11 @@ dspark_status dspark_propose_timed(const dspark_config* cfg, const dspark_head* 
                                    size_t workspace_bytes, void* stream,
                                    void* const* events);
 
-/* Number of kernels one dspark_propose call launches for this config and head (the
-   workspace reset is a memset node, not counted); -1 on invalid input. */
-int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head* head);
+/* Number of kernels one dspark_propose call launches for this config, head and set of
+   requested outputs (the workspace reset is a memset node, not counted); -1 on invalid
+   input. */
+int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head* head,
+                                    const dspark_outputs* out);
 
 /* Bytes of device workspace dspark_step_host needs: dspark_propose's plus staging for
    the host inputs and outputs.  256-byte aligned; 0 on invalid input. */

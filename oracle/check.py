@@ -24,13 +24,13 @@ from __future__ import annotations
 
 import numpy as np
 
-from .dspark_oracle import (argmax_lowest, corrected_logits, topk_sorted, upcast,
-                            verify)
+from .dspark_oracle import (MASK_BIAS_LIMIT, argmax_lowest, corrected_logits, topk_sorted,
+                            upcast, verify)
 
 
 def check_propose(oracle_out: dict, *, anchors, markov_w1, markov_w2, top_k: int,
                   topk_markov: bool, conf_min: float, gpu: dict, tol: float,
-                  head_rows=None, max_report: int = 20) -> dict:
+                  head_rows=None, lm_bias=None, max_report: int = 20) -> dict:
     """Compare GPU proposal outputs with the oracle.
 
     ``oracle_out`` is the dict of :func:`oracle.propose` (its base logits are used).
@@ -38,6 +38,9 @@ def check_propose(oracle_out: dict, *, anchors, markov_w1, markov_w2, top_k: int
     topk_vals [B,N,k], conf [B,N], logits [B,N,V or V_head].
     ``head_rows`` maps the GPU's logits columns to token ids when the GPU evaluated a
     compact head (d2t form); None means the columns are the token ids.
+    ``lm_bias`` (the full-vocabulary bias, or None) marks masked rows: their logits are
+    about -1e9, where fp32 spacing is 64, so for them the check is only that the GPU
+    value stays at or below the mask limit.
     Returns {"failures": [...], "near_ties": int, "slots": int}.
     """
     z = oracle_out["base_logits"]
@@ -45,6 +48,7 @@ def check_propose(oracle_out: dict, *, anchors, markov_w1, markov_w2, top_k: int
     w2 = upcast(markov_w2)
     fails: list[str] = []
     near = 0
+    masked = None if lm_bias is None else upcast(lm_bias) <= MASK_BIAS_LIMIT
 
     def fail(msg):
         if len(fails) < max_report:
@@ -100,6 +104,11 @@ def check_propose(oracle_out: dict, *, anchors, markov_w1, markov_w2, top_k: int
                 gl = np.asarray(g_logits[b, i], np.float64)
                 ref = zc if head_rows is None else zc[head_rows]
                 d = np.abs(gl - ref)
+                if masked is not None:
+                    mcols = masked if head_rows is None else masked[head_rows]
+                    d[mcols] = 0.0
+                    if np.any(gl[mcols] > MASK_BIAS_LIMIT):
+                        fail(f"logits[{b},{i}]: a masked row rose above the mask limit")
                 if np.any(d > tol):
                     j = int(np.argmax(d))
                     fail(f"logits[{b},{i}] off by {d[j]:.3g} at column {j}")

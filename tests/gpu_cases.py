@@ -43,7 +43,8 @@ def compare(wl, hd, bt, o, g, form="full"):
     rep = check.check_propose(o, anchors=bt["anchors"], markov_w1=hd["markov_w1"],
                               markov_w2=hd["markov_w2"], top_k=wl.top_k,
                               topk_markov=wl.topk_markov, conf_min=wl.conf_min,
-                              gpu=g, tol=TOL[wl.dtype], head_rows=head_rows)
+                              gpu=g, tol=TOL[wl.dtype], head_rows=head_rows,
+                              lm_bias=hd.get("lm_bias"))
     return rep
 
 

@@ -100,3 +100,30 @@ def test_verify_check():
     t = np.array([[1, 2, 0, 5]])
     assert check.check_verify(d, [3], t, [2], [0]) == []
     assert check.check_verify(d, [3], t, [3], [0])
+
+
+def test_masked_rows_only_need_to_stay_masked():
+    rng = np.random.default_rng(4)
+    B, L, H, V, r, k = 2, 4, 16, 150, 4, 2
+    hidden = rng.standard_normal((B, L, H)).astype(np.float32)
+    W = rng.standard_normal((V, H)).astype(np.float32)
+    w1 = (rng.standard_normal((V, r)) * 0.3).astype(np.float32)
+    w2 = (rng.standard_normal((r, V)) * 0.3).astype(np.float32)
+    bias = np.zeros(V, np.float32)
+    bias[::3] = -1e9
+    anchors = rng.integers(0, V, B)
+    o = propose(hidden, anchors, W, w1, w2, L_in=L, sample_from_anchor=True, top_k=k,
+                conf_min=0.0, lm_bias=bias, return_logits=True)
+    # fp32-sized error on the masked rows only
+    logits = (o["logits"] + np.where(bias < 0, 30.0, 0.0)).astype(np.float32)
+    g = dict(draft=o["draft"], n_draft=o["n_draft"], logits=logits)
+    kw = dict(anchors=anchors, markov_w1=w1, markov_w2=w2, top_k=k, topk_markov=True,
+              conf_min=0.0, tol=2e-2, lm_bias=bias)
+    assert check.check_propose(o, gpu=g, **kw)["failures"] == []
+    logits[0, 0, 0] = 0.0            # a masked row that came back unmasked
+    rep = check.check_propose(o, gpu=g, **kw)
+    assert any("mask" in f for f in rep["failures"])
+    logits[0, 0, 0] = -1e9
+    logits[1, 2, 1] += 0.1           # an emittable row off by more than tol
+    rep = check.check_propose(o, gpu=g, **kw)
+    assert any("off by" in f for f in rep["failures"])
