@@ -26,6 +26,8 @@ static constexpr size_t kAlign = 256;
 WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype) {
   WorkspaceLayout w{};
   w.ldz = align_up((size_t)Vh, 64);
+  w.Vhp = align_up((size_t)Vh, 128);
+  w.ldb = align_up((size_t)B, 4);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -33,10 +35,10 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype) {
     return o;
   };
   w.ctrl = take(256);
-  w.bar = take(sizeof(unsigned) * (size_t)((B + 63) / 64));
+  w.bar = take(sizeof(unsigned) * (size_t)((B + 31) / 32));
   w.keys = take(sizeof(unsigned long long) * (size_t)N * B);
   w.zero_end = off;
-  w.z = take(sizeof(float) * (size_t)N * B * w.ldz);
+  w.z = take(sizeof(float) * (size_t)N * w.Vhp * w.ldb);
   if (dtype == DSPARK_F32) {          // the CUDA-core chain keeps one corrected row per block
     w.zc = take(sizeof(float) * (size_t)B * w.ldz);
     w.prev = take(sizeof(int32_t) * (size_t)B);
@@ -154,6 +156,8 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   p.keys = (unsigned long long*)(ws + wl.keys);
   p.z = (float*)(ws + wl.z);
   p.ldz = wl.ldz;
+  p.Vhp = wl.Vhp;
+  p.ldb = wl.ldb;
   p.zc = (float*)(ws + wl.zc);
   p.prev = (int32_t*)(ws + wl.prev);
   p.part_val = (float*)(ws + wl.part_val);
@@ -207,7 +211,8 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK || !out) return -1;
   if (cfg->dtype == DSPARK_F32) return 1 + 1 + 2 * N;   // confidence, GEMM, 2 per slot
   const bool topk = out->topk_ids || out->topk_vals;
-  return 1 /* confidence */ + 1 /* GEMM */ + (cfg->B + 63) / 64 /* chain */ + (topk ? 1 : 0);
+  return 1 /* confidence */ + 1 /* GEMM */ + (cfg->B + 31) / 32 /* chain, 32 blocks each */ +
+         (topk ? 1 : 0);
 }
 
 // staging for dspark_step_host, placed after dspark_propose's workspace

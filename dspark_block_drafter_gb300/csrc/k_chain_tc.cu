@@ -1,5 +1,5 @@
 // The Markov-corrected greedy chain on the 5th-generation tensor cores, one persistent
-// cooperative kernel for all N slots of a group of up to 64 blocks.
+// cooperative kernel for all N slots of a group of up to 32 blocks.
 //
 // llama.cpp commit 6fed9f6 ("spec: add DSpark speculative decoding", the proposal
 // formula):
@@ -38,12 +38,16 @@ constexpr int kTileV = 128;
 constexpr int kKB = 64;                                 // K rows per stage
 constexpr uint32_t kHalf = 64 * kKB * 2;                // one 64-column half: 8 KB
 constexpr uint32_t kStage = 2 * kHalf;                  // 16 KB
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                            // two groups of four
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kProducerWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
+constexpr int kThreads = 32 * (kEpiWarps + 2);
+constexpr int kPanel = 32 * 33;                         // one padded 32 x 32 transpose panel
 constexpr long long kWaitBudget = 2000000000ll;         // ~1 s of SM clocks
 
 struct ChainArgs {
-  const float* z;
-  size_t ldz;
+  const float* z;       // base logits [N][Vhp][ldb]
+  size_t Vhp, ldb;
   const __nv_bfloat16* w1;
   const int32_t* anchors;
   const int32_t* d2t;
@@ -54,17 +58,19 @@ struct ChainArgs {
   unsigned long long* keys;
   unsigned int* bar;
   uint32_t* err;
-  int B, b0, Bg, N, V, Vh, r, k, topk_markov, want_topk;
+  int B, b0, Bg, N, V, Vh, r, k, want_topk;
   int n_mma, kb_count, tiles, stages, n_acc;
   uint32_t acc_stride, tmem_cols;
   uint32_t u_kb_bytes;      // n_mma * 128
   uint32_t scratch_bytes;
 };
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
 
-// All 128 epilogue threads agree on whether to stop: one thread samples the abort
-// flag between two named barriers and everyone reads that sample.
+// All epilogue threads agree on whether to stop: one thread samples the abort flag
+// between two named barriers and everyone reads that sample.
 __device__ __forceinline__ bool epi_agree_abort(volatile int* abort_flag,
                                                 volatile int* decision, int tid) {
   epi_sync();
@@ -83,15 +89,29 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Insert (v, id) into a sorted top-KMAX list of which the first k entries are live.
-template <int KMAX>
-__device__ __forceinline__ void list_insert(float (&lv)[KMAX], int (&li)[KMAX], int k,
-                                            float v, int id) {
+// 32 consecutive floats from a 16-byte aligned row holding `avail` valid entries; the
+// rest read as -inf.
+__device__ __forceinline__ void load_z32(const float* row, bool ok, long long avail,
+                                         float (&zv)[32]) {
 #pragma unroll
-  for (int q = 0; q < KMAX; ++q) {
-    if (q < k && better(v, id, lv[q], li[q])) {
-      float tv = lv[q];
-      int ti = li[q];
+  for (int q = 0; q < 8; ++q) {
+    float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (ok && 4 * q < avail) f = __ldcs(reinterpret_cast<const float4*>(row) + q);
+    zv[4 * q] = f.x;
+    zv[4 * q + 1] = f.y;
+    zv[4 * q + 2] = f.z;
+    zv[4 * q + 3] = f.w;
+  }
+}
+
+// Insert (v, id) into a sorted list of KT entries (best first); the last one drops out.
+template <int KT>
+__device__ __forceinline__ void list_insert(float (&lv)[KT], int (&li)[KT], float v, int id) {
+#pragma unroll
+  for (int q = 0; q < KT; ++q) {
+    if (better(v, id, lv[q], li[q])) {
+      const float tv = lv[q];
+      const int ti = li[q];
       lv[q] = v;
       li[q] = id;
       v = tv;
@@ -100,7 +120,9 @@ __device__ __forceinline__ void list_insert(float (&lv)[KMAX], int (&li)[KMAX], 
   }
 }
 
-template <int KMAX, int NCH>
+// KT: size of the per-lane candidate lists (>= top_k; 1 when no list is kept).
+// NCH: 32-block chunks per group of blocks.  ZRANK: top-k ranks the base logits.
+template <int KT, int NCH, bool ZRANK>
 __global__ void __launch_bounds__(kThreads, 1)
 chain_tc(const __grid_constant__ CUtensorMap tm_w2, const ChainArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -129,14 +151,14 @@ chain_tc(const __grid_constant__ CUtensorMap tm_w2, const ChainArgs a) {
     }
     for (int q = 0; q < a.n_acc; ++q) {
       ptx::mbar_init(&acc_full[q], 1);
-      ptx::mbar_init(&acc_empty[q], 128);
+      ptx::mbar_init(&acc_empty[q], 128);       // the four warps of one group
     }
     ptx::mbar_init(u_ready, 1);
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) ptx::tma_prefetch_desc(&tm_w2);
+  if (warp == kProducerWarp && lane == 0) ptx::tma_prefetch_desc(&tm_w2);
   if (warp == 0) {
     ptx::tmem_alloc(tmem_slot, a.tmem_cols);
     ptx::tmem_relinquish();
@@ -147,13 +169,14 @@ chain_tc(const __grid_constant__ CUtensorMap tm_w2, const ChainArgs a) {
   const uint32_t tmem = *tmem_slot;
   const int t_begin = (int)((long long)blockIdx.x * a.tiles / G);
   const int t_end = (int)((long long)(blockIdx.x + 1) * a.tiles / G);
+  const int nt = t_end - t_begin;
 
   auto give_up = [&]() {
     *abort_flag = 1;
     flag_error(a.err, kErrTimeout);
   };
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       uint32_t it = 0;
@@ -178,11 +201,11 @@ chain_tc(const __grid_constant__ CUtensorMap tm_w2, const ChainArgs a) {
           ptx::mbar_wait(&full[j % a.stages], (j / a.stages) & 1, kWaitBudget, nullptr);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = ptx::idesc_bf16_f32(kTileV, a.n_mma, /*A MN-major*/ 1, 0);
-      uint32_t it = 0, local = 0;
+      uint32_t it = 0;
       bool ok = true;
       for (int step = 0; ok && step < a.N; ++step) {
         if (!ptx::mbar_wait(u_ready, step & 1, kWaitBudget, abort_flag)) {
@@ -191,8 +214,9 @@ chain_tc(const __grid_constant__ CUtensorMap tm_w2, const ChainArgs a) {
         }
         ptx::tc_fence_after();
         const uint32_t u0 = ptx::smem_u32(s_u);
-        for (int t = t_begin; ok && t < t_end; ++t, ++local) {
-          const uint32_t acc = local % a.n_acc, aph = (local / a.n_acc) & 1;
+        for (int lt = 0; ok && lt < nt; ++lt) {
+          const uint32_t gl = (uint32_t)(step * nt + lt);
+          const uint32_t acc = gl % a.n_acc, aph = (gl / a.n_acc) & 1;
           if (!ptx::mbar_wait(&acc_empty[acc], aph ^ 1, kWaitBudget, abort_flag)) {
             ok = false;
             break;
@@ -223,11 +247,11 @@ chain_tc(const __grid_constant__ CUtensorMap tm_w2, const ChainArgs a) {
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int tid = threadIdx.x;                    // 0..127
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float* scr_x = s_scr + warp * (2 * 32 * 33);    // this warp's transpose panels
-    float* scr_z = scr_x + 32 * 33;
-    uint32_t local = 0;
+    const int tid = threadIdx.x;                    // 0..255
+    const int quad = warp % 4, grp = warp / 4;      // TMEM lane quadrant, tile parity
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    float* scr_x = s_scr + warp * (ZRANK ? 2 : 1) * kPanel;
+    float* scr_z = scr_x + kPanel;
     bool ok = true;
     for (int step = 0; ok && step < a.N; ++step) {
       // -------- 1. previous tokens of this slot
@@ -249,62 +273,79 @@ chain_tc(const __grid_constant__ CUtensorMap tm_w2, const ChainArgs a) {
       }
       epi_sync();
       // -------- 2. u = markov_w1[prev] into the swizzled K-major B operand
-      const int chunks = a.n_mma * a.kb_count * 8;
-      for (int idx = tid; idx < chunks; idx += 128) {
-        const int n = idx / (a.kb_count * 8);
-        const int rem = idx % (a.kb_count * 8);
-        const int kb = rem / 8, j = rem % 8;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (n < a.Bg) {
-          const int k0 = kb * kKB + j * 8;
-          const __nv_bfloat16* src = a.w1 + (size_t)s_prev[n] * a.r + k0;
-          if ((a.r & 7) == 0 && k0 + 8 <= a.r) {
-            val = *reinterpret_cast<const uint4*>(src);
-          } else {
-            __nv_bfloat16 e[8];
+      {
+        const int per_row = a.kb_count * 8;
+        const int chunks = a.n_mma * per_row;
+        for (int base = 0; base < chunks; base += 4 * kEpiThreads) {
+          uint4 val[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) e[q] = (k0 + q < a.r) ? src[q] : __float2bfloat16(0.f);
-            val = *reinterpret_cast<uint4*>(e);
+          for (int q = 0; q < 4; ++q) {
+            const int idx = base + q * kEpiThreads + tid;
+            val[q] = make_uint4(0, 0, 0, 0);
+            const int n = idx / per_row, rem = idx % per_row;
+            if (idx < chunks && n < a.Bg) {
+              const int k0 = (rem / 8) * kKB + (rem % 8) * 8;
+              const __nv_bfloat16* src = a.w1 + (size_t)s_prev[n] * a.r + k0;
+              if ((a.r & 7) == 0 && k0 + 8 <= a.r) {
+                val[q] = __ldg(reinterpret_cast<const uint4*>(src));
+              } else {                                 // ragged rank: element-wise
+                uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  if (k0 + c < a.r)
+                    w[c / 2] |= (uint32_t)__bfloat16_as_ushort(src[c]) << (16 * (c % 2));
+                val[q] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int idx = base + q * kEpiThreads + tid;
+            if (idx < chunks) {
+              const int n = idx / per_row, rem = idx % per_row;
+              const int kb = rem / 8, j = rem % 8;
+              *reinterpret_cast<uint4*>(s_u + (size_t)kb * a.u_kb_bytes + n * 128 +
+                                        ((j ^ (n & 7)) << 4)) = val[q];
+            }
           }
         }
-        *reinterpret_cast<uint4*>(s_u + (size_t)kb * a.u_kb_bytes + n * 128 +
-                                  ((j ^ (n & 7)) << 4)) = val;
       }
       fence_proxy_async();
       epi_sync();
       if (tid == 0) ptx::mbar_arrive(u_ready);
 
-      // -------- 3. tiles: add base logits, running argmax / top-k per block
+      // -------- 3. tiles of this group: base logits + Markov term, running argmax/top-k
       float amax_v[NCH], thr_v[NCH];
       int amax_i[NCH], thr_i[NCH];
-      float lv[NCH][KMAX];
-      int li[NCH][KMAX];
+      float lv[NCH][KT];
+      int li[NCH][KT];
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         amax_v[c] = thr_v[c] = -INFINITY;
         amax_i[c] = thr_i[c] = 0x7FFFFFFF;
 #pragma unroll
-        for (int q = 0; q < KMAX; ++q) {
+        for (int q = 0; q < KT; ++q) {
           lv[c][q] = -INFINITY;
           li[c][q] = 0x7FFFFFFF;
         }
       }
-      const float* z_i = a.z + (size_t)step * a.B * a.ldz;
-      for (int t = t_begin; t < t_end; ++t, ++local) {
-        const int v = t * kTileV + warp * 32 + lane;
+      const float* z_i = a.z + (size_t)step * a.Vhp * a.ldb;
+      for (int lt = grp; lt < nt; lt += 2) {
+        const int t = t_begin + lt;
+        const int v = t * kTileV + quad * 32 + lane;
         const bool v_ok = v < a.Vh;
-        const uint32_t acc = local % a.n_acc, aph = (local / a.n_acc) & 1;
+        const int id0 = t * kTileV + quad * 32;          // id of candidate j is id0 + j
+        // base logits of this head row for the chunk's 32 blocks: contiguous, 16-byte loads
+        const float* zrow = z_i + (size_t)v * a.ldb + a.b0;
+        float zv[32];
+        load_z32(zrow, v_ok, a.ldb - a.b0, zv);
+        const uint32_t gl = (uint32_t)(step * nt + lt);
+        const uint32_t acc = gl % a.n_acc, aph = (gl / a.n_acc) & 1;
         ok = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&acc_full[acc], aph, kWaitBudget, abort_flag));
         if (!ok) break;
         ptx::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-          float zv[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int b = c * 32 + j;
-            zv[j] = (v_ok && b < a.Bg) ? __ldcs(&z_i[(size_t)(a.b0 + b) * a.ldz + v]) : -INFINITY;
-          }
           uint32_t r[32];
           ptx::tmem_ld_32x32b_x32(tmem + lane_base + acc * a.acc_stride + c * 32, r);
           ptx::tmem_ld_wait();
@@ -312,33 +353,28 @@ chain_tc(const __grid_constant__ CUtensorMap tm_w2, const ChainArgs a) {
           for (int j = 0; j < 32; ++j) {
             const float x = zv[j] + __uint_as_float(r[j]);
             scr_x[j * 33 + lane] = x;
-            scr_z[j * 33 + lane] = zv[j];
-            const int b = c * 32 + j;
-            if (a.logits && v_ok && b < a.Bg)
-              a.logits[((size_t)(a.b0 + b) * a.N + step) * a.Vh + v] = x;
+            if (ZRANK) scr_z[j * 33 + lane] = zv[j];
+            if (a.logits && v_ok && c * 32 + j < a.Bg)
+              a.logits[((size_t)(a.b0 + c * 32 + j) * a.N + step) * a.Vh + v] = x;
           }
+          if (c + 1 < NCH)                                 // next chunk's base logits
+            load_z32(zrow + (c + 1) * 32, v_ok, (long long)a.ldb - a.b0 - (c + 1) * 32, zv);
           __syncwarp();
-          const int b = c * 32 + lane;
-          if (b < a.Bg) {
 #pragma unroll 4
-            for (int j = 0; j < 32; ++j) {
-              const int id = t * kTileV + warp * 32 + j;
-              if (id >= a.Vh) break;
+          for (int j = 0; j < 32; ++j) {
+            const int id = id0 + j;
+            if (id < a.Vh) {                               // uniform over the warp
               const float x = scr_x[lane * 33 + j];
               if (better(x, id, amax_v[c], amax_i[c])) {
                 amax_v[c] = x;
                 amax_i[c] = id;
               }
-              if (a.want_topk) {
-                const float rk = a.topk_markov ? x : scr_z[lane * 33 + j];
-                if (better(rk, id, thr_v[c], thr_i[c])) {     // beats the current k-th
-                  list_insert<KMAX>(lv[c], li[c], a.k, rk, id);
-#pragma unroll
-                  for (int q = 0; q < KMAX; ++q)
-                    if (q == a.k - 1) {
-                      thr_v[c] = lv[c][q];
-                      thr_i[c] = li[c][q];
-                    }
+              if (KT > 1 || ZRANK) {
+                const float rk = ZRANK ? scr_z[lane * 33 + j] : x;
+                if (better(rk, id, thr_v[c], thr_i[c])) {  // beats the list's last entry
+                  list_insert<KT>(lv[c], li[c], rk, id);
+                  thr_v[c] = lv[c][KT - 1];
+                  thr_i[c] = li[c][KT - 1];
                 }
               }
             }
@@ -348,65 +384,72 @@ chain_tc(const __grid_constant__ CUtensorMap tm_w2, const ChainArgs a) {
         ptx::tc_fence_before();
         ptx::mbar_arrive(&acc_empty[acc]);
       }
-      // a warp that gave up raises the flag; the others then stop waiting, and all four
-      // take the same decision here (the named barriers below need all 128 threads)
+      // a warp that gave up raises the flag; the others then stop waiting, and all take
+      // the same decision here (the named barriers below need every epilogue thread)
       if (!ok) give_up();
       if (epi_agree_abort(abort_flag, s_decision, tid)) {
         ok = false;
         break;
       }
-      // -------- 4. merge the four warps, publish the CTA's candidates
-      float* m_av = s_scr;                             // [4][64]
-      int* m_ai = (int*)(m_av + 4 * 64);               // [4][64]
-      float* m_lv = (float*)(m_ai + 4 * 64);           // [4][64][k]
-      int* m_li = (int*)(m_lv + 4 * 64 * a.k);         // [4][64][k]
+      // -------- 4. merge the eight warps, publish the CTA's candidates
+      constexpr int KL = (KT > 1 || ZRANK) ? KT : 1;   // entries per lane list in smem
+      constexpr int BS = NCH * 32;                     // block stride of the merge arrays
+      float* m_av = s_scr;                             // [8][BS]
+      int* m_ai = (int*)(m_av + kEpiWarps * BS);       // [8][BS]
+      float* m_lv = (float*)(m_ai + kEpiWarps * BS);   // [8][BS][KL]
+      int* m_li = (int*)(m_lv + kEpiWarps * BS * KL);  // [8][BS][KL]
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         const int b = c * 32 + lane;
-        if (b < a.Bg) {
-          m_av[warp * 64 + b] = amax_v[c];
-          m_ai[warp * 64 + b] = amax_i[c];
-          if (a.want_topk)
+        m_av[warp * BS + b] = amax_v[c];
+        m_ai[warp * BS + b] = amax_i[c];
+        if (KT > 1 || ZRANK) {
 #pragma unroll
-            for (int q = 0; q < KMAX; ++q)
-              if (q < a.k) {
-                m_lv[(warp * 64 + b) * a.k + q] = lv[c][q];
-                m_li[(warp * 64 + b) * a.k + q] = li[c][q];
-              }
+          for (int q = 0; q < KL; ++q) {
+            m_lv[(warp * BS + b) * KL + q] = lv[c][q];
+            m_li[(warp * BS + b) * KL + q] = li[c][q];
+          }
         }
       }
       epi_sync();
-      if (tid < a.Bg) {
+      if (tid < a.Bg) {                                // argmax of each block
         const int b = tid;
-        float bv = -INFINITY;
-        int bi = 0x7FFFFFFF;
-        for (int w = 0; w < 4; ++w)
-          if (better(m_av[w * 64 + b], m_ai[w * 64 + b], bv, bi)) {
-            bv = m_av[w * 64 + b];
-            bi = m_ai[w * 64 + b];
+        float bv = m_av[b];
+        int bi = m_ai[b];
+#pragma unroll
+        for (int w = 1; w < kEpiWarps; ++w)
+          if (better(m_av[w * BS + b], m_ai[w * BS + b], bv, bi)) {
+            bv = m_av[w * BS + b];
+            bi = m_ai[w * BS + b];
           }
-        if (bi != 0x7FFFFFFF)
-          atomicMax(&a.keys[(size_t)step * a.B + a.b0 + b], order_key(bv, bi));
-        if (a.want_topk) {
-          int ptr[4] = {0, 0, 0, 0};
+        if (bi != 0x7FFFFFFF) atomicMax(&a.keys[(size_t)step * a.B + a.b0 + b], order_key(bv, bi));
+      }
+      if (a.want_topk) {
+        // one warp per block: k rounds of a warp-wide best among the 8 lists' entries
+        // strictly after the previous pick
+        for (int b = warp; b < a.Bg; b += kEpiWarps) {
           const size_t o = (((size_t)step * a.B + a.b0 + b) * G + blockIdx.x) * a.k;
+          float pv = 0.f;
+          int pid = 0;
           for (int q = 0; q < a.k; ++q) {
-            int bw = -1;
-            float cv = -INFINITY;
-            int ci = 0x7FFFFFFF;
-            for (int w = 0; w < 4; ++w) {
-              if (ptr[w] >= a.k) continue;
-              const float x = m_lv[(w * 64 + b) * a.k + ptr[w]];
-              const int xi = m_li[(w * 64 + b) * a.k + ptr[w]];
-              if (bw < 0 || better(x, xi, cv, ci)) {
-                bw = w;
-                cv = x;
-                ci = xi;
+            float bv = -INFINITY;
+            int bi = 0x7FFFFFFF;
+            for (int e = lane; e < kEpiWarps * KL; e += 32) {
+              const int w = e / KL, s2 = e % KL;
+              const float x = (KT > 1 || ZRANK) ? m_lv[(w * BS + b) * KL + s2] : m_av[w * BS + b];
+              const int xi = (KT > 1 || ZRANK) ? m_li[(w * BS + b) * KL + s2] : m_ai[w * BS + b];
+              if ((q == 0 || better(pv, pid, x, xi)) && better(x, xi, bv, bi)) {
+                bv = x;
+                bi = xi;
               }
             }
-            ++ptr[bw];
-            a.part_val[o + q] = cv;
-            a.part_id[o + q] = ci;
+            warp_best(bv, bi);
+            if (lane == 0) {
+              a.part_val[o + q] = bv;
+              a.part_id[o + q] = bi;
+            }
+            pv = bv;
+            pid = bi;
           }
         }
       }
@@ -461,7 +504,11 @@ topk_merge(const float* __restrict__ part_val, const int32_t* __restrict__ part_
     lv[q] = -INFINITY;
     li[q] = 0x7FFFFFFF;
   }
-  for (int c = lane; c < G * k; c += 32) list_insert<KMAX>(lv, li, k, part_val[base + c], part_id[base + c]);
+  for (int c = lane; c < G * k; c += 32) {
+    const float x = part_val[base + c];
+    const int xi = part_id[base + c];
+    if (better(x, xi, lv[KMAX - 1], li[KMAX - 1])) list_insert<KMAX>(lv, li, x, xi);
+  }
   // k rounds of a warp-wide pick of the best list head
   for (int q = 0; q < k; ++q) {
     float bv = lv[0];
@@ -499,10 +546,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int KMAX, int NCH>
+template <int KT, int NCH, bool ZRANK>
 cudaError_t launch_chain_inst(const CUtensorMap& tm, const ChainArgs& a, int grid, size_t smem,
                               cudaStream_t stream) {
-  auto kern = chain_tc<KMAX, NCH>;
+  auto kern = chain_tc<KT, NCH, ZRANK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
@@ -533,8 +580,12 @@ cudaError_t launch_chain_tc(const ProposePlan& p) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int tiles = (p.Vh + kTileV - 1) / kTileV;
   const int grid = std::max(1, std::min({sms, tiles, kChainMaxCtas}));
-  const int kmax = p.k <= 1 ? 1 : (p.k <= 8 ? 8 : 32);
   const bool want_topk = p.topk_ids || p.topk_vals;
+  const bool zrank = want_topk && !p.topk_markov;
+  // per-lane list size: none when only the argmax is needed (or when the argmax is the
+  // whole top-1), else the smallest of 8 / 32 that holds top_k
+  const int kt = (!want_topk || (p.k == 1 && p.topk_markov)) ? 1 : (p.k <= 8 ? 8 : 32);
+  const int group = 32;                        // blocks per launch: one per lane
 
   CUtensorMap tm;
   {
@@ -548,10 +599,11 @@ cudaError_t launch_chain_tc(const ProposePlan& p) {
         CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  for (int b0 = 0; b0 < p.B; b0 += 64) {
+  for (int b0 = 0; b0 < p.B; b0 += group) {
     ChainArgs a{};
     a.z = p.z;
-    a.ldz = p.ldz;
+    a.Vhp = p.Vhp;
+    a.ldb = p.ldb;
     a.w1 = (const __nv_bfloat16*)p.w1;
     a.anchors = p.anchors;
     a.d2t = p.d2t;
@@ -560,17 +612,16 @@ cudaError_t launch_chain_tc(const ProposePlan& p) {
     a.part_val = p.part_val;
     a.part_id = p.part_id;
     a.keys = p.keys;
-    a.bar = p.bar + b0 / 64;
+    a.bar = p.bar + b0 / 32;
     a.err = p.ctrl;
     a.B = p.B;
     a.b0 = b0;
-    a.Bg = std::min(64, p.B - b0);
+    a.Bg = std::min(group, p.B - b0);
     a.N = p.N;
     a.V = p.V;
     a.Vh = p.Vh;
     a.r = p.r;
     a.k = p.k;
-    a.topk_markov = p.topk_markov;
     a.want_topk = want_topk ? 1 : 0;
     a.n_mma = (a.Bg + 15) / 16 * 16;
     a.kb_count = (p.r + kKB - 1) / kKB;
@@ -581,8 +632,10 @@ cudaError_t launch_chain_tc(const ProposePlan& p) {
     while (cols < a.n_acc * a.acc_stride) cols <<= 1;
     a.tmem_cols = cols;
     a.u_kb_bytes = (uint32_t)a.n_mma * 128;
-    const size_t transpose = 4 * 2 * 32 * 33 * sizeof(float);
-    const size_t merge = 4 * 64 * 8 + 4 * 64 * (size_t)p.k * 8;
+    const int kl = (kt > 1 || zrank) ? kt : 1;
+    const size_t transpose = (size_t)kEpiWarps * (zrank ? 2 : 1) * kPanel * sizeof(float);
+    const size_t bs = a.Bg <= 32 ? 32 : 64;
+    const size_t merge = (size_t)kEpiWarps * bs * 8 + (size_t)kEpiWarps * bs * kl * 8;
     a.scratch_bytes = (uint32_t)align_up(std::max(transpose, merge), 1024);
     const size_t fixed = 1024 + (size_t)a.kb_count * a.u_kb_bytes + a.scratch_bytes + 1024;
     const size_t budget = 225 * 1024;
@@ -590,18 +643,18 @@ cudaError_t launch_chain_tc(const ProposePlan& p) {
     a.stages = (int)std::min<size_t>(12, (budget - fixed) / kStage);
     const size_t smem = fixed + (size_t)a.stages * kStage;
     cudaError_t e;
-    const int nch = a.Bg <= 32 ? 1 : 2;
-    if (kmax == 1)
-      e = nch == 1 ? launch_chain_inst<1, 1>(tm, a, grid, smem, p.stream)
-                   : launch_chain_inst<1, 2>(tm, a, grid, smem, p.stream);
-    else if (kmax == 8)
-      e = nch == 1 ? launch_chain_inst<8, 1>(tm, a, grid, smem, p.stream)
-                   : launch_chain_inst<8, 2>(tm, a, grid, smem, p.stream);
+    if (kt == 1)
+      e = zrank ? launch_chain_inst<1, 1, true>(tm, a, grid, smem, p.stream)
+                : launch_chain_inst<1, 1, false>(tm, a, grid, smem, p.stream);
+    else if (kt == 8)
+      e = zrank ? launch_chain_inst<8, 1, true>(tm, a, grid, smem, p.stream)
+                : launch_chain_inst<8, 1, false>(tm, a, grid, smem, p.stream);
     else
-      e = nch == 1 ? launch_chain_inst<32, 1>(tm, a, grid, smem, p.stream)
-                   : launch_chain_inst<32, 2>(tm, a, grid, smem, p.stream);
+      e = zrank ? launch_chain_inst<32, 1, true>(tm, a, grid, smem, p.stream)
+                : launch_chain_inst<32, 1, false>(tm, a, grid, smem, p.stream);
     if (e != cudaSuccess) return e;
   }
+  const int kmax = p.k <= 1 ? 1 : (p.k <= 8 ? 8 : 32);
   if (want_topk) {
     const int warps = p.B * p.N;
     const int threads = 256;

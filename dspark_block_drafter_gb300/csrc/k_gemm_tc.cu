@@ -1,19 +1,21 @@
 // Base logits on the 5th-generation tensor cores (bf16 in, fp32 accumulate in TMEM).
 //
-//   z[i][b][v] = sum_h hidden[b, ifp + i, h] * lm_head[v, h] + lm_bias[v]
+//   z[i][v][b] = sum_h hidden[b, ifp + i, h] * lm_head[v, h] + lm_bias[v]
 //
 // (llama.cpp commit 6fed9f6, "spec: add DSpark speculative decoding": logits(i) of the
 // proposal formula.)  The GEMM runs "swap-AB": the MMA's M dimension is the vocabulary
-// (128 head rows per tile), its N dimension the prediction rows of whole blocks
-// (BB blocks x N slots, up to 256), so a small batch still fills the instruction.
+// (128 head rows per tile), its N dimension the prediction rows of Ni slots x BB blocks
+// (blocks fastest, up to 256), so a small batch still fills the instruction.  The
+// output keeps the blocks of one (slot, head row) contiguous, so each thread stores
+// runs of 16 bytes and the chain reads them back the same way.
 //
 // One persistent CTA per SM, warp-specialised:
-//   warp 4      TMA producer: lm_head tile [128 x 64] and hidden tile [BB, N, 64] per
+//   warp 4      TMA producer: lm_head tile [128 x 64] and hidden tile [Ni, BB, 64] per
 //               K-block into a ring of shared-memory stages (128-byte swizzle)
 //   warp 5      MMA issuer: 4 x tcgen05.mma (K = 16) per stage into a TMEM accumulator;
 //               tcgen05.commit frees the stage, and the accumulator when the tile ends
 //   warps 0-3   epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 head rows), + bias,
-//               coalesced fp32 stores of z (consecutive lanes = consecutive v)
+//               fp32 stores of z (16-byte runs of blocks per thread)
 // Two TMEM accumulators alternate so that the epilogue of one tile overlaps the MMAs of
 // the next.  Tiles are ordered vocabulary-major: CTAs that run side by side share the
 // same lm_head tile through L2, so lm_head streams from HBM once.
@@ -39,16 +41,27 @@ constexpr long long kWaitBudget = 2000000000ll;       // ~1 s of SM clocks
 
 struct GemmArgs {
   float* z;
-  size_t ldz;
+  size_t Vhp, ldb;
   const float* bias;
   uint32_t* err;
   int B, N, ifp, Vh;
-  int BB;          // blocks per N-tile
+  int BB, Ni;      // blocks and slots per N-tile
+  int n_bt;        // N-tiles along the blocks (the slot index is tile / n_bt)
   int bn_mma;      // MMA N (rows of the B operand per stage), multiple of 16
   int acc_stride;  // TMEM columns between the two accumulators (multiple of 32)
   int n_tiles, v_tiles, num_kb, stages;
   uint32_t tmem_cols;
 };
+
+// Valid prediction rows of N-tile nt: slots and blocks it covers.
+__device__ __forceinline__ void ntile_extent(const GemmArgs& g, int nt, int& i0, int& ni,
+                                             int& bb0, int& nb) {
+  const int it = nt / g.n_bt, bt = nt % g.n_bt;
+  i0 = it * g.Ni;
+  ni = min(g.Ni, g.N - i0);
+  bb0 = bt * g.BB;
+  nb = min(g.BB, g.B - bb0);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
@@ -102,7 +115,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
   if (warp == 4) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint32_t tx = kStageA + (uint32_t)(g.BB * g.N) * kBlockK * 2;
+      const uint32_t tx = kStageA + (uint32_t)(g.BB * g.Ni) * kBlockK * 2;
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
@@ -116,8 +129,8 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
           ptx::mbar_arrive_expect_tx(&full[s], tx);
           ptx::tma_load_2d(sA + (size_t)s * kStageA, &tm_w, &full[s], kb * kBlockK,
                            vt * kBlockV);
-          ptx::tma_load_3d(sB + (size_t)s * b_stage, &tm_h, &full[s], kb * kBlockK, g.ifp,
-                           nt * g.BB);
+          ptx::tma_load_3d(sB + (size_t)s * b_stage, &tm_h, &full[s], kb * kBlockK,
+                           (nt % g.n_bt) * g.BB, g.ifp + (nt / g.n_bt) * g.Ni);
         }
       }
       if (!ok) {
@@ -134,9 +147,9 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       uint32_t it = 0, local = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
-        const int nt = tile % g.n_tiles;
-        const int rows = min(g.BB, g.B - nt * g.BB) * g.N;
-        const int n_mma = (rows + 15) / 16 * 16;
+        int i0, ni, bb0, nb;
+        ntile_extent(g, tile % g.n_tiles, i0, ni, bb0, nb);
+        const int n_mma = (ni * g.BB + 15) / 16 * 16;   // rows up to the last valid slot
         const uint32_t idesc = ptx::idesc_bf16_f32(kBlockV, n_mma, 0, 0);
         const uint32_t acc = local & 1, aph = (local >> 1) & 1;
         if (!ptx::mbar_wait(&acc_empty[acc], aph ^ 1, kWaitBudget, abort_flag)) {
@@ -172,8 +185,10 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     uint32_t local = 0;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-      const int vt = tile / g.n_tiles, nt = tile % g.n_tiles;
-      const int rows = min(g.BB, g.B - nt * g.BB) * g.N;
+      const int vt = tile / g.n_tiles;
+      int i0, ni, bb0, nb;
+      ntile_extent(g, tile % g.n_tiles, i0, ni, bb0, nb);
+      const int rows = ni * g.BB;
       const uint32_t acc = local & 1, aph = (local >> 1) & 1;
       // the warp leaves together: tcgen05.ld below is a warp-collective instruction
       const bool ok = __all_sync(0xFFFFFFFFu,
@@ -186,17 +201,33 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       const int v = vt * kBlockV + warp * 32 + lane;
       const bool live = v < g.Vh;
       const float bias_v = (g.bias && live) ? g.bias[v] : 0.f;
-      const int b_first = nt * g.BB;
       for (int c0 = 0; c0 < rows; c0 += 32) {
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(tmem + lane_base + acc * (uint32_t)g.acc_stride + c0, r);
         ptx::tmem_ld_wait();
-        int bl = c0 / g.N, il = c0 % g.N;
+        if (!live) continue;
+        if ((g.BB & 3) == 0) {
+          // runs of four consecutive blocks of one slot: 16-byte stores
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (live && c0 + j < rows)
-            g.z[((size_t)il * g.B + b_first + bl) * g.ldz + v] = __uint_as_float(r[j]) + bias_v;
-          if (++il == g.N) { il = 0; ++bl; }
+          for (int j = 0; j < 32; j += 4) {
+            const int c = c0 + j, il = c / g.BB, bl = c % g.BB;
+            if (c < rows && bl < nb) {
+              float4 o = make_float4(__uint_as_float(r[j]) + bias_v,
+                                     __uint_as_float(r[j + 1]) + bias_v,
+                                     __uint_as_float(r[j + 2]) + bias_v,
+                                     __uint_as_float(r[j + 3]) + bias_v);
+              *reinterpret_cast<float4*>(
+                  &g.z[((size_t)(i0 + il) * g.Vhp + v) * g.ldb + bb0 + bl]) = o;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = c0 + j, il = c / g.BB, bl = c % g.BB;
+            if (c < rows && bl < nb)
+              g.z[((size_t)(i0 + il) * g.Vhp + v) * g.ldb + bb0 + bl] =
+                  __uint_as_float(r[j]) + bias_v;
+          }
         }
       }
       ptx::tc_fence_before();
@@ -238,10 +269,12 @@ int sm_count() {
 // Tile plan of the lm_head GEMM for B blocks of N prediction slots.
 GemmTilePlan plan_logits_gemm(int B, int N) {
   GemmTilePlan t{};
-  const int bb_max = 256 / N;
-  t.n_tiles = (B + bb_max - 1) / bb_max;
-  t.BB = (B + t.n_tiles - 1) / t.n_tiles;
-  t.bn_mma = (t.BB * N + 15) / 16 * 16;
+  t.BB = B < 256 ? B : 256;
+  const int ni_max = std::max(1, 256 / t.BB);
+  t.n_it = (N + ni_max - 1) / ni_max;
+  t.Ni = (N + t.n_it - 1) / t.n_it;                  // balanced slot chunks
+  t.n_bt = (B + t.BB - 1) / t.BB;
+  t.bn_mma = (t.BB * t.Ni + 15) / 16 * 16;
   return t;
 }
 
@@ -251,7 +284,8 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   const GemmTilePlan tp = plan_logits_gemm(p.B, p.N);
   GemmArgs g{};
   g.z = p.z;
-  g.ldz = p.ldz;
+  g.Vhp = p.Vhp;
+  g.ldb = p.ldb;
   g.bias = p.lm_bias;
   g.err = p.ctrl;
   g.B = p.B;
@@ -259,8 +293,10 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   g.ifp = p.ifp;
   g.Vh = p.Vh;
   g.BB = tp.BB;
+  g.Ni = tp.Ni;
+  g.n_bt = tp.n_bt;
   g.bn_mma = tp.bn_mma;
-  g.n_tiles = tp.n_tiles;
+  g.n_tiles = tp.n_it * tp.n_bt;
   g.v_tiles = (p.Vh + kBlockV - 1) / kBlockV;
   g.num_kb = (p.H + kBlockK - 1) / kBlockK;
   const uint32_t stage_bytes = kStageA + (uint32_t)g.bn_mma * kBlockK * 2;
@@ -287,9 +323,11 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
       return cudaErrorInvalidValue;
   }
   {
-    cuuint64_t dims[3] = {(cuuint64_t)p.H, (cuuint64_t)p.L_in, (cuuint64_t)p.B};
-    cuuint64_t strides[2] = {(cuuint64_t)p.H * 2, (cuuint64_t)p.L_in * p.H * 2};
-    cuuint32_t box[3] = {kBlockK, (cuuint32_t)p.N, (cuuint32_t)g.BB};
+    // hidden [B, L_in, H] viewed as (h, block, slot) so that a box lands slot-major with
+    // the blocks of one slot contiguous
+    cuuint64_t dims[3] = {(cuuint64_t)p.H, (cuuint64_t)p.B, (cuuint64_t)p.L_in};
+    cuuint64_t strides[2] = {(cuuint64_t)p.L_in * p.H * 2, (cuuint64_t)p.H * 2};
+    cuuint32_t box[3] = {kBlockK, (cuuint32_t)g.BB, (cuuint32_t)g.Ni};
     cuuint32_t es[3] = {1, 1, 1};
     if (encode(&tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)p.hidden, dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

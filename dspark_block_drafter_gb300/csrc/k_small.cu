@@ -1,5 +1,7 @@
 // Small kernels of the path: the confidence head with the truncation length, and the
 // greedy verify/accept step.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -12,7 +14,7 @@ namespace {
 // draft pruning for DSpark": truncate at the first position below the threshold, 0
 // disables).  One CTA per block; warps take slots round-robin.
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(512)
 conf_truncate(const T* __restrict__ hidden, const T* __restrict__ w_conf, float b_conf,
               int L_in, int N, int ifp, int H, float conf_min, float* __restrict__ conf,
               int32_t* __restrict__ n_draft) {
@@ -23,7 +25,24 @@ conf_truncate(const T* __restrict__ hidden, const T* __restrict__ w_conf, float 
     for (int i = warp; i < N; i += nw) {
       const T* h = hidden + ((size_t)b * L_in + ifp + i) * H;
       float acc = 0.f;
-      for (int c = lane; c < H; c += 32) acc = fmaf(to_f32(h[c]), to_f32(w_conf[c]), acc);
+      constexpr int kVec = 16 / sizeof(T);            // elements per 16-byte load
+      const bool vec = (H % kVec == 0) && ((uintptr_t)h % 16 == 0) && ((uintptr_t)w_conf % 16 == 0);
+      int c0 = 0;
+      if (vec) {
+        const uint4* h4 = reinterpret_cast<const uint4*>(h);
+        const uint4* w4 = reinterpret_cast<const uint4*>(w_conf);
+        const int n4 = H / kVec;
+#pragma unroll 4
+        for (int q = lane; q < n4; q += 32) {
+          const uint4 hv = h4[q], wv = w4[q];
+          const T* he = reinterpret_cast<const T*>(&hv);
+          const T* we = reinterpret_cast<const T*>(&wv);
+#pragma unroll
+          for (int e = 0; e < kVec; ++e) acc = fmaf(to_f32(he[e]), to_f32(we[e]), acc);
+        }
+        c0 = H;
+      }
+      for (int c = c0 + lane; c < H; c += 32) acc = fmaf(to_f32(h[c]), to_f32(w_conf[c]), acc);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
       if (lane == 0) {
@@ -80,12 +99,13 @@ verify_kernel(int B, int N, const int32_t* __restrict__ draft,
 cudaError_t launch_conf(const ProposePlan& p) {
   float* conf = p.conf ? p.conf : p.conf_ws;
   size_t smem = sizeof(float) * (size_t)p.N;
+  const int threads = 32 * std::min(16, std::max(1, p.N));   // one warp per slot
   if (p.dtype == 0)
-    conf_truncate<float><<<p.B, 256, smem, p.stream>>>(
+    conf_truncate<float><<<p.B, threads, smem, p.stream>>>(
         (const float*)p.hidden, (const float*)p.w_conf, p.b_conf, p.L_in, p.N, p.ifp, p.H,
         p.conf_min, conf, p.n_draft);
   else
-    conf_truncate<__nv_bfloat16><<<p.B, 256, smem, p.stream>>>(
+    conf_truncate<__nv_bfloat16><<<p.B, threads, smem, p.stream>>>(
         (const __nv_bfloat16*)p.hidden, (const __nv_bfloat16*)p.w_conf, p.b_conf, p.L_in,
         p.N, p.ifp, p.H, p.conf_min, conf, p.n_draft);
   return cudaGetLastError();

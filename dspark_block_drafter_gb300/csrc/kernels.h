@@ -30,12 +30,14 @@ struct ProposePlan {
   float* logits;
   // workspace pieces
   uint32_t* ctrl;       // [0] = error word
-  unsigned int* bar;    // grid-barrier counters of the chain, one per group of 64 blocks
+  unsigned int* bar;    // grid-barrier counters of the chain, one per launch (<= 32 blocks
+                        // apart)
   unsigned long long* keys;  // [N][B] order keys of each slot's winner
   float* part_val;      // [N][B][kChainMaxCtas][k] per-CTA top-k partials
   int32_t* part_id;
-  float* z;             // base logits [N][B][ldz]
-  size_t ldz;
+  float* z;             // base logits [N][Vhp][ldb]: slot, head row, block (fastest)
+  size_t Vhp, ldb;      // head rows rounded up to whole 128-row tiles; blocks rounded to 4
+  size_t ldz;           // row stride of zc
   float* zc;            // corrected logits of the current slot [B][ldz]
   int32_t* prev;        // previous tokens [B]
   float* conf_ws;       // confidences when the caller did not ask for them [B][N]
@@ -49,14 +51,15 @@ constexpr int kChainMaxCtas = 256;
 // cleared at the start of every call.
 struct WorkspaceLayout {
   size_t ctrl, bar, keys, zero_end, z, zc, prev, conf, part_val, part_id, total;
-  size_t ldz;
+  size_t Vhp, ldb, ldz;
 };
 WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype);
 
-// Blocking of the lm_head GEMM's N dimension: BB whole blocks (BB * N prediction rows,
-// padded to bn_mma, a multiple of 16 and at most 256) per tile, n_tiles tiles.
+// Blocking of the lm_head GEMM's N dimension: a tile holds Ni slots x BB blocks of
+// prediction rows (blocks fastest; padded to bn_mma, a multiple of 16, at most 256);
+// n_it x n_bt such tiles cover all N slots and B blocks.
 struct GemmTilePlan {
-  int BB, bn_mma, n_tiles;
+  int BB, Ni, n_it, n_bt, bn_mma;
 };
 GemmTilePlan plan_logits_gemm(int B, int N);
 
