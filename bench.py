@@ -24,6 +24,7 @@ bounded sample of the same workload and prints the same JSON line with
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -221,6 +222,53 @@ def _config(wl, l2):
 
 
 # ------------------------------------------------------------------ GPU arm
+def _time_steps(tio, _abi, cfg, head, ws, hidden, anchors, out, target, acc, bonus,
+                emitted, stream, flush, K, W, world):
+    """W warm-up then K timed steps (L2 flushed before each); device time per step from
+    CUDA events on the launching stream, and the library's stage events."""
+    import torch
+    ns = _abi.DSPARK_NUM_STAGES
+
+    def step(events=None):
+        if events is None:
+            tio.propose(cfg, head, hidden, anchors, out, ws, stream)
+        else:
+            _abi.check(_abi.dspark_propose_timed(
+                cfg, head.struct(), hidden.data_ptr(), anchors.data_ptr(), out.struct(),
+                ws.data_ptr(), ws.numel(), stream.cuda_stream, [e.cuda_event for e in events]))
+        tio.verify(out.draft, out.n_draft, target, acc, bonus, emitted, stream)
+
+    for _ in range(W):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert tio.device_status(ws, stream) == 0
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    ev_stage = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(K)]
+    for evs in ev_stage:          # materialise the handles the library records into
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for s_ in range(K):
+        flush.zero_()                                   # untimed L2 flush
+        ev_step[s_][0].record(stream)
+        step(ev_stage[s_])
+        ev_step[s_][1].record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    t_wall = time.perf_counter() - t_wall
+    assert tio.device_status(ws, stream) == 0
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    stage_ms = {name: statistics.mean(ev_stage[s_][i].elapsed_time(ev_stage[s_][i + 1])
+                                      for s_ in range(K))
+                for i, name in enumerate(_abi.STAGE_NAMES)}
+    return statistics.mean(step_ms), stage_ms, t_wall
+
+
 def run_ours(args):
     import torch
     rank, world, local = _dist()
@@ -237,73 +285,57 @@ def run_ours(args):
     hd = make_head(wl)
     bt = make_batch(wl, batch_index=rank)           # each replica drafts its own batch
     form = "d2t" if wl.n_emit else "full"
-    head = tio.head_to_device(hd, form, dev)
+    dense_head = tio.head_to_device(hd, form, dev)
     cfg = tio.make_config(wl.B, wl.L_in, wl.H, wl.V, wl.r, wl.top_k, wl.sample_from_anchor,
                           wl.conf_min, wl.dtype, wl.topk_markov)
     hidden = tio.to_device(bt["hidden"], dev)
     anchors = tio.to_device(bt["anchors"], dev)
-    out = tio.Outputs.allocate(wl.B, wl.N, wl.top_k, head.V_head, dev, topk=True, conf=True)
-    ws = tio.workspace_for(cfg, head, dev)
+    out = tio.Outputs.allocate(wl.B, wl.N, wl.top_k, dense_head.V_head, dev, topk=True,
+                               conf=True)
     stream = torch.cuda.current_stream(dev)
     acc = torch.empty(wl.B, dtype=torch.int32, device=dev)
     bonus = torch.empty(wl.B, dtype=torch.int32, device=dev)
     emitted = torch.empty(wl.B, wl.N + 1, dtype=torch.int32, device=dev)
 
     # target tokens: agree with this replica's draft for a seeded geometric prefix
-    tio.propose(cfg, head, hidden, anchors, out, ws, stream)
+    ws_d = tio.workspace_for(cfg, dense_head, dev)
+    tio.propose(cfg, dense_head, hidden, anchors, out, ws_d, stream)
     torch.cuda.synchronize()
     target = tio.to_device(make_target(wl, out.draft.cpu().numpy(), rank), dev)
 
-    def step(events=None):
-        if events is None:
-            tio.propose(cfg, head, hidden, anchors, out, ws, stream)
-        else:
-            _abi.check(_abi.dspark_propose_timed(
-                cfg, head.struct(), hidden.data_ptr(), anchors.data_ptr(), out.struct(),
-                ws.data_ptr(), ws.numel(), stream.cuda_stream, [e.cuda_event for e in events]))
-        tio.verify(out.draft, out.n_draft, target, acc, bonus, emitted, stream)
-
+    # the pruned chain needs the head prepared once (markov_w2 transposed + column norms),
+    # like converting a checkpoint: done before timing
+    head, ws, t_prep = dense_head, ws_d, None
+    if args.chain == "pruned" and wl.dtype == "bf16":
+        head = dataclasses.replace(dense_head)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        head.prepare(cfg, stream)
+        torch.cuda.synchronize()
+        t_prep = time.perf_counter() - t0
+        ws = tio.workspace_for(cfg, head, dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    assert tio.device_status(ws, stream) == 0
+    common = (hidden, anchors, out, target, acc, bonus, emitted, stream, flush)
 
     K = args.steps
-    ns = _abi.DSPARK_NUM_STAGES
-    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
-    ev_stage = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(K)]
-    for evs in ev_stage:          # materialise the handles the library records into
-        for e in evs:
-            e.record(stream)
-    torch.cuda.synchronize()
     clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     clocks.start()
-    _barrier(world)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter()
-    for s in range(K):
-        flush.zero_()                                   # untimed L2 flush
-        ev_step[s][0].record(stream)
-        step(ev_stage[s])
-        ev_step[s][1].record(stream)
-    torch.cuda.synchronize()
-    _barrier(world)
-    t_wall = time.perf_counter() - t_wall
+    ms, stage_ms, t_wall = _time_steps(tio, _abi, cfg, head, ws, *common, K, args.warmup, world)
     clk = clocks.stop()
-    assert tio.device_status(ws, stream) == 0
-
-    step_ms = [a.elapsed_time(b) for a, b in ev_step]
-    stage_ms = {name: statistics.mean(ev_stage[s][i].elapsed_time(ev_stage[s][i + 1])
-                                      for s in range(K))
-                for i, name in enumerate(_abi.STAGE_NAMES)}
-    ms = statistics.mean(step_ms)
     ms_max = _max_over_ranks(ms, world, dev)
     slots = wl.B * wl.N * world
     value = slots / (ms_max / 1e3)
+    launches = _abi.dspark_propose_kernel_count(cfg, head.struct(), out.struct()) + 1
+
+    # the other chain form on the same inputs, for reference
+    other = None
+    if head is not dense_head:
+        ms_o, stage_o, _ = _time_steps(tio, _abi, cfg, dense_head, ws_d, *common,
+                                       max(3, K // 2), args.warmup, world)
+        ms_o = _max_over_ranks(ms_o, world, dev)
+        other = {"chain": "dense", "value": slots / (ms_o / 1e3), "ms_per_step": ms_o,
+                 "stage_us": {k: v * 1e3 for k, v in stage_o.items()}}
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = e2e_host(cfg, head, wl, bt, target, dev, stream, flush, K, args.warmup, world)
@@ -324,6 +356,8 @@ def run_ours(args):
         "verified_blocks_per_s": wl.B * world / (ms_max / 1e3),
         "t_pass_us": ms_max * 1e3,
         "stage_us": {k: v * 1e3 for k, v in stage_ms.items()},
+        "chain": "pruned" if head is not dense_head else "dense",
+        "head_prepare_ms": None if t_prep is None else t_prep * 1e3,
         "pass_roofline": {"t_roof_us": t_roof * 1e6, "frac": t_roof / (ms_max / 1e3),
                           "bytes": alg["bytes"], "flops": alg["flops"],
                           "peaks": peaks["_source"]},
@@ -332,8 +366,8 @@ def run_ours(args):
                      "frac": achieved / peak_tf, "traffic": None,
                      "peak_source": f"{peaks['_source']} bf16 burst"},
         "e2e": e2e,
-        "gpu_launches": K * (_abi.dspark_propose_kernel_count(cfg, head.struct(),
-                                                              out.struct()) + 1),
+        "gpu_launches": K * launches,
+        "other_chain": other,
         "clocks": clk,
         "wall_s_timed_region": t_wall,
     }
@@ -399,6 +433,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_8b_b32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chain", choices=["pruned", "dense"], default="pruned",
+                    help="pruned: exact-bound pruned chain (prepared head); dense: every row")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

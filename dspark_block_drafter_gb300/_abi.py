@@ -36,7 +36,7 @@ class dspark_config(ctypes.Structure):
 class dspark_head(ctypes.Structure):
     _fields_ = [("lm_head", c_ptr), ("lm_bias", c_ptr), ("d2t", c_ptr), ("V_head", c_i32),
                 ("markov_w1", c_ptr), ("markov_w2", c_ptr), ("w_conf", c_ptr),
-                ("b_conf", ctypes.c_float)]
+                ("b_conf", ctypes.c_float), ("prepared", c_ptr)]
 
 
 class dspark_outputs(ctypes.Structure):
@@ -72,6 +72,10 @@ SIGNATURES = {
     "dspark_step_host": (c_i32, [ctypes.POINTER(dspark_config), ctypes.POINTER(dspark_head),
                                  c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
                                  c_ptr, c_ptr, ctypes.c_size_t, c_ptr]),
+    "dspark_prepare_head_size": (ctypes.c_size_t, [ctypes.POINTER(dspark_config),
+                                                   ctypes.POINTER(dspark_head)]),
+    "dspark_prepare_head": (c_i32, [ctypes.POINTER(dspark_config), ctypes.POINTER(dspark_head),
+                                    c_ptr, ctypes.c_size_t, c_ptr]),
     "dspark_verify": (c_i32, [c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "dspark_device_status": (c_i32, [c_ptr, c_ptr]),
     "dspark_status_string": (ctypes.c_char_p, [c_i32]),
@@ -116,6 +120,16 @@ def dspark_propose(cfg: dspark_config, head: dspark_head, hidden: int, anchors: 
                    stream: int = 0) -> int:
     return lib().dspark_propose(ctypes.byref(cfg), ctypes.byref(head), hidden, anchors,
                                 ctypes.byref(out), workspace, workspace_bytes, stream)
+
+
+def dspark_prepare_head_size(cfg: dspark_config, head: dspark_head) -> int:
+    return lib().dspark_prepare_head_size(ctypes.byref(cfg), ctypes.byref(head))
+
+
+def dspark_prepare_head(cfg: dspark_config, head: dspark_head, prepared: int,
+                        prepared_bytes: int, stream: int = 0) -> int:
+    return lib().dspark_prepare_head(ctypes.byref(cfg), ctypes.byref(head), prepared,
+                                     prepared_bytes, stream)
 
 
 DSPARK_NUM_STAGES = 4

@@ -23,7 +23,7 @@ static dspark_status cuda_fail(cudaError_t e, const char* where) {
 
 static constexpr size_t kAlign = 256;
 
-WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype) {
+WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool pruned) {
   WorkspaceLayout w{};
   w.ldz = align_up((size_t)Vh, 64);
   w.Vhp = align_up((size_t)Vh, 128);
@@ -39,6 +39,7 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype) {
   w.keys = take(sizeof(unsigned long long) * (size_t)N * B);
   w.zero_end = off;
   w.z = take(sizeof(float) * (size_t)N * w.Vhp * w.ldb);
+  if (pruned) w.zmax = take(sizeof(float) * (size_t)N * B * (w.Vhp / 128));
   if (dtype == DSPARK_F32) {          // the CUDA-core chain keeps one corrected row per block
     w.zc = take(sizeof(float) * (size_t)B * w.ldz);
     w.prev = take(sizeof(int32_t) * (size_t)B);
@@ -52,6 +53,11 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype) {
 }
 
 static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// The pruned chain runs for bf16 heads that come with a prepared buffer.
+static bool use_pruned(const dspark_config* c, const dspark_head* h) {
+  return c->dtype == DSPARK_BF16 && h->prepared != nullptr;
+}
 
 // Host-side checks; on success fills N and i_first_pred.
 static dspark_status validate(const dspark_config* c, const dspark_head* h, int* N,
@@ -103,7 +109,7 @@ static dspark_status validate(const dspark_config* c, const dspark_head* h, int*
 using namespace dspark;
 
 static_assert(sizeof(dspark_config) == 40, "dspark_config layout");
-static_assert(sizeof(dspark_head) == 64, "dspark_head layout");
+static_assert(sizeof(dspark_head) == 72, "dspark_head layout");
 static_assert(sizeof(dspark_outputs) == 48, "dspark_outputs layout");
 
 extern "C" {
@@ -117,7 +123,8 @@ int32_t dspark_num_slots(const dspark_config* cfg) {
 size_t dspark_propose_workspace_size(const dspark_config* cfg, const dspark_head* head) {
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return 0;
-  return plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype).total;
+  return plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype, use_pruned(cfg, head))
+      .total;
 }
 
 static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* head,
@@ -133,7 +140,8 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
     return fail(DSPARK_ERR_INVALID_ARG, "outputs draft and n_draft are required");
   if (cfg->dtype == DSPARK_BF16 && !aligned(hidden, 16))
     return fail(DSPARK_ERR_INVALID_ARG, "bf16 hidden must be 16-byte aligned");
-  WorkspaceLayout wl = plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype);
+  const bool pruned = use_pruned(cfg, head) && !out->logits;
+  WorkspaceLayout wl = plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype, pruned);
   if (!workspace || !aligned(workspace, 256))
     return fail(DSPARK_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
   if (workspace_bytes < wl.total)
@@ -164,6 +172,14 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   p.part_id = (int32_t*)(ws + wl.part_id);
   p.conf_ws = (float*)(ws + wl.conf);
   p.stream = (cudaStream_t)stream;
+  if (pruned) {
+    const PreparedLayout pl = plan_prepared(head->V_head, cfg->r);
+    const char* pr = (const char*)head->prepared;
+    p.zmax = (float*)(ws + wl.zmax);
+    p.w2t = (const __nv_bfloat16*)(pr + pl.w2t);
+    p.cnorm = (const float*)(pr + pl.cnorm);
+    p.cnmax = (const float*)(pr + pl.cnmax);
+  }
 
   cudaError_t e;
   auto mark = [&](int s) -> cudaError_t {
@@ -178,7 +194,8 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   e = p.dtype == DSPARK_BF16 ? launch_base_logits_tc(p) : launch_base_logits_simt(p);
   if (e != cudaSuccess) return cuda_fail(e, "base logits");
   if ((e = mark(DSPARK_STAGE_CHAIN)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = p.dtype == DSPARK_BF16 ? launch_chain_tc(p) : launch_chain_simt(p);
+  e = p.dtype == DSPARK_F32 ? launch_chain_simt(p)
+                            : (pruned ? launch_chain_pruned(p) : launch_chain_tc(p));
   if (e != cudaSuccess) return cuda_fail(e, "chain");
   if ((e = mark(DSPARK_STAGE_TOPK)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = mark(DSPARK_NUM_STAGES)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -210,6 +227,7 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK || !out) return -1;
   if (cfg->dtype == DSPARK_F32) return 1 + 1 + 2 * N;   // confidence, GEMM, 2 per slot
+  if (use_pruned(cfg, head) && !out->logits) return 3;  // confidence, GEMM, pruned chain
   const bool topk = out->topk_ids || out->topk_vals;
   return 1 /* confidence */ + 1 /* GEMM */ + (cfg->B + 31) / 32 /* chain, 32 blocks each */ +
          (topk ? 1 : 0);
@@ -240,7 +258,10 @@ static StageLayout plan_stage(const dspark_config* c, int N, size_t base) {
 size_t dspark_step_host_workspace_size(const dspark_config* cfg, const dspark_head* head) {
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return 0;
-  return plan_stage(cfg, N, plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype).total)
+  return plan_stage(cfg, N,
+                    plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype,
+                                   use_pruned(cfg, head))
+                        .total)
       .total;
 }
 
@@ -255,7 +276,8 @@ dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head
   if (st != DSPARK_OK) return st;
   if (!hidden_h || !anchors_h || !target_h || !draft_h || !n_draft_h || !accepted_h || !bonus_h)
     return fail(DSPARK_ERR_INVALID_ARG, "a required host buffer is NULL");
-  size_t base = plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype).total;
+  size_t base =
+      plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype, use_pruned(cfg, head)).total;
   StageLayout s = plan_stage(cfg, N, base);
   if (!workspace || !aligned(workspace, 256))
     return fail(DSPARK_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
@@ -326,6 +348,31 @@ dspark_status dspark_device_status(void* workspace, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
   if (word & kErrTimeout) return fail(DSPARK_ERR_TIMEOUT, "a device-side wait timed out");
   return fail(DSPARK_ERR_DEVICE, "a kernel saw a token outside [0, V)");
+}
+
+size_t dspark_prepare_head_size(const dspark_config* cfg, const dspark_head* head) {
+  int N, ifp;
+  if (validate(cfg, head, &N, &ifp) != DSPARK_OK || cfg->dtype != DSPARK_BF16) return 0;
+  return plan_prepared(head->V_head, cfg->r).total;
+}
+
+dspark_status dspark_prepare_head(const dspark_config* cfg, const dspark_head* head,
+                                  void* prepared, size_t prepared_bytes, void* stream) {
+  int N, ifp;
+  dspark_status st = validate(cfg, head, &N, &ifp);
+  if (st != DSPARK_OK) return st;
+  if (cfg->dtype != DSPARK_BF16)
+    return fail(DSPARK_ERR_UNSUPPORTED, "head preparation is for the bf16 path");
+  const PreparedLayout pl = plan_prepared(head->V_head, cfg->r);
+  if (!prepared || !aligned(prepared, 256))
+    return fail(DSPARK_ERR_WORKSPACE, "prepared buffer must be non-NULL and 256-byte aligned");
+  if (prepared_bytes < pl.total)
+    return fail(DSPARK_ERR_WORKSPACE,
+                "prepared buffer too small: need " + std::to_string(pl.total) + " bytes");
+  cudaError_t e = launch_prepare_head(head->markov_w2, cfg->r, head->V_head, prepared,
+                                      (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "head preparation");
+  return DSPARK_OK;
 }
 
 const char* dspark_status_string(int32_t s) {

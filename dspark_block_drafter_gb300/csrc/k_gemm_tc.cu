@@ -42,6 +42,7 @@ constexpr long long kWaitBudget = 2000000000ll;       // ~1 s of SM clocks
 struct GemmArgs {
   float* z;
   size_t Vhp, ldb;
+  float* zmax;     // [N][B][v_tiles] per-tile maxima of z, or NULL
   const float* bias;
   uint32_t* err;
   int B, N, ifp, Vh;
@@ -76,8 +77,13 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
   uint64_t* acc_full = empty + g.stages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = (uint32_t*)(drain + 1);
+  uint64_t* tile_bar = drain + 1;                         // epilogue warps, per tile
+  uint32_t* tmem_slot = (uint32_t*)(tile_bar + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  // tile maxima: a padded 32 x 32 transpose panel per epilogue warp, and the four
+  // warps' column maxima, double-buffered by tile parity
+  float* s_panel = (float*)((uint8_t*)smem + g.stages * (kStageA + b_stage) + 256);
+  float* s_cmax = s_panel + 4 * 32 * 33;                 // [2][4][256]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -90,6 +96,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       ptx::mbar_init(&acc_empty[a], 128);
     }
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(tile_bar, 128);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -201,10 +208,24 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       const int v = vt * kBlockV + warp * 32 + lane;
       const bool live = v < g.Vh;
       const float bias_v = (g.bias && live) ? g.bias[v] : 0.f;
+      float* cmax = s_cmax + (local & 1) * 4 * 256;
       for (int c0 = 0; c0 < rows; c0 += 32) {
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(tmem + lane_base + acc * (uint32_t)g.acc_stride + c0, r);
         ptx::tmem_ld_wait();
+        if (g.zmax) {
+          // column maxima over this warp's 32 head rows, through a transpose panel
+          float* panel = s_panel + warp * 32 * 33;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            panel[j * 33 + lane] = live ? __uint_as_float(r[j]) + bias_v : -INFINITY;
+          __syncwarp();
+          float m = -INFINITY;
+#pragma unroll 8
+          for (int q = 0; q < 32; ++q) m = fmaxf(m, panel[lane * 33 + q]);
+          cmax[warp * 256 + c0 + lane] = m;
+          __syncwarp();
+        }
         if (!live) continue;
         if ((g.BB & 3) == 0) {
           // runs of four consecutive blocks of one slot: 16-byte stores
@@ -232,6 +253,23 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&acc_empty[acc]);
+      if (g.zmax) {
+        // the four warps' maxima are in (a bounded wait, so that a warp that gave up
+        // cannot strand the others)
+        ptx::mbar_arrive(tile_bar);
+        if (!ptx::mbar_wait(tile_bar, local & 1, kWaitBudget, abort_flag)) {
+          give_up();
+          break;
+        }
+        for (int c = threadIdx.x; c < rows; c += 128) {
+          const int il = c / g.BB, bl = c % g.BB;
+          if (bl < nb) {
+            const float m = fmaxf(fmaxf(cmax[c], cmax[256 + c]),
+                                  fmaxf(cmax[512 + c], cmax[768 + c]));
+            g.zmax[((size_t)(i0 + il) * g.B + bb0 + bl) * g.v_tiles + vt] = m;
+          }
+        }
+      }
     }
   }
   __syncwarp();
@@ -286,6 +324,7 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   g.z = p.z;
   g.Vhp = p.Vhp;
   g.ldb = p.ldb;
+  g.zmax = p.zmax;
   g.bias = p.lm_bias;
   g.err = p.ctrl;
   g.B = p.B;
@@ -300,7 +339,7 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   g.v_tiles = (p.Vh + kBlockV - 1) / kBlockV;
   g.num_kb = (p.H + kBlockK - 1) / kBlockK;
   const uint32_t stage_bytes = kStageA + (uint32_t)g.bn_mma * kBlockK * 2;
-  const size_t smem_budget = 220 * 1024;
+  const size_t smem_budget = 220 * 1024 - (4 * 32 * 33 + 2 * 4 * 256) * sizeof(float);
   g.stages = (int)std::min<size_t>(8, (smem_budget - 1024 - 256) / stage_bytes);
   // 32-column TMEM loads may run past the last valid column of an accumulator, so
   // each accumulator owns a multiple of 32 columns
@@ -308,7 +347,8 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   uint32_t cols = 32;
   while (cols < 2u * (uint32_t)g.acc_stride) cols <<= 1;
   g.tmem_cols = cols;
-  const size_t smem = 1024 + (size_t)g.stages * stage_bytes + 256;
+  const size_t smem = 1024 + (size_t)g.stages * stage_bytes + 256 +
+                      (4 * 32 * 33 + 2 * 4 * 256) * sizeof(float);
 
   CUtensorMap tm_w, tm_h;
   {

@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI layer and the kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -35,6 +36,10 @@ struct ProposePlan {
   unsigned long long* keys;  // [N][B] order keys of each slot's winner
   float* part_val;      // [N][B][kChainMaxCtas][k] per-CTA top-k partials
   int32_t* part_id;
+  float* zmax;          // per-tile maxima of z [N][B][Vhp / 128], or NULL (dense chain)
+  const __nv_bfloat16* w2t;   // prepared head: markov_w2 transposed [Vhp][r], or NULL
+  const float* cnorm;   // prepared head: column norms of markov_w2 [Vhp]
+  const float* cnmax;   // prepared head: per-tile maxima of cnorm [Vhp / 128]
   float* z;             // base logits [N][Vhp][ldb]: slot, head row, block (fastest)
   size_t Vhp, ldb;      // head rows rounded up to whole 128-row tiles; blocks rounded to 4
   size_t ldz;           // row stride of zc
@@ -50,10 +55,22 @@ constexpr int kChainMaxCtas = 256;
 // Workspace carve-up shared by the size query and the launch.  [ctrl, zero_end) is
 // cleared at the start of every call.
 struct WorkspaceLayout {
-  size_t ctrl, bar, keys, zero_end, z, zc, prev, conf, part_val, part_id, total;
+  size_t ctrl, bar, keys, zero_end, z, zmax, zc, prev, conf, part_val, part_id, total;
   size_t Vhp, ldb, ldz;
 };
-WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype);
+WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool pruned);
+
+// Layout of a prepared head (dspark_prepare_head): markov_w2 transposed to [Vhp][r]
+// bf16, the fp32 Euclidean norm of every markov_w2 column [Vhp] (0 past V_head), and the
+// maximum of those norms over each 128-row tile [Vhp / 128].
+struct PreparedLayout {
+  size_t w2t, cnorm, cnmax, total;
+  size_t Vhp, tiles;
+};
+PreparedLayout plan_prepared(int Vh, int r);
+cudaError_t launch_prepare_head(const void* w2, int r, int Vh, void* prepared,
+                                cudaStream_t stream);
+cudaError_t launch_chain_pruned(const ProposePlan& p);
 
 // Blocking of the lm_head GEMM's N dimension: a tile holds Ni slots x BB blocks of
 // prediction rows (blocks fastest; padded to bn_mma, a multiple of 16, at most 256);

@@ -52,6 +52,7 @@ class Head:
     d2t: Optional[torch.Tensor] = None
     w_conf: Optional[torch.Tensor] = None
     b_conf: float = 0.0
+    prepared: Optional[torch.Tensor] = None
 
     @property
     def V_head(self) -> int:
@@ -62,7 +63,19 @@ class Head:
                                 d2t=_ptr(self.d2t), V_head=self.V_head,
                                 markov_w1=_ptr(self.markov_w1),
                                 markov_w2=_ptr(self.markov_w2), w_conf=_ptr(self.w_conf),
-                                b_conf=float(self.b_conf))
+                                b_conf=float(self.b_conf), prepared=_ptr(self.prepared))
+
+    def prepare(self, cfg, stream=None) -> "Head":
+        """Fill ``prepared`` with dspark_prepare_head (enables the pruned chain)."""
+        bare = dataclasses.replace(self, prepared=None)
+        n = _abi.dspark_prepare_head_size(cfg, bare.struct())
+        if n == 0:
+            _abi.check(_abi.DSPARK_ERR_UNSUPPORTED)
+        buf = torch.empty(n, dtype=torch.uint8, device=self.lm_head.device)
+        _abi.check(_abi.dspark_prepare_head(cfg, bare.struct(), buf.data_ptr(), n,
+                                            _stream(stream)))
+        self.prepared = buf
+        return self
 
 
 def head_to_device(h: dict, form: str = "full", device="cuda") -> Head:

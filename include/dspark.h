@@ -94,6 +94,12 @@ typedef struct dspark_head {
   const void* w_conf;         /* device [H], dtype, or NULL (no confidence head:
                                  conf output is not written, n_draft = N) */
   float b_conf;
+  const void* prepared;       /* device buffer filled by dspark_prepare_head() for these
+                                 weights, or NULL.  With it (bf16 only), the chain runs
+                                 the exact-bound pruned form: same results, the Markov
+                                 term evaluated only where it can change them.  Without
+                                 it, or when the logits output is requested, the chain
+                                 evaluates every head row (dense form). */
 } dspark_head;
 
 /* Outputs of dspark_propose (device memory).  N = dspark_num_slots(cfg). */
@@ -154,6 +160,22 @@ dspark_status dspark_verify(int32_t B, int32_t N, const int32_t* draft,
                             const int32_t* n_draft, const int32_t* target,
                             int32_t* accepted, int32_t* bonus, int32_t* emitted,
                             void* stream);
+
+/* Bytes of the buffer dspark_prepare_head() fills for this head (bf16 only; 0 on invalid
+   input or fp32).  Layout: markov_w2 transposed [round_up(V_head, 128)][r] bf16, the fp32
+   Euclidean norm of every markov_w2 column, and their maximum over each 128-row tile. */
+size_t dspark_prepare_head_size(const dspark_config* cfg, const dspark_head* head);
+
+/*
+ * dspark_prepare_head -- one-time preparation of a head's Markov weights for the pruned
+ * chain (the weights are constant across calls, like a converted checkpoint).
+ *
+ * prepared  device buffer of dspark_prepare_head_size() bytes, 256-byte aligned, owned by
+ *           the caller; pass it as head->prepared to later dspark_propose calls.  It must
+ *           be re-prepared if markov_w2 changes.  head->prepared itself is ignored here.
+ */
+dspark_status dspark_prepare_head(const dspark_config* cfg, const dspark_head* head,
+                                  void* prepared, size_t prepared_bytes, void* stream);
 
 /* Stages of dspark_propose, in launch order, for dspark_propose_timed(). */
 enum {

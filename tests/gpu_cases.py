@@ -10,13 +10,21 @@ from workloads import make_batch, make_head
 TOL = {"f32": 1e-5, "bf16": 2e-2}
 
 
-def gpu_propose(wl, hd, bt, form="full", want_logits=False, want_topk=True, stream=None):
-    """Run dspark_propose on the GPU; returns (numpy outputs, workspace tensor)."""
+def gpu_propose(wl, hd, bt, form="full", want_logits=False, want_topk=True, stream=None,
+                chain="dense"):
+    """Run dspark_propose on the GPU; returns (numpy outputs, workspace tensor).
+
+    chain "dense" evaluates every head row; "pruned" prepares the head first so that the
+    exact-bound pruned chain runs (it needs the logits output off).
+    """
     import torch
     from dspark_block_drafter_gb300 import torch_io as tio
     cfg = tio.make_config(wl.B, wl.L_in, wl.H, wl.V, wl.r, wl.top_k, wl.sample_from_anchor,
                           wl.conf_min, wl.dtype, wl.topk_markov)
     head = tio.head_to_device(hd, form)
+    if chain == "pruned":
+        assert not want_logits
+        head.prepare(cfg)
     hidden = tio.to_device(bt["hidden"])
     anchors = tio.to_device(bt["anchors"])
     out = tio.Outputs.allocate(wl.B, wl.N, wl.top_k, head.V_head, topk=want_topk,
@@ -48,10 +56,10 @@ def compare(wl, hd, bt, o, g, form="full"):
     return rep
 
 
-def run_case(wl, form="full", want_logits=True, hd=None, bt=None):
+def run_case(wl, form="full", want_logits=True, hd=None, bt=None, chain="dense"):
     hd = make_head(wl) if hd is None else hd
     bt = make_batch(wl) if bt is None else bt
-    g, _ = gpu_propose(wl, hd, bt, form, want_logits)
+    g, _ = gpu_propose(wl, hd, bt, form, want_logits and chain == "dense", chain=chain)
     o = oracle_run(wl, hd, bt)
     rep = compare(wl, hd, bt, o, g, form)
     assert rep["failures"] == [], rep

@@ -111,5 +111,5 @@ def test_status_strings(lib):
 def test_struct_layouts_match_c():
     # pointer-sized fields are 8 bytes on both hosts; the int/float fields pack as in C
     assert ctypes.sizeof(_abi.dspark_config) == 40
-    assert ctypes.sizeof(_abi.dspark_head) == 64
+    assert ctypes.sizeof(_abi.dspark_head) == 72
     assert ctypes.sizeof(_abi.dspark_outputs) == 48

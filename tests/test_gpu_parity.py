@@ -30,6 +30,9 @@ def test_tiny_fp32_workload():
     assert rep["slots"] == 8
 
 
+CHAINS = ["dense", "pruned"]
+
+
 @pytest.mark.parametrize("sfa", [True, False])
 @pytest.mark.parametrize("topk_markov", [True, False])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -37,28 +40,47 @@ def test_small_dense(sfa, topk_markov, dtype):
     run_case(_small(sample_from_anchor=sfa, topk_markov=topk_markov, dtype=dtype))
 
 
+@pytest.mark.parametrize("sfa", [True, False])
+@pytest.mark.parametrize("topk_markov", [True, False])
+@pytest.mark.parametrize("k", [1, 5, 32])
+def test_small_pruned(sfa, topk_markov, k):
+    run_case(_small(sample_from_anchor=sfa, topk_markov=topk_markov, top_k=k), chain="pruned")
+
+
+@pytest.mark.parametrize("chain", CHAINS)
+def test_pruned_loose_bounds_many_candidates(chain):
+    # large Markov weights: the Cauchy-Schwarz bounds admit most rows, so the pruned
+    # chain has to evaluate and reduce its candidate buffer many times
+    wl = _small(B=5, L_in=4, H=64, V=8192, r=64, top_k=8, weight_std=1.0, seed=77)
+    run_case(wl, chain=chain)
+
+
+@pytest.mark.parametrize("chain", CHAINS)
 @pytest.mark.parametrize("form", ["full", "d2t"])
 @pytest.mark.parametrize("sfa", [True, False])
-def test_small_reduced_vocab(form, sfa):
+def test_small_reduced_vocab(form, sfa, chain):
     wl = _small(n_emit=304, sample_from_anchor=sfa, V=1024)
-    g, o, rep = run_case(wl, form)
+    g, o, rep = run_case(wl, form, chain=chain)
     emit = set(make_head(wl)["emit_rows"].tolist())
     assert set(g["draft"].ravel().tolist()) <= emit
     assert set(g["topk_ids"].ravel().tolist()) <= emit
 
 
-def test_single_block_single_slot():
-    run_case(_small(B=1, L_in=1, top_k=3))
+@pytest.mark.parametrize("chain", CHAINS)
+def test_single_block_single_slot(chain):
+    run_case(_small(B=1, L_in=1, top_k=3), chain=chain)
 
 
-def test_topk_equals_head_rows():
+@pytest.mark.parametrize("chain", CHAINS)
+def test_topk_equals_head_rows(chain):
     # k = V_head: every row is a candidate; ragged tiny vocabulary
     wl = _small(V=1000, n_emit=32, top_k=32, L_in=3)
-    run_case(wl, "d2t")
+    run_case(wl, "d2t", chain=chain)
 
 
-def test_large_rank_and_many_blocks():
-    run_case(_small(B=40, L_in=3, r=300, H=136, V=520, top_k=2))
+@pytest.mark.parametrize("chain", CHAINS)
+def test_large_rank_and_many_blocks(chain):
+    run_case(_small(B=40, L_in=3, r=300, H=136, V=520, top_k=2), chain=chain)
 
 
 def test_anchor_is_last_token():
@@ -126,6 +148,7 @@ def test_full_size_workload(name):
     forms = ["full", "d2t"] if wl.n_emit else ["full"]
     o = oracle_run(wl, hd, bt)
     for form in forms:
-        g, _ = gpu_propose(wl, hd, bt, form)
-        rep = compare(wl, hd, bt, o, g, form)
-        assert rep["failures"] == [], (form, rep)
+        for chain in CHAINS:
+            g, _ = gpu_propose(wl, hd, bt, form, chain=chain)
+            rep = compare(wl, hd, bt, o, g, form)
+            assert rep["failures"] == [], (form, chain, rep)
