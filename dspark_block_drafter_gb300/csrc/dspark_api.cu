@@ -37,9 +37,13 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
   w.ctrl = take(256);
   w.bar = take(sizeof(unsigned) * (size_t)((B + 31) / 32));
   w.keys = take(sizeof(unsigned long long) * (size_t)N * B);
+  if (pruned) w.cand_n = take(sizeof(int32_t) * (size_t)N * B);
   w.zero_end = off;
   w.z = take(sizeof(float) * (size_t)N * w.Vhp * w.ldb);
-  if (pruned) w.zmax = take(sizeof(float) * (size_t)N * B * (w.Vhp / 128));
+  if (pruned) {
+    w.zmax = take(sizeof(float) * (size_t)N * B * (w.Vhp / 128));
+    w.cand = take(pruned_list_bytes(B, N));
+  }
   if (dtype == DSPARK_F32) {          // the CUDA-core chain keeps one corrected row per block
     w.zc = take(sizeof(float) * (size_t)B * w.ldz);
     w.prev = take(sizeof(int32_t) * (size_t)B);
@@ -56,7 +60,7 @@ static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 // The pruned chain runs for bf16 heads that come with a prepared buffer.
 static bool use_pruned(const dspark_config* c, const dspark_head* h) {
-  return c->dtype == DSPARK_BF16 && h->prepared != nullptr;
+  return c->dtype == DSPARK_BF16 && h->prepared != nullptr && c->r % 8 == 0;
 }
 
 // Host-side checks; on success fills N and i_first_pred.
@@ -179,6 +183,10 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
     p.w2t = (const __nv_bfloat16*)(pr + pl.w2t);
     p.cnorm = (const float*)(pr + pl.cnorm);
     p.cnmax = (const float*)(pr + pl.cnmax);
+    p.w1max = (const unsigned*)(pr + pl.w1max);
+    p.cand_n = (int32_t*)(ws + wl.cand_n);
+    p.cand_v = (int32_t*)(ws + wl.cand);
+    p.cand_z = (float*)(ws + wl.cand + pruned_list_bytes(cfg->B, N) / 2);   // after cand_v
   }
 
   cudaError_t e;
@@ -227,7 +235,7 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK || !out) return -1;
   if (cfg->dtype == DSPARK_F32) return 1 + 1 + 2 * N;   // confidence, GEMM, 2 per slot
-  if (use_pruned(cfg, head) && !out->logits) return 3;  // confidence, GEMM, pruned chain
+  if (use_pruned(cfg, head) && !out->logits) return 4;  // confidence, GEMM, candidates, chain
   const bool topk = out->topk_ids || out->topk_vals;
   return 1 /* confidence */ + 1 /* GEMM */ + (cfg->B + 31) / 32 /* chain, 32 blocks each */ +
          (topk ? 1 : 0);
@@ -369,8 +377,8 @@ dspark_status dspark_prepare_head(const dspark_config* cfg, const dspark_head* h
   if (prepared_bytes < pl.total)
     return fail(DSPARK_ERR_WORKSPACE,
                 "prepared buffer too small: need " + std::to_string(pl.total) + " bytes");
-  cudaError_t e = launch_prepare_head(head->markov_w2, cfg->r, head->V_head, prepared,
-                                      (cudaStream_t)stream);
+  cudaError_t e = launch_prepare_head(head->markov_w1, head->markov_w2, cfg->V, cfg->r,
+                                      head->V_head, prepared, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "head preparation");
   return DSPARK_OK;
 }

@@ -40,6 +40,10 @@ struct ProposePlan {
   const __nv_bfloat16* w2t;   // prepared head: markov_w2 transposed [Vhp][r], or NULL
   const float* cnorm;   // prepared head: column norms of markov_w2 [Vhp]
   const float* cnmax;   // prepared head: per-tile maxima of cnorm [Vhp / 128]
+  const unsigned* w1max;  // prepared head: max row norm of markov_w1 (float bits)
+  int32_t* cand_v;      // pruned chain: candidate head rows [N][B][cap]
+  float* cand_z;        //               their base logits
+  int32_t* cand_n;      //               candidate counts [N][B] (zeroed per call)
   float* z;             // base logits [N][Vhp][ldb]: slot, head row, block (fastest)
   size_t Vhp, ldb;      // head rows rounded up to whole 128-row tiles; blocks rounded to 4
   size_t ldz;           // row stride of zc
@@ -55,21 +59,24 @@ constexpr int kChainMaxCtas = 256;
 // Workspace carve-up shared by the size query and the launch.  [ctrl, zero_end) is
 // cleared at the start of every call.
 struct WorkspaceLayout {
-  size_t ctrl, bar, keys, zero_end, z, zmax, zc, prev, conf, part_val, part_id, total;
+  size_t ctrl, bar, keys, cand_n, zero_end, z, zmax, cand, zc, prev, conf, part_val, part_id,
+      total;
   size_t Vhp, ldb, ldz;
 };
 WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool pruned);
 
 // Layout of a prepared head (dspark_prepare_head): markov_w2 transposed to [Vhp][r]
-// bf16, the fp32 Euclidean norm of every markov_w2 column [Vhp] (0 past V_head), and the
-// maximum of those norms over each 128-row tile [Vhp / 128].
+// bf16, the fp32 Euclidean norm of every markov_w2 column [Vhp] (0 past V_head), the
+// maximum of those norms over each 128-row tile [Vhp / 128], and the largest norm of a
+// markov_w1 row (one float).
 struct PreparedLayout {
-  size_t w2t, cnorm, cnmax, total;
+  size_t w2t, cnorm, cnmax, w1max, total;
   size_t Vhp, tiles;
 };
 PreparedLayout plan_prepared(int Vh, int r);
-cudaError_t launch_prepare_head(const void* w2, int r, int Vh, void* prepared,
-                                cudaStream_t stream);
+size_t pruned_list_bytes(int B, int N);   // candidate lists of the pruned chain
+cudaError_t launch_prepare_head(const void* w1, const void* w2, int V, int r, int Vh,
+                                void* prepared, cudaStream_t stream);
 cudaError_t launch_chain_pruned(const ProposePlan& p);
 
 // Blocking of the lm_head GEMM's N dimension: a tile holds Ni slots x BB blocks of
