@@ -47,6 +47,18 @@ def test_small_pruned(sfa, topk_markov, k):
     run_case(_small(sample_from_anchor=sfa, topk_markov=topk_markov, top_k=k), chain="pruned")
 
 
+@pytest.mark.parametrize("shape", [
+    dict(B=4, L_in=8),                                  # 32 prediction rows per tile
+    dict(B=2, L_in=16, V=1000),                         # ragged vocabulary tail
+    dict(B=16, L_in=3, sample_from_anchor=False),       # 1+N layout, 2 slots
+    dict(B=32, L_in=16, H=520, V=777 * 8),              # ragged K, several tiles
+])
+@pytest.mark.parametrize("chain", CHAINS)
+def test_even_slot_shapes(shape, chain):
+    # whole-block tiles of 32 prediction rows, ragged vocabulary and K tails
+    run_case(_small(**shape), chain=chain)
+
+
 @pytest.mark.parametrize("chain", CHAINS)
 def test_pruned_loose_bounds_many_candidates(chain):
     # large Markov weights: the Cauchy-Schwarz bounds admit most rows, so the pruned
