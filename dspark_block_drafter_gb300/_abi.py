@@ -76,6 +76,9 @@ SIGNATURES = {
                                                    ctypes.POINTER(dspark_head)]),
     "dspark_prepare_head": (c_i32, [ctypes.POINTER(dspark_config), ctypes.POINTER(dspark_head),
                                     c_ptr, ctypes.c_size_t, c_ptr]),
+    "dspark_propose_noalloc": (c_i32, [ctypes.POINTER(dspark_config),
+                                       ctypes.POINTER(dspark_head), c_ptr, c_ptr,
+                                       ctypes.POINTER(dspark_outputs), c_ptr]),
     "dspark_verify": (c_i32, [c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "dspark_device_status": (c_i32, [c_ptr, c_ptr]),
     "dspark_status_string": (ctypes.c_char_p, [c_i32]),
@@ -163,6 +166,13 @@ def dspark_step_host(cfg: dspark_config, head: dspark_head, hidden_h: int, ancho
     return lib().dspark_step_host(ctypes.byref(cfg), ctypes.byref(head), hidden_h, anchors_h,
                                   target_h, draft_h, n_draft_h, accepted_h, bonus_h,
                                   topk_ids_h, topk_vals_h, workspace, workspace_bytes, stream)
+
+
+def dspark_propose_noalloc(cfg: dspark_config, head: dspark_head, hidden: int, anchors: int,
+                           out: dspark_outputs, stream: int = 0) -> int:
+    """dspark_propose with the library's built-in 16 MiB scratch (no workspace)."""
+    return lib().dspark_propose_noalloc(ctypes.byref(cfg), ctypes.byref(head), hidden, anchors,
+                                        ctypes.byref(out), stream)
 
 
 def dspark_verify(B: int, N: int, draft: int, n_draft: int, target: int, accepted: int,

@@ -1,6 +1,7 @@
 // The C ABI: argument validation, workspace carve-up and kernel dispatch.
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "../../include/dspark.h"
@@ -397,5 +398,59 @@ const char* dspark_status_string(int32_t s) {
 }
 
 const char* dspark_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ no-allocation entry
+// Scratch for dspark_propose_noalloc: a fixed array in device memory that exists on every
+// GPU that loads this library, from the load until the process exits.  Host code must not
+// pass `g_noalloc_scratch` itself to a kernel: on the host that name is only a stand-in,
+// so the device address is looked up once per device with cudaGetSymbolAddress.
+static constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" {
+
+dspark_status dspark_propose_noalloc(const dspark_config* cfg, const dspark_head* head,
+                                     const void* hidden, const int32_t* anchors,
+                                     const dspark_outputs* out, void* stream) {
+  const size_t need = dspark_propose_workspace_size(cfg, head);
+  if (need == 0) {
+    int N, ifp;
+    return validate(cfg, head, &N, &ifp);     // sets the message of the failing check
+  }
+  if (need > kNoAllocScratchBytes)
+    return fail(DSPARK_ERR_WORKSPACE,
+                "this call needs " + std::to_string(need) +
+                    " bytes of scratch; the built-in scratch of dspark_propose_noalloc holds " +
+                    std::to_string(kNoAllocScratchBytes) +
+                    " bytes (use dspark_propose with a caller workspace)");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(DSPARK_ERR_UNSUPPORTED, "device ordinal beyond the supported range");
+  void* scratch;
+  {
+    // first call on this device (which is current): resolve the array's device address
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
+      g_noalloc_ptr[dev] = ptr;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  // the control words that must start at zero are cleared by dspark_propose itself
+  return propose_impl(cfg, head, hidden, anchors, out, scratch, kNoAllocScratchBytes, stream,
+                      nullptr);
+}
 
 }  // extern "C"

@@ -227,6 +227,33 @@ dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head
                                int32_t* topk_ids_h, float* topk_vals_h,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * dspark_propose_noalloc -- dspark_propose for callers that cannot allocate device memory.
+ *
+ * (No counterpart on the pages: an interface addition of this library.)  Some callers
+ * cannot call cudaMalloc or any allocating routine: code that runs inside a host
+ * framework owning every allocation, allocator-free plugins, or callers that must not
+ * touch the allocator while the device is in use elsewhere.  This entry point takes the
+ * same arguments as dspark_propose minus the workspace: its scratch is a fixed 16 MiB
+ * array of device memory built into the library, which every GPU that loads the library
+ * holds until the process exits.  It allocates nothing itself.
+ *
+ *   - Calls whose dspark_propose_workspace_size() exceeds 16 MiB return
+ *     DSPARK_ERR_WORKSPACE before launching anything (small batches and vocabularies
+ *     only; larger ones need dspark_propose and a caller workspace).
+ *   - The first call on a device looks up the scratch's device address (with that device
+ *     current) and keeps it; make that first call before any stream capture.
+ *   - Every call on a device shares the one scratch array, which keeps the contents the
+ *     last call left (each call clears what has to start at zero).  Calls that overlap on
+ *     the GPU -- on different streams, or from different host threads without ordering --
+ *     race on it and give wrong results: order them on one stream.
+ *   - Device-side error words land in that shared scratch and are not readable through
+ *     dspark_device_status().
+ */
+dspark_status dspark_propose_noalloc(const dspark_config* cfg, const dspark_head* head,
+                                     const void* hidden, const int32_t* anchors,
+                                     const dspark_outputs* out, void* stream);
+
 /* Synchronises `stream`, reads the sticky device error word of a workspace used by
    dspark_propose, and clears it.  DSPARK_OK when no kernel flagged anything. */
 dspark_status dspark_device_status(void* workspace, void* stream);
