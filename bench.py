@@ -101,23 +101,29 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9 and parts[1].isdigit():
-                    rows.append(parts)
-        if not rows:
-            return None
-        sm = [int(r[1]) for r in rows]
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            for n, v in zip(names, r[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]),
-                "samples": len(rows), "reasons": sorted(reasons)}
+            return parse_clocks(f)
+
+
+def parse_clocks(lines):
+    """Summary of nvidia-smi samples (the query columns of ClockSampler.Q, no header):
+    median SM clock, the maximum clock, and every throttle reason seen active."""
+    rows = []
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) >= 9 and parts[1].isdigit():
+            rows.append(parts)
+    if not rows:
+        return None
+    sm = [int(r[1]) for r in rows]
+    reasons = set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in rows:
+        for n, v in zip(names, r[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]),
+            "samples": len(rows), "reasons": sorted(reasons)}
 
 
 def _dist():
@@ -127,14 +133,26 @@ def _dist():
     return rank, world, local
 
 
-def _max_over_ranks(x: float, world: int, device=None) -> float:
+def _reduce_over_ranks(x: float, world: int, op: str, device=None) -> float:
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
     t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def _max_over_ranks(x: float, world: int, device=None) -> float:
+    return _reduce_over_ranks(x, world, "max", device)
+
+
+def job_throughput(ms_local: float, units_local: float, world: int, device=None):
+    """(step ms, units/s) of the whole job: every rank runs its own replica, the step
+    time is the slowest rank's and the throughput counts the units of all ranks."""
+    ms_max = _reduce_over_ranks(ms_local, world, "max", device)
+    units = _reduce_over_ranks(units_local, world, "sum", device)
+    return ms_max, units / (ms_max / 1e3)
 
 
 def _barrier(world):
@@ -323,9 +341,8 @@ def run_ours(args):
     clocks.start()
     ms, stage_ms, t_wall = _time_steps(tio, _abi, cfg, head, ws, *common, K, args.warmup, world)
     clk = clocks.stop()
-    ms_max = _max_over_ranks(ms, world, dev)
+    ms_max, value = job_throughput(ms, wl.B * wl.N, world, dev)
     slots = wl.B * wl.N * world
-    value = slots / (ms_max / 1e3)
     launches = _abi.dspark_propose_kernel_count(cfg, head.struct(), out.struct()) + 1
 
     # the other chain form on the same inputs, for reference

@@ -1,0 +1,101 @@
+"""The benchmark's multi-process host logic on the CPU: two `gloo` ranks.
+
+Blocks are independent, so under torchrun every rank runs its own replica and nothing
+crosses ranks on the data path.  What the ranks do share is host logic: the step time is
+the slowest rank's, the throughput counts every rank's slots, and the reference arm
+runs on rank 0 alone.  These tests run that logic with world_size 2 over gloo.
+"""
+import contextlib
+import io
+import json
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _init(rank, world, port):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+
+
+def _throughput_worker(rank, world, port, results):
+    _init(rank, world, port)
+    try:
+        ms = [1.0, 2.5][rank]           # rank 1 is the slow one
+        slots = [512, 512][rank]
+        results[rank] = bench.job_throughput(ms, slots, world)
+    finally:
+        dist.destroy_process_group()
+
+
+def _reference_worker(rank, world, port, results):
+    _init(rank, world, port)
+    try:
+        buf = io.StringIO()
+        with contextlib.redirect_stdout(buf):
+            rc = bench.main(["--impl", "reference", "--workload", "tiny_fp32", "--steps", "1",
+                             "--warmup", "3", "--gpus", str(world)])
+        results[rank] = (rc, buf.getvalue())
+    finally:
+        dist.destroy_process_group()
+
+
+def _spawn(fn, world=2):
+    port = _free_port()
+    with mp.Manager() as m:
+        results = m.dict()
+        mp.spawn(fn, args=(world, port, results), nprocs=world, join=True)
+        return dict(results)
+
+
+def test_job_throughput_takes_slowest_rank_and_all_slots():
+    res = _spawn(_throughput_worker)
+    for rank in (0, 1):
+        ms, value = res[rank]
+        assert ms == 2.5                                 # the slowest rank's step
+        assert value == pytest.approx(1024 / 2.5e-3)     # both ranks' slots
+
+
+def test_job_throughput_single_process_needs_no_group():
+    assert bench.job_throughput(2.0, 512, 1) == (2.0, 512 / 2e-3)
+
+
+def test_reference_arm_runs_on_rank0_only():
+    res = _spawn(_reference_worker)
+    rc0, out0 = res[0]
+    rc1, out1 = res[1]
+    assert rc0 == 0 and rc1 == 0
+    assert out1 == ""                                     # the other rank does no work
+    lines = [json.loads(x) for x in out0.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    line = lines[0]
+    assert line["impl"] == "reference" and line["unit"] == "slots/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_parse_clocks_reports_median_and_reasons():
+    rows = [
+        "0, 1900, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 2000, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 1950, 2070, 1350.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "garbage line",
+    ]
+    c = bench.parse_clocks(rows)
+    assert c == {"sm_mhz": 1950, "sm_max_mhz": 2070, "samples": 3,
+                 "reasons": ["sw_power_cap"]}
+    assert bench.parse_clocks([]) is None
