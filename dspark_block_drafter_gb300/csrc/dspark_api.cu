@@ -38,12 +38,11 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
   w.ctrl = take(256);
   w.bar = take(sizeof(unsigned) * (size_t)((B + 31) / 32));
   w.keys = take(sizeof(unsigned long long) * (size_t)N * B);
-  if (pruned) w.cand_n = take(sizeof(int32_t) * (size_t)N * B);
   w.zero_end = off;
   w.z = take(sizeof(float) * (size_t)N * w.Vhp * w.ldb);
   if (pruned) {
     w.zmax = take(sizeof(float) * (size_t)N * B * (w.Vhp / 128));
-    w.cand = take(pruned_list_bytes(B, N));
+    w.cand = take(plan_pruned_lists(B, N, k).total);
   }
   if (dtype == DSPARK_F32) {          // the CUDA-core chain keeps one corrected row per block
     w.zc = take(sizeof(float) * (size_t)B * w.ldz);
@@ -185,9 +184,17 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
     p.cnorm = (const float*)(pr + pl.cnorm);
     p.cnmax = (const float*)(pr + pl.cnmax);
     p.w1max = (const unsigned*)(pr + pl.w1max);
-    p.cand_n = (int32_t*)(ws + wl.cand_n);
-    p.cand_v = (int32_t*)(ws + wl.cand);
-    p.cand_z = (float*)(ws + wl.cand + pruned_list_bytes(cfg->B, N) / 2);   // after cand_v
+    const PrunedLists ll = plan_pruned_lists(cfg->B, N, cfg->top_k);
+    char* lists = ws + wl.cand;
+    p.cand_v = (int32_t*)(lists + ll.cand_v);
+    p.cand_z = (float*)(lists + ll.cand_z);
+    p.cand_n = (int32_t*)(lists + ll.cand_n);
+    p.prev_v = (int32_t*)(lists + ll.prev_v);
+    p.prev_n = (int32_t*)(lists + ll.prev_n);
+    p.amax = (int32_t*)(lists + ll.amax);
+    p.tk_id = (int32_t*)(lists + ll.tk_id);
+    p.tk_val = (float*)(lists + ll.tk_val);
+    p.z_octet = true;           // the candidate scans read one block's rows of z
   }
 
   cudaError_t e;
@@ -198,7 +205,8 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   e = cudaMemsetAsync(ws + wl.ctrl, 0, wl.zero_end - wl.ctrl, p.stream);
   if (e != cudaSuccess) return cuda_fail(e, "control reset");
   if ((e = mark(DSPARK_STAGE_CONF)) != cudaSuccess) return cuda_fail(e, "event record");
-  if ((e = launch_conf(p)) != cudaSuccess) return cuda_fail(e, "confidence kernel");
+  // the pruned chain evaluates the confidence head and truncation in its own kernels
+  if (!pruned && (e = launch_conf(p)) != cudaSuccess) return cuda_fail(e, "confidence kernel");
   if ((e = mark(DSPARK_STAGE_LOGITS)) != cudaSuccess) return cuda_fail(e, "event record");
   e = p.dtype == DSPARK_BF16 ? launch_base_logits_tc(p) : launch_base_logits_simt(p);
   if (e != cudaSuccess) return cuda_fail(e, "base logits");
@@ -236,7 +244,7 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK || !out) return -1;
   if (cfg->dtype == DSPARK_F32) return 1 + 1 + 2 * N;   // confidence, GEMM, 2 per slot
-  if (use_pruned(cfg, head) && !out->logits) return 4;  // confidence, GEMM, candidates, chain
+  if (use_pruned(cfg, head) && !out->logits) return 3;  // GEMM, tables, walk
   const bool topk = out->topk_ids || out->topk_vals;
   return 1 /* confidence */ + 1 /* GEMM */ + (cfg->B + 31) / 32 /* chain, 32 blocks each */ +
          (topk ? 1 : 0);

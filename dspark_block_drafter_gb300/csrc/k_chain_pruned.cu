@@ -9,13 +9,17 @@
 //   * theta = the k-th largest lb[T] is therefore <= the k-th largest z';
 //   * a row can reach the top k only if ub[v] = z[v] + Umax cn[v] >= theta, and a tile
 //     only if zmax[T] + Umax cmax[T] >= theta.
-// None of this depends on the previous token, so the candidate rows of every (slot,
-// block) are found by one fully parallel kernel; the sequential chain then evaluates z'
-// exactly (fp32) for the candidates only (their markov_w2 rows prefetched one slot
-// ahead) and selects the argmax (the next previous token) and the top-k.  The bounds
-// carry a small margin for fp32 rounding, so the selection equals that of evaluating
-// every row.  A (slot, block) with more candidates than the list holds is evaluated
-// over every row instead, so the pruning only changes the cost, never the result.
+// None of this depends on the previous token.  So one fully parallel kernel, one CTA per
+// (slot i, block b), finds the candidate rows C(i) of the slot (theta of rank k) and the
+// rows A(i - 1) that can be the previous slot's argmax (theta of rank 1); the previous
+// token of slot i is the head row chosen in slot i - 1, which lies in A(i - 1) (slot 0:
+// the anchor).  It then evaluates z' exactly (fp32) for every pair of a possible previous
+// row and a candidate: a small table.  The sequential walk over the slots, one CTA per
+// block, is left with table lookups and a warp-wide argmax per slot; top-k follows for
+// all slots in parallel.  The bounds carry a margin for fp32 rounding, so every
+// selection equals that of evaluating every row.  Where a list or a table would not fit
+// (loose bounds), the walk evaluates that slot on the fly, over every row if need be, so
+// the pruning only changes the cost, never the result.
 //
 // One-time preparation (dspark_prepare_head) stores markov_w2 transposed ([V_head][r],
 // a row's Markov weights contiguous), the column norms cn, their per-tile maxima and
@@ -32,13 +36,12 @@ namespace dspark {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 256;
-constexpr int kCap = 512;                    // candidate list entries per (slot, block)
-constexpr int kRowsMax = 64;                 // candidates whose rows are staged per slot
-constexpr size_t kRowsBytes = 128 * 1024;     // shared memory for both staging buffers
-constexpr int kCandThreads = 512;            // threads of the candidate pass
-constexpr int kCandWarps = kCandThreads / 32;
+constexpr int kThreads = 256;                // threads of both kernels
 constexpr int kWarps = kThreads / 32;
+constexpr int kCap = 512;                    // candidate list entries per (slot, block)
+constexpr int kCapA = 16;                    // possible previous rows tabulated per slot
+constexpr int kTabC = 128;                   // candidates tabulated per slot
+constexpr int kRowsChunk = 16;               // markov_w2 rows staged at a time
 constexpr int kMaxKeep = 33;                 // survivors of a reduction: top_k <= 32, + argmax
 // candidate buffer entries: one round of appends (kWarps tiles of kTile rows) on top of
 // the survivors of a reduction
@@ -150,37 +153,6 @@ __device__ void block_pick(const Cand* buf, int n, bool by_z, bool first, float 
   warp_best(bv, bi);
   out_v = bv;
   out_id = bi;
-}
-
-// Block-wide k-th best of vals[0..n) (ids = indices) under the candidate order;
-// -inf when n < k.
-__device__ float block_kth(const float* vals, int n, int k, float* s_v, int* s_i) {
-  const int w = threadIdx.x / 32, l = threadIdx.x % 32;
-  float pv = 0.f, res = -INFINITY;
-  int pid = 0;
-  for (int q = 0; q < k; ++q) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    for (int t = threadIdx.x; t < n; t += kThreads)
-      if ((q == 0 || better(pv, pid, vals[t], t)) && better(vals[t], t, bv, bi)) {
-        bv = vals[t];
-        bi = t;
-      }
-    warp_best(bv, bi);
-    __syncthreads();
-    if (l == 0) {
-      s_v[w] = bv;
-      s_i[w] = bi;
-    }
-    __syncthreads();
-    bv = l < kWarps ? s_v[l] : -INFINITY;
-    bi = l < kWarps ? s_i[l] : 0x7FFFFFFF;
-    warp_best(bv, bi);
-    pv = bv;
-    pid = bi;
-    res = bv;
-  }
-  return n < k ? -INFINITY : res;
 }
 
 // Warp-wide best (value, id) among vals/ids[0..n) strictly after (pv, pid) (all when
@@ -318,144 +290,351 @@ __device__ void reduce_buffer(Cand* buf, int* s_n, int kk, bool by_z, const floa
 }
 
 
-// ------------------------------------------------------------------ candidates
-struct CandArgs {
-  const float* z;          // [N][Vhp][ldb]
-  const float* zmax;       // [N][B][T]
+
+// ------------------------------------------------------------------ tables
+struct TableArgs {
+  const float* z;            // octet layout (z_octet_index)
+  const float* zmax;         // [N][B][T]
   size_t Vhp, ldb;
-  const float* cnorm;      // [Vhp]
-  const float* cnmax;      // [T]
-  const unsigned* w1max;   // Umax as float bits
-  int32_t* cand_v;         // [N][B][kCap]
-  float* cand_z;           // [N][B][kCap]
-  int32_t* cand_n;         // [N][B] (zeroed; may exceed kCap: the list overflowed)
-  int B, N, Vh, T, kk, zrank;
+  const float* cnorm;        // [Vhp]
+  const float* cnmax;        // [T]
+  const unsigned* w1max;     // Umax as float bits
+  const __nv_bfloat16* w1;   // [V][r]
+  const __nv_bfloat16* w2t;  // [Vhp][r]
+  const int32_t* anchors;
+  const int32_t* d2t;
+  const __nv_bfloat16* hidden;   // [B][L_in][H], read for the confidence head
+  const __nv_bfloat16* w_conf;   // [H] or NULL
+  float b_conf;
+  float* conf;               // [B][N]
+  int32_t* cand_v;           // [N][B][kCap]
+  float* cand_z;             // [N][B][kCap]
+  int32_t* cand_n;           // [N][B] (above kCap: the list overflowed)
+  int32_t* prev_v;           // [N][B][kCapA]
+  int32_t* prev_n;           // [N][B] (above kCapA: too many to tabulate)
+  int32_t* amax;             // [N][B][kCapA]: head row of the argmax given each prev row
+  int32_t* tk_id;            // [N][B][kCapA][k]: top-k tokens given each prev row
+  float* tk_val;             // [N][B][kCapA][k]
+  uint32_t* err;
+  int B, N, V, Vh, T, r, k, kk, zrank, want_topk, L_in, ifp, H;
 };
 
-// One CTA per (slot, block): thresholds, candidate tiles, candidate rows.
-__global__ void __launch_bounds__(kCandThreads)
-pruned_candidates(const CandArgs a) {
-  extern __shared__ float smem[];
-  float* s_lb = smem;                                   // [T]
-  int* s_tiles = (int*)(s_lb + ((a.T + 3) & ~3));       // [T]
-  __shared__ float s_sc_v[kCandWarps * 32];
-  __shared__ int s_sc_i[kCandWarps * 32];
-  __shared__ float s_theta;
-  __shared__ int s_ntiles;
-  const int b = blockIdx.x, i = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const float* zm = a.zmax + ((size_t)i * a.B + b) * a.T;
-  const float umax = __uint_as_float(*a.w1max) * (1.f + kRelMargin);
-  for (int t = tid; t < a.T; t += kCandThreads)
-    s_lb[t] = zm[t] - umax * a.cnmax[t] * (1.f + kRelMargin) - kAbsMargin;
-  if (tid == 0) s_ntiles = 0;
-  __syncthreads();
-  const float theta_x =
-      block_kth_fast(s_lb, a.T, a.zrank ? 1 : a.kk, s_sc_v, s_sc_i, &s_theta);
-  float theta_z = INFINITY;
-  if (a.zrank) {
-    for (int t = tid; t < a.T; t += kCandThreads) s_lb[t] = zm[t];
-    __syncthreads();
-    theta_z = block_kth_fast(s_lb, a.T, a.kk, s_sc_v, s_sc_i, &s_theta) - kAbsMargin;
-  }
-  for (int t = tid; t < a.T; t += kCandThreads) {
-    const bool cx = zm[t] + umax * a.cnmax[t] * (1.f + kRelMargin) + kAbsMargin >= theta_x;
-    if (cx || zm[t] >= theta_z) s_tiles[atomicAdd(&s_ntiles, 1)] = t;
-  }
-  __syncthreads();
-  const int nt = s_ntiles;
-  const float* z_i = a.z + (size_t)i * a.Vhp * a.ldb + b;
-  int32_t* cv = a.cand_v + ((size_t)i * a.B + b) * kCap;
-  float* cz = a.cand_z + ((size_t)i * a.B + b) * kCap;
-  int32_t* cn = a.cand_n + (size_t)i * a.B + b;
-  for (int j = warp; j < nt; j += kCandWarps) {
-    const int t = s_tiles[j];
+// Rows of the listed tiles whose upper bound reaches theta_x or whose base logit reaches
+// theta_z, appended in any order to s_v (and s_z): at most cap are kept, *s_cnt counts
+// them all.  One warp per tile, four rows a lane; each warp loads two tiles before it
+// looks at them.  zrow(v) = z + z_octet_index(slot, v, block).
+__device__ void scan_rows(const float* z, size_t i, size_t b, size_t Vhp, size_t ldb,
+                          const int* s_tiles, int ntiles, const float* cnorm, float umax,
+                          float theta_x, float theta_z, int Vh, int32_t* s_v, float* s_z,
+                          int cap, int* s_cnt) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int j0 = warp; j0 < ntiles; j0 += 2 * kWarps) {
+    float4 z4[2], c4[2];
+    int v0[2];
 #pragma unroll
-    for (int q = 0; q < kTile / 32; ++q) {
-      const int v = t * kTile + q * 32 + lane;
-      bool take = false;
-      float zv = -INFINITY;
-      if (v < a.Vh) {
-        zv = z_i[(size_t)v * a.ldb];
-        const float ub = zv + umax * a.cnorm[v] * (1.f + kRelMargin) + kAbsMargin;
-        take = ub >= theta_x || zv >= theta_z;
+    for (int h = 0; h < 2; ++h) {
+      const int j = j0 + h * kWarps;
+      v0[h] = j < ntiles ? s_tiles[j] * kTile + lane * 4 : -1;
+      if (v0[h] >= 0) {
+        z4[h] = *reinterpret_cast<const float4*>(z + z_octet_index(i, v0[h], b, Vhp, ldb));
+        c4[h] = *reinterpret_cast<const float4*>(cnorm + v0[h]);
       }
-      const unsigned m = __ballot_sync(0xFFFFFFFFu, take);
-      int base = 0;
-      if (lane == 0 && m) base = atomicAdd(cn, __popc(m));
-      base = __shfl_sync(0xFFFFFFFFu, base, 0);
-      if (take) {
-        const int slot = base + __popc(m & ((1u << lane) - 1));
-        if (slot < kCap) {
-          cv[slot] = v;
-          cz[slot] = zv;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (j0 + h * kWarps >= ntiles) break;         // warp-uniform
+      const float zq[4] = {z4[h].x, z4[h].y, z4[h].z, z4[h].w};
+      const float cq[4] = {c4[h].x, c4[h].y, c4[h].z, c4[h].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int v = v0[h] + q;
+        const bool take =
+            v < Vh && (zq[q] + umax * cq[q] * (1.f + kRelMargin) + kAbsMargin >= theta_x ||
+                       zq[q] >= theta_z);
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, take);
+        if (m == 0) continue;
+        int base = 0;
+        if (lane == 0) base = atomicAdd(s_cnt, __popc(m));
+        base = __shfl_sync(0xFFFFFFFFu, base, 0);
+        if (take) {
+          const int slot = base + __popc(m & ((1u << lane) - 1));
+          if (slot < cap) {
+            s_v[slot] = v;
+            if (s_z) s_z[slot] = zq[q];
+          }
         }
       }
     }
   }
 }
 
-// ------------------------------------------------------------------ the chain
-struct PrunedArgs {
-  const float* z;            // [N][Vhp][ldb] (only read on list overflow)
+// One CTA per (block, slot i): candidate rows C(i) (bound of rank kk), the rows A(i - 1)
+// that can be the argmax of slot i - 1 (bound of rank 1; slot 0: the anchor), z' exactly
+// for every pair in A(i - 1) x C(i), and from it, for each possible previous row, the
+// argmax and the top-k of slot i.  Also the slot's confidence.
+__global__ void __launch_bounds__(kThreads)
+pruned_table(const TableArgs a) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  const int T4 = (a.T + 3) & ~3;
+  float* s_lb = (float*)dsm;                                   // [T4] lower bounds, slot i
+  float* s_ub = s_lb + T4;                                     // [T4] upper bounds, slot i
+  float* s_up = s_ub + T4;                                     // [T4] upper bounds, slot i-1
+  int* s_tc = (int*)(s_up + T4);                               // [T4] tiles of C(i)
+  int* s_ta = s_tc + T4;                                       // [T4] tiles of A(i-1)
+  int32_t* s_cv = (int32_t*)(s_ta + T4);                       // [kCap]
+  float* s_cz = (float*)(s_cv + kCap);                         // [kCap]
+  float* s_x = s_cz + kCap;                                    // [kCapA][kTabC]
+  __nv_bfloat16* s_w1 = (__nv_bfloat16*)(s_x + kCapA * kTabC); // [kCapA][r]
+  __nv_bfloat16* s_w2 = s_w1 + (size_t)kCapA * a.r;            // [kRowsChunk][r]
+  __shared__ float s_sc_v[kWarps * 32];
+  __shared__ int s_sc_i[kWarps * 32];
+  __shared__ float s_theta, s_red[kWarps];
+  __shared__ int s_ntc, s_nta, s_nc, s_na;
+  __shared__ int32_t s_av[kCapA];
+  const int b = blockIdx.x, i = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const float umax = __uint_as_float(*a.w1max) * (1.f + kRelMargin);
+  const float* zm = a.zmax + ((size_t)i * a.B + b) * a.T;
+  const float* zp = i > 0 ? a.zmax + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
+
+  if (tid == 0) {
+    s_ntc = 0;
+    s_nta = 0;
+    s_nc = 0;
+    s_na = 0;
+  }
+  // ---- bounds of slot i and slot i - 1 (all warps but the last), confidence (the last)
+  float mp = -INFINITY;                              // running max of slot i-1's lower bounds
+  if (warp < kWarps - 1) {
+    for (int t = tid; t < a.T; t += kThreads - 32) {
+      const float d = umax * a.cnmax[t] * (1.f + kRelMargin) + kAbsMargin;
+      const float z0 = zm[t];
+      s_lb[t] = z0 - d;
+      s_ub[t] = z0 + d;
+      if (zp) {
+        const float z1 = zp[t];
+        s_up[t] = z1 + d;
+        mp = fmaxf(mp, z1 - d);
+      }
+    }
+  } else if (a.w_conf) {
+    // sigmoid(h . w_conf + b_conf) (llama.cpp commit 6fed9f6, "spec: add confidence-based
+    // draft pruning for DSpark")
+    const __nv_bfloat16* h = a.hidden + ((size_t)b * a.L_in + a.ifp + i) * a.H;
+    float acc = 0.f;
+    int c0 = 0;
+    if ((a.H % 8) == 0 && ((uintptr_t)h % 16) == 0 && ((uintptr_t)a.w_conf % 16) == 0) {
+      const uint4* h4 = reinterpret_cast<const uint4*>(h);
+      const uint4* w4 = reinterpret_cast<const uint4*>(a.w_conf);
+      const int n4 = a.H / 8;
+#pragma unroll 4
+      for (int q = lane; q < n4; q += 32) {
+        const uint4 hv = h4[q], wv = w4[q];
+        const __nv_bfloat16* he = reinterpret_cast<const __nv_bfloat16*>(&hv);
+        const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&wv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(to_f32(he[e]), to_f32(we[e]), acc);
+      }
+      c0 = a.H;
+    }
+    for (int c = c0 + lane; c < a.H; c += 32) acc = fmaf(to_f32(h[c]), to_f32(a.w_conf[c]), acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (lane == 0) a.conf[(size_t)b * a.N + i] = 1.f / (1.f + expf(-(acc + a.b_conf)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xFFFFFFFFu, mp, o));
+  if (lane == 0) s_red[warp] = mp;
+  __syncthreads();
+  // ---- thresholds: rank kk of slot i's lower bounds (rank 1 when the top-k ranks base
+  //      logits, which then take rank kk of the tile maxima); rank 1 of slot i-1's
+  const float theta_x =
+      block_kth_fast(s_lb, a.T, a.zrank ? 1 : a.kk, s_sc_v, s_sc_i, &s_theta);
+  float theta_z = INFINITY;
+  if (a.zrank) {
+    for (int t = tid; t < a.T; t += kThreads) s_lb[t] = zm[t];
+    __syncthreads();
+    theta_z = block_kth_fast(s_lb, a.T, a.kk, s_sc_v, s_sc_i, &s_theta) - kAbsMargin;
+  }
+  float theta1 = s_red[0];
+  for (int w = 1; w < kWarps; ++w) theta1 = fmaxf(theta1, s_red[w]);
+  // ---- candidate tiles of both lists
+  for (int t = tid; t < a.T; t += kThreads) {
+    if (s_ub[t] >= theta_x || zm[t] >= theta_z) s_tc[atomicAdd(&s_ntc, 1)] = t;
+    if (zp && s_up[t] >= theta1) s_ta[atomicAdd(&s_nta, 1)] = t;
+  }
+  __syncthreads();
+  // ---- their rows
+  scan_rows(a.z, i, b, a.Vhp, a.ldb, s_tc, s_ntc, a.cnorm, umax, theta_x, theta_z, a.Vh, s_cv,
+            s_cz, kCap, &s_nc);
+  if (zp) {
+    scan_rows(a.z, i - 1, b, a.Vhp, a.ldb, s_ta, s_nta, a.cnorm, umax, theta1, INFINITY, a.Vh,
+              s_av, nullptr, kCapA, &s_na);
+  } else if (tid == 0) {
+    int p = a.anchors[b];
+    if (p < 0 || p >= a.V) {
+      flag_error(a.err, kErrBadToken);
+      p = 0;
+    }
+    s_av[0] = p;                                     // slot 0: the anchor (a token)
+    s_na = 1;
+  }
+  __syncthreads();
+  // ---- the lists
+  const int nc = s_nc, na = s_na;
+  const size_t ib = (size_t)i * a.B + b;
+  for (int j = tid; j < min(nc, kCap); j += kThreads) {
+    a.cand_v[ib * kCap + j] = s_cv[j];
+    a.cand_z[ib * kCap + j] = s_cz[j];
+  }
+  for (int j = tid; j < min(na, kCapA); j += kThreads) a.prev_v[ib * kCapA + j] = s_av[j];
+  if (tid == 0) {
+    a.cand_n[ib] = nc;
+    a.prev_n[ib] = na;
+  }
+  if (nc < 1 || nc > kTabC || na < 1 || na > kCapA) return;   // evaluated on the fly later
+  // ---- z' = z + markov_w1[p] . w2[:, v] for every p in A(i - 1), v in C(i): eight lanes
+  //      per pair, the same summation order as the on-the-fly evaluation
+  const int chunks = a.r / 8;                        // r % 8 == 0 on this path
+  for (int c = tid; c < na * chunks; c += kThreads) {
+    const int p = c / chunks, q = c % chunks;
+    int tok = (i == 0 || !a.d2t) ? s_av[p] : a.d2t[s_av[p]];
+    if (tok < 0 || tok >= a.V) {
+      flag_error(a.err, kErrBadToken);
+      tok = 0;
+    }
+    *reinterpret_cast<uint4*>(s_w1 + (size_t)p * a.r + q * 8) =
+        *reinterpret_cast<const uint4*>(a.w1 + (size_t)tok * a.r + q * 8);
+  }
+  for (int c0 = 0; c0 < nc; c0 += kRowsChunk) {
+    const int cnt = min(kRowsChunk, nc - c0);
+    for (int c = tid; c < cnt * chunks; c += kThreads) {
+      const int e = c / chunks, q = c % chunks;
+      *reinterpret_cast<uint4*>(s_w2 + (size_t)e * a.r + q * 8) =
+          *reinterpret_cast<const uint4*>(a.w2t + (size_t)s_cv[c0 + e] * a.r + q * 8);
+    }
+    __syncthreads();
+    const int pairs = na * cnt, sub = tid % 8;
+    for (int q0 = 0; q0 < pairs; q0 += kThreads / 8) {
+      const int pr = q0 + tid / 8;
+      float s0 = 0.f, s1 = 0.f;
+      if (pr < pairs) {
+        const __nv_bfloat16* u = s_w1 + (size_t)(pr / cnt) * a.r;
+        const __nv_bfloat16* w = s_w2 + (size_t)(pr % cnt) * a.r;
+        for (int ch = sub; ch < chunks; ch += 8) {
+          const uint4 ru = *reinterpret_cast<const uint4*>(u + ch * 8);
+          const uint4 rw = *reinterpret_cast<const uint4*>(w + ch * 8);
+          const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&ru);
+          const __nv_bfloat162* pw = reinterpret_cast<const __nv_bfloat162*>(&rw);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float2 fu = __bfloat1622float2(pu[h]), fw = __bfloat1622float2(pw[h]);
+            s0 = fmaf(fu.x, fw.x, s0);
+            s1 = fmaf(fu.y, fw.y, s1);
+          }
+        }
+      }
+      float s = s0 + s1;
+      s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
+      s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+      s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+      if (pr < pairs && sub == 0) {
+        const int e = pr % cnt;
+        s_x[(pr / cnt) * kTabC + c0 + e] = s_cz[c0 + e] + s;
+      }
+    }
+    __syncthreads();
+  }
+  // ---- for each possible previous row: the argmax (the next previous row) and the top-k
+  for (int p = warp; p < na; p += kWarps) {
+    const float* x = s_x + p * kTabC;
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int c = lane; c < nc; c += 32)
+      if (better(x[c], s_cv[c], bv, bi)) {
+        bv = x[c];
+        bi = s_cv[c];
+      }
+    warp_best(bv, bi);
+    if (lane == 0) a.amax[ib * kCapA + p] = (bi >= 0 && bi < a.Vh) ? bi : -1;
+    if (!a.want_topk) continue;
+    const float* rk = a.zrank ? s_cz : x;
+    float pv = 0.f;
+    int pid = 0;
+    for (int q = 0; q < a.k; ++q) {
+      bv = -INFINITY;
+      bi = 0x7FFFFFFF;
+      for (int c = lane; c < nc; c += 32) {
+        const float val = rk[c];
+        const int id = s_cv[c];
+        if (q > 0 && !better(pv, pid, val, id)) continue;
+        if (better(val, id, bv, bi)) {
+          bv = val;
+          bi = id;
+        }
+      }
+      warp_best(bv, bi);
+      if (lane == 0) {
+        const size_t o = (ib * kCapA + p) * a.k + q;
+        const int row = (bi >= 0 && bi < a.Vh) ? bi : 0;
+        a.tk_id[o] = a.d2t ? a.d2t[row] : row;
+        a.tk_val[o] = bv;
+      }
+      pv = bv;
+      pid = bi;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the walk
+struct SelectArgs {
+  const float* z;            // octet layout (read only to evaluate every row)
   size_t Vhp, ldb;
   const __nv_bfloat16* w1;   // [V][r]
   const __nv_bfloat16* w2t;  // [Vhp][r]
   const int32_t* cand_v;
   const float* cand_z;
   const int32_t* cand_n;
+  const int32_t* prev_v;
+  const int32_t* prev_n;
+  const int32_t* amax;
+  const int32_t* tk_id;
+  const float* tk_val;
   const int32_t* anchors;
   const int32_t* d2t;
+  const float* conf;         // [B][N], or NULL without a confidence head
+  float conf_min;
+  int32_t* n_draft;          // [B]
   int32_t* draft;            // [B][N]
   int32_t* topk_ids;         // [B][N][k] or NULL
   float* topk_vals;
   uint32_t* err;
   int B, N, V, Vh, r, k, kk, zrank, want_topk;
-  int rows_cap;              // candidates whose rows are staged per slot
 };
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+constexpr int kMaxSlots = 256;               // prediction slots of the bf16 path
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
                    (uint32_t)__cvta_generic_to_shared(dst)),
                "l"(src)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_prev() {    // all but the latest group
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// Stage the markov_w2 rows and the markov_w1 rows (the candidate as a previous token)
-// of the first `cap` candidates of a list into shared memory.
-__device__ void stage_rows(const int32_t* s_v, int n, int cap, const __nv_bfloat16* w2t,
-                           const __nv_bfloat16* w1, const int32_t* d2t, int r,
-                           __nv_bfloat16* rows2, __nv_bfloat16* rows1) {
-  const int chunks_per_row = r / 8;                      // r % 8 == 0 on this path
-  const int total = min(n, cap) * chunks_per_row;
-  for (int c = threadIdx.x; c < total; c += kThreads) {
-    const int j = c / chunks_per_row, q = c % chunks_per_row;
-    const int v = s_v[j];
-    const int tok = d2t ? d2t[v] : v;
-    cp_async16(rows2 + (size_t)j * r + q * 8, w2t + (size_t)v * r + q * 8);
-    cp_async16(rows1 + (size_t)j * r + q * 8, w1 + (size_t)tok * r + q * 8);
-  }
-}
-
-// z' = z + u . w2[:, v] for list entries [0, n): eight lanes per entry.  Lane `sub`
-// takes the 8-element chunks sub, sub + 8, ... of the row, so that the eight lanes of an
-// entry read consecutive 16-byte chunks of the row and of u (no bank conflicts); rows
-// [0, cap) come from shared memory, later ones from global memory.
-__device__ void evaluate_list(Cand* buf, int n, int cap, const float* s_u,
-                              const __nv_bfloat16* rows, const __nv_bfloat16* w2t, int r) {
+// z' = z + u . w2[:, v] for buffer entries [0, n), rows read from global memory: eight
+// lanes per entry, lane `sub` taking the 8-element chunks sub, sub + 8, ... of the row.
+__device__ void evaluate_list(Cand* buf, int n, const float* s_u, const __nv_bfloat16* w2t,
+                              int r) {
   const int sub = threadIdx.x % 8;
   const int chunks = r / 8;                              // r % 8 == 0 on this path
   for (int e0 = 0; e0 < n; e0 += kThreads / 8) {
     const int e = e0 + threadIdx.x / 8;
     float s0 = 0.f, s1 = 0.f;
     if (e < n) {
-      const __nv_bfloat16* w = e < cap ? rows + (size_t)e * r : w2t + (size_t)buf[e].v * r;
+      const __nv_bfloat16* w = w2t + (size_t)buf[e].v * r;
       for (int c = sub; c < chunks; c += 8) {
         const uint4 raw = *reinterpret_cast<const uint4*>(w + c * 8);
         const float4 u0 = *reinterpret_cast<const float4*>(s_u + c * 8);
@@ -481,101 +660,143 @@ __device__ void evaluate_list(Cand* buf, int n, int cap, const float* s_u,
   }
 }
 
-// One CTA per block walks its N slots.  The candidate lists, the markov_w2 rows and the
-// markov_w1 rows of slot i + 1 are staged while slot i is evaluated, so that a slot's
-// critical path touches shared memory only.
+// One CTA per block walks its N slots.  A tabulated slot is a lookup: the previous row's
+// index in A(i - 1), then the argmax stored for it; warp 0 walks those alone.  A slot
+// without a table (a list that overflowed, too many previous rows, a previous row not
+// found) is evaluated on the fly by the whole CTA, over every row if need be.
 __global__ void __launch_bounds__(kThreads)
-chain_pruned(const PrunedArgs a) {
+pruned_select(const SelectArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
-  const size_t rows_elems = (size_t)a.rows_cap * a.r;
-  __nv_bfloat16* s_rows2 = (__nv_bfloat16*)dsm;                  // [2][rows_cap][r]
-  __nv_bfloat16* s_rows1 = s_rows2 + 2 * rows_elems;              // [2][rows_cap][r]
-  float* s_u = (float*)(s_rows1 + 2 * rows_elems);                // [r]
-  int32_t* s_lv = (int32_t*)(s_u + ((a.r + 3) & ~3));             // [2][kCap]
-  float* s_lz = (float*)(s_lv + 2 * kCap);                        // [2][kCap]
-  Cand* buf = (Cand*)(s_lz + 2 * kCap);                           // [kCand]
+  float* s_u = (float*)dsm;                                    // [r]
+  Cand* buf = (Cand*)(s_u + ((a.r + 3) & ~3));                 // [kCand]
+  __shared__ int s_nc[kMaxSlots], s_na[kMaxSlots], s_pi[kMaxSlots];
+  __shared__ int32_t s_av[kMaxSlots][kCapA], s_am[kMaxSlots][kCapA];
+  __shared__ float s_conf[kMaxSlots];
   __shared__ float s_red_v[kWarps];
   __shared__ int s_red_i[kWarps];
-  __shared__ int s_n[2], s_nfull, s_prev, s_sel;
+  __shared__ int s_nfull, s_prev, s_stop;
   __shared__ int s_keep[kMaxKeep];
   __shared__ Cand s_stage[kMaxKeep];
-
   const int b = blockIdx.x;
-  const int tid = threadIdx.x;
-  auto list_base = [&](int i) { return ((size_t)i * a.B + b) * kCap; };
-  auto load_list = [&](int i, int slot) {
-    const int n = a.cand_n[(size_t)i * a.B + b];
-    const int m = min(n, kCap);
-    for (int j = tid; j < m; j += kThreads) {
-      s_lv[slot * kCap + j] = a.cand_v[list_base(i) + j];
-      s_lz[slot * kCap + j] = a.cand_z[list_base(i) + j];
-    }
-    if (tid == 0) s_n[slot] = n;
-  };
-  // slot 0: u from the anchor, list and rows of slot 0, list of slot 1
-  {
-    int p = a.anchors[b];
-    if (p < 0 || p >= a.V) {
-      if (tid == 0) flag_error(a.err, kErrBadToken);
-      p = 0;
-    }
-    for (int q = tid; q < a.r; q += kThreads) s_u[q] = __bfloat162float(a.w1[(size_t)p * a.r + q]);
-    load_list(0, 0);
-    if (a.N > 1) load_list(1, 1);
-    __syncthreads();
-    if (s_n[0] <= kCap)
-      stage_rows(s_lv, s_n[0], a.rows_cap, a.w2t, a.w1, a.d2t, a.r, s_rows2, s_rows1);
-    cp_async_commit();
-  }
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
 
-  for (int step = 0; step < a.N; ++step) {
-    const int cur = step & 1, nxt = cur ^ 1;
-    // -------- stage the next slot's rows (its list is in), fetch the list after it
-    if (step + 1 < a.N && s_n[nxt] <= kCap)
-      stage_rows(s_lv + nxt * kCap, s_n[nxt], a.rows_cap, a.w2t, a.w1, a.d2t, a.r,
-                 s_rows2 + nxt * rows_elems, s_rows1 + nxt * rows_elems);
-    cp_async_commit();
-    // the list two slots ahead: plain loads issued now (the whole kCap slots, so that no
-    // instruction waits on the count), stored to shared memory after this slot
-    int nv2 = 0, v2[kCap / kThreads];
-    float z2[kCap / kThreads];
-    if (step + 2 < a.N) {
-      nv2 = a.cand_n[(size_t)(step + 2) * a.B + b];
-#pragma unroll
-      for (int q = 0; q < kCap / kThreads; ++q) {
-        const int j = tid + q * kThreads;
-        v2[q] = a.cand_v[list_base(step + 2) + j];
-        z2[q] = a.cand_z[list_base(step + 2) + j];
-      }
+  // ---- counts, then the previous rows and argmax rows of every tabulated slot
+  for (int i = tid; i < a.N; i += kThreads) {
+    s_nc[i] = a.cand_n[(size_t)i * a.B + b];
+    s_na[i] = a.prev_n[(size_t)i * a.B + b];
+  }
+  if (a.conf)
+    for (int i = tid; i < a.N; i += kThreads) cp_async4(&s_conf[i], a.conf + (size_t)b * a.N + i);
+  __syncthreads();
+  auto tabulated = [&](int i) {
+    return s_nc[i] >= 1 && s_nc[i] <= kTabC && s_na[i] >= 1 && s_na[i] <= kCapA;
+  };
+  for (int e = tid; e < a.N * kCapA; e += kThreads) {
+    const int i = e / kCapA, p = e % kCapA;
+    if (tabulated(i) && p < s_na[i]) {
+      const size_t o = ((size_t)i * a.B + b) * kCapA + p;
+      cp_async4(&s_av[i][p], a.prev_v + o);
+      cp_async4(&s_am[i][p], a.amax + o);
     }
-    cp_async_wait_prev();                      // this slot's rows
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- warp 0 walks the tabulated slots as far as it can
+  if (warp == 0) {
+    int prev = -1, step = 0;
+    for (; step < a.N; ++step) {
+      if (!tabulated(step)) break;
+      int pi = 0;
+      if (step > 0) {
+        const bool hit = lane < s_na[step] && s_av[step][lane] == prev;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, hit);
+        if (m == 0) break;
+        pi = __ffs(m) - 1;
+      }
+      const int row = s_am[step][pi];
+      if (row < 0 || row >= a.Vh) break;
+      if (lane == 0) {
+        s_pi[step] = pi;
+        a.draft[(size_t)b * a.N + step] = a.d2t ? a.d2t[row] : row;
+      }
+      prev = row;
+    }
+    if (lane == 0) {
+      s_stop = step;
+      s_prev = prev;
+    }
+  }
+  __syncthreads();
+  for (int step = s_stop; step < a.N; ++step) {
+    // -------- a tabulated slot whose previous row is listed: a lookup
+    if (tid == 0) {
+      int pi = -1;
+      if (tabulated(step)) {
+        if (step == 0) {
+          pi = 0;
+        } else {
+          for (int p = 0; p < s_na[step]; ++p)
+            if (s_av[step][p] == s_prev) {
+              pi = p;
+              break;
+            }
+        }
+        if (pi >= 0) {
+          const int row = s_am[step][pi];
+          if (row >= 0 && row < a.Vh) {
+            s_prev = row;
+            a.draft[(size_t)b * a.N + step] = a.d2t ? a.d2t[row] : row;
+          } else {
+            pi = -1;
+          }
+        }
+      }
+      s_pi[step] = pi;
+    }
     __syncthreads();
-    const int n = s_n[cur];
-    float av;
-    int ai;
+    if (s_pi[step] >= 0) continue;
+    // -------- on the fly: u of the previous token, z' of the list (or of every row)
+    {
+      int p;
+      if (step == 0) {
+        p = a.anchors[b];
+      } else {
+        const int pv = s_prev;
+        p = (pv >= 0 && pv < a.Vh) ? (a.d2t ? a.d2t[pv] : pv) : -1;
+      }
+      if (p < 0 || p >= a.V) {
+        if (tid == 0) flag_error(a.err, kErrBadToken);
+        p = 0;
+      }
+      for (int q = tid; q < a.r; q += kThreads)
+        s_u[q] = __bfloat162float(a.w1[(size_t)p * a.r + q]);
+    }
+    const int n = s_nc[step];
+    const size_t ib = (size_t)step * a.B + b;
     int nsel;
-    if (n <= kCap) {
-      // -------- exact z' of the candidates
+    __syncthreads();
+    if (n >= 1 && n <= kCap) {
       for (int j = tid; j < n; j += kThreads) {
-        buf[j].v = s_lv[cur * kCap + j];
-        buf[j].z = s_lz[cur * kCap + j];
+        buf[j].v = a.cand_v[ib * kCap + j];
+        buf[j].z = a.cand_z[ib * kCap + j];
+        buf[j].x = NAN;
       }
       __syncthreads();
-      evaluate_list(buf, n, a.rows_cap, s_u, s_rows2 + cur * rows_elems, a.w2t, a.r);
+      evaluate_list(buf, n, s_u, a.w2t, a.r);
       __syncthreads();
       nsel = n;
     } else {
-      // -------- the list overflowed: every row, streamed through the buffer
+      // the list overflowed: every row, streamed through the buffer
       if (tid == 0) s_nfull = 0;
       __syncthreads();
-      const float* z_i = a.z + (size_t)step * a.Vhp * a.ldb + b;
       for (int v0 = 0; v0 < a.Vh; v0 += kCand - kMaxKeep) {
         const int cnt = min(kCand - kMaxKeep, a.Vh - v0);
         const int base = s_nfull;
         __syncthreads();
         for (int j = tid; j < cnt; j += kThreads) {
           buf[base + j].v = v0 + j;
-          buf[base + j].z = z_i[(size_t)(v0 + j) * a.ldb];
+          buf[base + j].z = a.z[z_octet_index(step, v0 + j, b, a.Vhp, a.ldb)];
           buf[base + j].x = NAN;
         }
         __syncthreads();
@@ -586,94 +807,58 @@ chain_pruned(const PrunedArgs a) {
       }
       nsel = s_nfull;
     }
-    // -------- selection: each entry counts the entries that beat it (its rank)
-    if (nsel <= kThreads) {
-      if (tid == 0) s_sel = -1;
-      __syncthreads();
-      if (tid < nsel) {
-        const float x = buf[tid].x, zz = buf[tid].z;
-        const int v = buf[tid].v;
-        const float rk = a.zrank ? zz : x;
-        int rank_x = 0, rank_r = 0;
-        for (int j = 0; j < nsel; ++j) {
-          const float xj = buf[j].x;
-          const float rj = a.zrank ? buf[j].z : xj;
-          const int vj = buf[j].v;
-          rank_x += better(xj, vj, x, v);
-          rank_r += better(rj, vj, rk, v);
-        }
-        if (rank_x == 0) {                     // the argmax: the next previous token
-          const int tok = a.d2t ? a.d2t[v] : v;
-          a.draft[(size_t)b * a.N + step] = tok;
-          s_prev = tok;
-          s_sel = tid;
-        }
-        if (a.want_topk && rank_r < a.k) {
-          const size_t o = ((size_t)b * a.N + step) * a.k + rank_r;
-          if (a.topk_ids) a.topk_ids[o] = a.d2t ? a.d2t[v] : v;
-          if (a.topk_vals) a.topk_vals[o] = rk;
-        }
-      }
-      __syncthreads();
-    } else {
-      block_pick(buf, nsel, false, true, 0.f, 0, av, ai, s_red_v, s_red_i);
-      if (ai < 0 || ai >= a.Vh) ai = 0;      // only if every candidate value was NaN
-      const int tok = a.d2t ? a.d2t[ai] : ai;
-      if (tid == 0) {
-        a.draft[(size_t)b * a.N + step] = tok;
-        s_prev = tok;
-        s_sel = -1;
-      }
-      if (a.want_topk) {
-        float pv = 0.f;
-        int pid = 0;
-        for (int q = 0; q < a.k; ++q) {
-          float bv;
-          int bi;
-          block_pick(buf, nsel, a.zrank != 0, q == 0, pv, pid, bv, bi, s_red_v, s_red_i);
-          if (tid == 0) {
-            const size_t o = ((size_t)b * a.N + step) * a.k + q;
-            const int row = (bi >= 0 && bi < a.Vh) ? bi : 0;   // fewer candidates than k:
-                                                                // impossible, k <= V_head
-            if (a.topk_ids) a.topk_ids[o] = a.d2t ? a.d2t[row] : row;
-            if (a.topk_vals) a.topk_vals[o] = bv;
-          }
-          pv = bv;
-          pid = bi;
-        }
-      }
-      __syncthreads();
+    // -------- selection over the evaluated entries: argmax, then the top-k
+    float av;
+    int ai;
+    block_pick(buf, nsel, false, true, 0.f, 0, av, ai, s_red_v, s_red_i);
+    if (ai < 0 || ai >= a.Vh) ai = 0;                  // only if every value was NaN
+    if (tid == 0) {
+      a.draft[(size_t)b * a.N + step] = a.d2t ? a.d2t[ai] : ai;
+      s_prev = ai;
     }
-    // -------- the next slot's u: staged with this slot's candidates when possible
-    {
-      const int sel = s_sel;
-      int p = s_prev;
-      if (p < 0 || p >= a.V) {
-        if (tid == 0) flag_error(a.err, kErrBadToken);
-        p = 0;
-      }
-      if (sel >= 0 && sel < a.rows_cap && n <= kCap) {
-        const __nv_bfloat16* src = s_rows1 + cur * rows_elems + (size_t)sel * a.r;
-        for (int q = tid; q < a.r; q += kThreads) s_u[q] = __bfloat162float(src[q]);
-      } else {
-        for (int q = tid; q < a.r; q += kThreads)
-          s_u[q] = __bfloat162float(a.w1[(size_t)p * a.r + q]);
-      }
-      // the list two slots ahead lands where this slot's list was
-      if (step + 2 < a.N) {
-        const int m = min(nv2, kCap);
-#pragma unroll
-        for (int q = 0; q < kCap / kThreads; ++q) {
-          const int j = tid + q * kThreads;
-          if (j < m) {
-            s_lv[cur * kCap + j] = v2[q];
-            s_lz[cur * kCap + j] = z2[q];
-          }
+    if (a.want_topk) {
+      float pv = 0.f;
+      int pid = 0;
+      for (int q = 0; q < a.k; ++q) {
+        float bv;
+        int bi;
+        block_pick(buf, nsel, a.zrank != 0, q == 0, pv, pid, bv, bi, s_red_v, s_red_i);
+        if (tid == 0) {
+          const size_t o = ((size_t)b * a.N + step) * a.k + q;
+          const int row = (bi >= 0 && bi < a.Vh) ? bi : 0;
+          if (a.topk_ids) a.topk_ids[o] = a.d2t ? a.d2t[row] : row;
+          if (a.topk_vals) a.topk_vals[o] = bv;
         }
-        if (tid == 0) s_n[cur] = nv2;
+        pv = bv;
+        pid = bi;
       }
-      __syncthreads();
     }
+    __syncthreads();
+  }
+
+  // ---- top-k of the looked-up slots: the entries stored for the chosen previous row
+  if (a.want_topk) {
+    for (int e = tid; e < a.N * a.k; e += kThreads) {
+      const int i = e / a.k, q = e % a.k;
+      const int pi = s_pi[i];
+      if (pi < 0) continue;                          // written by the on-the-fly step
+      const size_t src = (((size_t)i * a.B + b) * kCapA + pi) * a.k + q;
+      const size_t dst = ((size_t)b * a.N + i) * a.k + q;
+      if (a.topk_ids) a.topk_ids[dst] = a.tk_id[src];
+      if (a.topk_vals) a.topk_vals[dst] = a.tk_val[src];
+    }
+  }
+  // ---- truncation at the first slot whose confidence is below conf_min (llama.cpp
+  //      commit 6fed9f6, "spec: add confidence-based draft pruning for DSpark")
+  if (tid == 0) {
+    int nd = a.N;
+    if (a.conf && a.conf_min > 0.f)
+      for (int i = 0; i < a.N; ++i)
+        if (s_conf[i] < a.conf_min) {
+          nd = i;
+          break;
+        }
+    a.n_draft[b] = nd;
   }
 }
 
@@ -696,8 +881,25 @@ PreparedLayout plan_prepared(int Vh, int r) {
   return l;
 }
 
-size_t pruned_list_bytes(int B, int N) {
-  return (size_t)N * B * kCap * (sizeof(int32_t) + sizeof(float));
+PrunedLists plan_pruned_lists(int B, int N, int k) {
+  PrunedLists l{};
+  const size_t nb = (size_t)N * B;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  l.cand_v = take(sizeof(int32_t) * nb * kCap);
+  l.cand_z = take(sizeof(float) * nb * kCap);
+  l.cand_n = take(sizeof(int32_t) * nb);
+  l.prev_v = take(sizeof(int32_t) * nb * kCapA);
+  l.prev_n = take(sizeof(int32_t) * nb);
+  l.amax = take(sizeof(int32_t) * nb * kCapA);
+  l.tk_id = take(sizeof(int32_t) * nb * kCapA * k);
+  l.tk_val = take(sizeof(float) * nb * kCapA * k);
+  l.total = off;
+  return l;
 }
 
 cudaError_t launch_prepare_head(const void* w1, const void* w2, int V, int r, int Vh,
@@ -724,63 +926,92 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   const bool want_topk = p.topk_ids || p.topk_vals;
   const int kk = want_topk ? p.k : 1;
   const int zrank = (want_topk && !p.topk_markov) ? 1 : 0;
+  if (!p.z_octet || p.N > kMaxSlots || p.r % 8 != 0) return cudaErrorInvalidValue;
+  cudaError_t e;
   {
-    CandArgs c{};
-    c.z = p.z;
-    c.zmax = p.zmax;
-    c.Vhp = p.Vhp;
-    c.ldb = p.ldb;
-    c.cnorm = p.cnorm;
-    c.cnmax = p.cnmax;
-    c.w1max = p.w1max;
-    c.cand_v = p.cand_v;
-    c.cand_z = p.cand_z;
-    c.cand_n = p.cand_n;
-    c.B = p.B;
-    c.N = p.N;
-    c.Vh = p.Vh;
-    c.T = T;
-    c.kk = kk;
-    c.zrank = zrank;
-    const size_t smem = sizeof(float) * 2 * ((T + 3) & ~3);
-    cudaError_t e = cudaFuncSetAttribute(pruned_candidates,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    TableArgs t{};
+    t.z = p.z;
+    t.zmax = p.zmax;
+    t.Vhp = p.Vhp;
+    t.ldb = p.ldb;
+    t.cnorm = p.cnorm;
+    t.cnmax = p.cnmax;
+    t.w1max = p.w1max;
+    t.w1 = (const __nv_bfloat16*)p.w1;
+    t.w2t = p.w2t;
+    t.anchors = p.anchors;
+    t.d2t = p.d2t;
+    t.hidden = (const __nv_bfloat16*)p.hidden;
+    t.w_conf = (const __nv_bfloat16*)p.w_conf;
+    t.b_conf = p.b_conf;
+    t.conf = p.conf ? p.conf : p.conf_ws;
+    t.cand_v = p.cand_v;
+    t.cand_z = p.cand_z;
+    t.cand_n = p.cand_n;
+    t.prev_v = p.prev_v;
+    t.prev_n = p.prev_n;
+    t.amax = p.amax;
+    t.tk_id = p.tk_id;
+    t.tk_val = p.tk_val;
+    t.err = p.ctrl;
+    t.B = p.B;
+    t.N = p.N;
+    t.V = p.V;
+    t.Vh = p.Vh;
+    t.T = T;
+    t.r = p.r;
+    t.k = p.k;
+    t.kk = kk;
+    t.zrank = zrank;
+    t.want_topk = want_topk ? 1 : 0;
+    t.L_in = p.L_in;
+    t.ifp = p.ifp;
+    t.H = p.H;
+    const size_t T4 = (size_t)((T + 3) & ~3);
+    const size_t smem = sizeof(float) * 5 * T4 + (sizeof(int32_t) + sizeof(float)) * kCap +
+                        sizeof(float) * kCapA * kTabC +
+                        sizeof(__nv_bfloat16) * (size_t)(kCapA + kRowsChunk) * p.r;
+    e = cudaFuncSetAttribute(pruned_table, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    pruned_candidates<<<dim3(p.B, p.N), kCandThreads, smem, p.stream>>>(c);
+    pruned_table<<<dim3(p.B, p.N), kThreads, smem, p.stream>>>(t);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  PrunedArgs a{};
-  a.z = p.z;
-  a.Vhp = p.Vhp;
-  a.ldb = p.ldb;
-  a.w1 = (const __nv_bfloat16*)p.w1;
-  a.w2t = p.w2t;
-  a.cand_v = p.cand_v;
-  a.cand_z = p.cand_z;
-  a.cand_n = p.cand_n;
-  a.anchors = p.anchors;
-  a.d2t = p.d2t;
-  a.draft = p.draft;
-  a.topk_ids = p.topk_ids;
-  a.topk_vals = p.topk_vals;
-  a.err = p.ctrl;
-  a.B = p.B;
-  a.N = p.N;
-  a.V = p.V;
-  a.Vh = p.Vh;
-  a.r = p.r;
-  a.k = p.k;
-  a.kk = kk;
-  a.zrank = zrank;
-  a.want_topk = want_topk ? 1 : 0;
-  a.rows_cap = (int)std::min<size_t>(kRowsMax, kRowsBytes / (4 * sizeof(__nv_bfloat16) * a.r));
-  const size_t smem = sizeof(__nv_bfloat16) * 4 * (size_t)a.rows_cap * a.r +
-                      sizeof(float) * ((a.r + 3) & ~3) +
-                      (sizeof(int32_t) + sizeof(float)) * 2 * kCap + sizeof(Cand) * kCand;
-  cudaError_t e = cudaFuncSetAttribute(chain_pruned, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  SelectArgs s{};
+  s.z = p.z;
+  s.Vhp = p.Vhp;
+  s.ldb = p.ldb;
+  s.w1 = (const __nv_bfloat16*)p.w1;
+  s.w2t = p.w2t;
+  s.cand_v = p.cand_v;
+  s.cand_z = p.cand_z;
+  s.cand_n = p.cand_n;
+  s.prev_v = p.prev_v;
+  s.prev_n = p.prev_n;
+  s.amax = p.amax;
+  s.tk_id = p.tk_id;
+  s.tk_val = p.tk_val;
+  s.anchors = p.anchors;
+  s.d2t = p.d2t;
+  s.conf = p.w_conf ? (p.conf ? p.conf : p.conf_ws) : nullptr;
+  s.conf_min = p.conf_min;
+  s.n_draft = p.n_draft;
+  s.draft = p.draft;
+  s.topk_ids = p.topk_ids;
+  s.topk_vals = p.topk_vals;
+  s.err = p.ctrl;
+  s.B = p.B;
+  s.N = p.N;
+  s.V = p.V;
+  s.Vh = p.Vh;
+  s.r = p.r;
+  s.k = p.k;
+  s.kk = kk;
+  s.zrank = zrank;
+  s.want_topk = want_topk ? 1 : 0;
+  const size_t smem = sizeof(float) * ((p.r + 3) & ~3) + sizeof(Cand) * kCand;
+  e = cudaFuncSetAttribute(pruned_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  chain_pruned<<<p.B, kThreads, smem, p.stream>>>(a);
+  pruned_select<<<p.B, kThreads, smem, p.stream>>>(s);
   return cudaGetLastError();
 }
 

@@ -9,7 +9,7 @@
 // output keeps the blocks of one (slot, head row) contiguous, so each thread stores
 // runs of 16 bytes and the chain reads them back the same way.
 //
-// One persistent CTA per SM, warp-specialised:
+// Persistent and warp-specialised, one CTA per SM:
 //   warp 4      TMA producer: lm_head tile [128 x 64] and hidden tile [Ni, BB, 64] per
 //               K-block into a ring of shared-memory stages (128-byte swizzle)
 //   warp 5      MMA issuer: 4 x tcgen05.mma (K = 16) per stage into a TMEM accumulator;
@@ -19,6 +19,13 @@
 // Two TMEM accumulators alternate so that the epilogue of one tile overlaps the MMAs of
 // the next.  Tiles are ordered vocabulary-major: CTAs that run side by side share the
 // same lm_head tile through L2, so lm_head streams from HBM once.
+//
+// When a tile's slots split evenly in two, CTAs run in pairs (a cluster of two on one
+// TPC) on 256-row tiles with M = 256 MMAs (cta_group::2): each CTA stages its own 128
+// lm_head rows and half of the hidden rows, so a pair moves two thirds of the bytes
+// through shared memory and L2 that two single CTAs would.  The leader (rank 0) posts
+// the byte count of both halves on its own barrier, both CTAs' copies count against it,
+// the leader issues the MMAs, and the commits arrive in both CTAs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -42,7 +49,8 @@ constexpr long long kWaitBudget = 2000000000ll;       // ~1 s of SM clocks
 struct GemmArgs {
   float* z;
   size_t Vhp, ldb;
-  float* zmax;     // [N][B][v_tiles] per-tile maxima of z, or NULL
+  float* zmax;     // [N][B][zm_tiles] per-tile maxima of z, or NULL
+  int octet;       // z layout: [N][Vhp / 8][ldb][8] (1) or [N][Vhp][ldb] (0)
   const float* bias;
   uint32_t* err;
   int B, N, ifp, Vh;
@@ -51,6 +59,7 @@ struct GemmArgs {
   int bn_mma;      // MMA N (rows of the B operand per stage), multiple of 16
   int acc_stride;  // TMEM columns between the two accumulators (multiple of 32)
   int n_tiles, v_tiles, num_kb, stages;
+  int zm_tiles;    // 128-row tiles of the vocabulary (zmax row length)
   uint32_t tmem_cols;
 };
 
@@ -64,12 +73,18 @@ __device__ __forceinline__ void ntile_extent(const GemmArgs& g, int nt, int& i0,
   nb = min(g.BB, g.B - bb0);
 }
 
+// CG = 1: one CTA per 128-row tile (cta_group::1).  CG = 2: a cluster of two CTAs
+// shares a 256-row tile with M = 256 pair MMAs (cta_group::2): each CTA stages its
+// 128 lm_head rows and half of the prediction rows, the leader (rank 0) issues the MMAs,
+// and each CTA's TMEM receives its own 128 rows of the result.
+template <int CG>
 __global__ void __launch_bounds__(kThreads, 1)
 logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_h, const GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t b_stage = (uint32_t)g.bn_mma * kBlockK * 2;
+  const uint32_t b_rows = (uint32_t)g.bn_mma / CG;            // B rows staged by this CTA
+  const uint32_t b_stage = b_rows * kBlockK * 2;
   uint8_t* sA = smem;
   uint8_t* sB = sA + (size_t)g.stages * kStageA;
   uint64_t* full = (uint64_t*)(sB + (size_t)g.stages * b_stage);
@@ -86,14 +101,18 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
   float* s_cmax = s_panel + 4 * 32 * 33;                 // [2][4][256]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0;
+  const bool leader = rank == 0;
+  const int unit = CG == 2 ? (int)(blockIdx.x / 2) : (int)blockIdx.x;   // cluster or CTA
+  const int units = CG == 2 ? (int)(gridDim.x / 2) : (int)gridDim.x;
   if (threadIdx.x == 0) {
     for (int s = 0; s < g.stages; ++s) {
-      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&full[s], 1);              // the leader's producer (bytes of both)
       ptx::mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
-      ptx::mbar_init(&acc_empty[a], 128);
+      ptx::mbar_init(&acc_empty[a], 4 * CG);    // every epilogue warp of the pair
     }
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(tile_bar, 128);
@@ -105,14 +124,23 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     ptx::tma_prefetch_desc(&tm_h);
   }
   if (warp == 0) {
-    ptx::tmem_alloc(tmem_slot, g.tmem_cols);
-    ptx::tmem_relinquish();
+    if (CG == 2) {
+      ptx::tmem_alloc_pair(tmem_slot, g.tmem_cols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_slot, g.tmem_cols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (CG == 2) ptx::cluster_sync();             // the peer's barriers are initialised
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int num_tiles = g.v_tiles * g.n_tiles;
+  // cluster addresses of the leader's full / acc_empty barriers (unused for CG = 1)
+  const uint32_t full0 = CG == 2 ? ptx::mapa_shared(ptx::smem_u32(full), 0) : 0;
+  const uint32_t acc_empty0 = CG == 2 ? ptx::mapa_shared(ptx::smem_u32(acc_empty), 0) : 0;
 
   auto give_up = [&]() {
     *abort_flag = 1;
@@ -122,42 +150,61 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
   if (warp == 4) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint32_t tx = kStageA + (uint32_t)(g.BB * g.Ni) * kBlockK * 2;
+      const int ni_half = g.Ni / CG;
+      const uint32_t tx = CG * (kStageA + (uint32_t)(g.BB * ni_half) * kBlockK * 2);
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int tile = unit; ok && tile < num_tiles; tile += units) {
         const int vt = tile / g.n_tiles, nt = tile % g.n_tiles;
+        const int row_a = (vt * CG + (int)rank) * kBlockV;
+        const int bcol = (nt % g.n_bt) * g.BB;
+        const int slot = g.ifp + (nt / g.n_bt) * g.Ni + (int)rank * ni_half;
         for (int kb = 0; kb < g.num_kb; ++kb, ++it) {
           const uint32_t s = it % g.stages, ph = (it / g.stages) & 1;
           if (!ptx::mbar_wait(&empty[s], ph ^ 1, kWaitBudget, abort_flag)) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full[s], tx);
-          ptx::tma_load_2d(sA + (size_t)s * kStageA, &tm_w, &full[s], kb * kBlockK,
-                           vt * kBlockV);
-          ptx::tma_load_3d(sB + (size_t)s * b_stage, &tm_h, &full[s], kb * kBlockK,
-                           (nt % g.n_bt) * g.BB, g.ifp + (nt / g.n_bt) * g.Ni);
+          if (CG == 2) {
+            const uint32_t bar = full0 + s * 8;
+            if (leader) ptx::mbar_arrive_expect_tx(&full[s], tx);
+            ptx::tma_load_2d_pair(sA + (size_t)s * kStageA, &tm_w, bar, kb * kBlockK, row_a);
+            ptx::tma_load_3d_pair(sB + (size_t)s * b_stage, &tm_h, bar, kb * kBlockK, bcol,
+                                  slot);
+          } else {
+            ptx::mbar_arrive_expect_tx(&full[s], tx);
+            ptx::tma_load_2d(sA + (size_t)s * kStageA, &tm_w, &full[s], kb * kBlockK, row_a);
+            ptx::tma_load_3d(sB + (size_t)s * b_stage, &tm_h, &full[s], kb * kBlockK, bcol,
+                             slot);
+          }
         }
       }
       if (!ok) {
         give_up();
         // let the copies already issued land before the CTA can exit
-        const uint32_t first = it > (uint32_t)g.stages ? it - g.stages : 0;
-        for (uint32_t j = first; j < it; ++j)
-          ptx::mbar_wait(&full[j % g.stages], (j / g.stages) & 1, kWaitBudget, nullptr);
+        if (CG == 1) {
+          const uint32_t first = it > (uint32_t)g.stages ? it - g.stages : 0;
+          for (uint32_t j = first; j < it; ++j)
+            ptx::mbar_wait(&full[j % g.stages], (j / g.stages) & 1, kWaitBudget, nullptr);
+        } else {
+          // a pair's copies count on the leader's barrier: give them time to land
+          const long long t0 = clock64();
+          while (clock64() - t0 < 1000000) {
+          }
+        }
       }
     }
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t it = 0, local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+      for (int tile = unit; ok && tile < num_tiles; tile += units, ++local) {
         int i0, ni, bb0, nb;
         ntile_extent(g, tile % g.n_tiles, i0, ni, bb0, nb);
-        const int n_mma = (ni * g.BB + 15) / 16 * 16;   // rows up to the last valid slot
-        const uint32_t idesc = ptx::idesc_bf16_f32(kBlockV, n_mma, 0, 0);
+        // rows up to the last valid slot (a pair always covers the full tile)
+        const int n_mma = CG == 2 ? g.bn_mma : (ni * g.BB + 15) / 16 * 16;
+        const uint32_t idesc = ptx::idesc_bf16_f32(kBlockV * CG, n_mma, 0, 0);
         const uint32_t acc = local & 1, aph = (local >> 1) & 1;
         if (!ptx::mbar_wait(&acc_empty[acc], aph ^ 1, kWaitBudget, abort_flag)) {
           ok = false;
@@ -175,24 +222,41 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
           const uint32_t a0 = ptx::smem_u32(sA + (size_t)s * kStageA);
           const uint32_t b0 = ptx::smem_u32(sB + (size_t)s * b_stage);
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k)
-            ptx::mma_f16(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
-                         ptx::desc_kmajor_sw128(b0 + k * 32), idesc, (kb | k) != 0);
-          ptx::mma_commit(&empty[s]);
+          for (int k = 0; k < kBlockK / 16; ++k) {
+            if (CG == 2)
+              ptx::mma_f16_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
+                                ptx::desc_kmajor_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+            else
+              ptx::mma_f16(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
+                           ptx::desc_kmajor_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+          }
+          if (CG == 2)
+            ptx::mma_commit_pair_multicast(&empty[s], 0x3);
+          else
+            ptx::mma_commit(&empty[s]);
         }
-        if (ok) ptx::mma_commit(&acc_full[acc]);
+        if (ok) {
+          if (CG == 2)
+            ptx::mma_commit_pair_multicast(&acc_full[acc], 0x3);
+          else
+            ptx::mma_commit(&acc_full[acc]);
+        }
       }
       if (!ok) give_up();
       // every MMA issued has finished once this commit lands
-      ptx::mma_commit(drain);
+      if (CG == 2)
+        ptx::mma_commit_pair_multicast(drain, 0x1);
+      else
+        ptx::mma_commit(drain);
       ptx::mbar_wait(drain, 0, kWaitBudget, nullptr);
     }
   } else {
     // ---------------------------------------------------------------- epilogue
     uint32_t local = 0;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = unit; tile < num_tiles; tile += units, ++local) {
       const int vt = tile / g.n_tiles;
+      const int rt = vt * CG + (int)rank;              // this CTA's 128-row tile
       int i0, ni, bb0, nb;
       ntile_extent(g, tile % g.n_tiles, i0, ni, bb0, nb);
       const int rows = ni * g.BB;
@@ -205,7 +269,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
         break;
       }
       ptx::tc_fence_after();
-      const int v = vt * kBlockV + warp * 32 + lane;
+      const int v = rt * kBlockV + warp * 32 + lane;
       const bool live = v < g.Vh;
       const float bias_v = (g.bias && live) ? g.bias[v] : 0.f;
       float* cmax = s_cmax + (local & 1) * 4 * 256;
@@ -227,7 +291,21 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
           __syncwarp();
         }
         if (!live) continue;
-        if ((g.BB & 3) == 0) {
+        if (g.octet) {
+          // z[slot][row / 8][block][row % 8]: one column's 32 lanes store four 32-byte
+          // runs, and the columns of one slot fill a contiguous stretch
+          int il = c0 / g.BB, bl = c0 - (c0 / g.BB) * g.BB;
+          float* zo = g.z + ((size_t)(i0 + il) * (g.Vhp / 8) + (v >> 3)) * g.ldb * 8 + (v & 7);
+          const size_t slot_step = (g.Vhp / 8) * g.ldb * 8;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (c0 + j < rows && bl < nb) zo[(size_t)(bb0 + bl) * 8] = __uint_as_float(r[j]) + bias_v;
+            if (++bl == g.BB) {
+              bl = 0;
+              zo += slot_step;
+            }
+          }
+        } else if ((g.BB & 3) == 0) {
           // runs of four consecutive blocks of one slot: 16-byte stores
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
@@ -252,7 +330,13 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
         }
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&acc_empty[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if (CG == 2)
+          ptx::mbar_arrive_cluster(acc_empty0 + acc * 8);   // the leader's barrier
+        else
+          ptx::mbar_arrive(&acc_empty[acc]);
+      }
       if (g.zmax) {
         // the four warps' maxima are in (a bounded wait, so that a warp that gave up
         // cannot strand the others)
@@ -261,12 +345,14 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
           give_up();
           break;
         }
-        for (int c = threadIdx.x; c < rows; c += 128) {
-          const int il = c / g.BB, bl = c % g.BB;
-          if (bl < nb) {
-            const float m = fmaxf(fmaxf(cmax[c], cmax[256 + c]),
-                                  fmaxf(cmax[512 + c], cmax[768 + c]));
-            g.zmax[((size_t)(i0 + il) * g.B + bb0 + bl) * g.v_tiles + vt] = m;
+        if (rt * kBlockV < g.Vh) {
+          for (int c = threadIdx.x; c < rows; c += 128) {
+            const int il = c / g.BB, bl = c % g.BB;
+            if (bl < nb) {
+              const float m = fmaxf(fmaxf(cmax[c], cmax[256 + c]),
+                                    fmaxf(cmax[512 + c], cmax[768 + c]));
+              g.zmax[((size_t)(i0 + il) * g.B + bb0 + bl) * g.zm_tiles + rt] = m;
+            }
           }
         }
       }
@@ -275,9 +361,13 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
+  if (CG == 2) ptx::cluster_sync();             // the pair's MMAs and arrivals are done
   if (warp == 0) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, g.tmem_cols);
+    if (CG == 2)
+      ptx::tmem_dealloc_pair(tmem, g.tmem_cols);
+    else
+      ptx::tmem_dealloc(tmem, g.tmem_cols);
   }
 }
 
@@ -295,11 +385,51 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+constexpr int kMaxDevices = 64;
+constexpr int kSmemMax = 227 * 1024;   // opt-in shared memory limit of one CTA
+
+// Once per device and kernel form: allow the largest dynamic shared memory, and find how
+// many CTAs (CG = 1) or pairs (CG = 2) can be resident at once, which sizes the
+// persistent grid.
+template <int CG>
+cudaError_t resident_units(int* out) {
+  static std::mutex mu;
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] > 0) {
+    *out = cached[dev];
+    return cudaSuccess;
+  }
+  auto kern = logits_gemm_tc<CG>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int units = std::max(1, sms / CG);
+  if (CG > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * CG);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemMax;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0)
+      units = std::min(units, clusters);
+    cudaGetLastError();   // an occupancy query that failed leaves the estimate above
+  }
+  cached[dev] = units;
+  *out = units;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -316,15 +446,42 @@ GemmTilePlan plan_logits_gemm(int B, int N) {
   return t;
 }
 
+template <int CG>
+cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_h, const GemmArgs& g,
+                        size_t smem, cudaStream_t stream) {
+  if (smem > (size_t)kSmemMax) return cudaErrorInvalidValue;
+  int resident = 0;
+  cudaError_t e = resident_units<CG>(&resident);
+  if (e != cudaSuccess) return e;
+  const int tiles = g.v_tiles * g.n_tiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(std::max(1, std::min(tiles, resident)) * CG);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, logits_gemm_tc<CG>, tm_w, tm_h, g);
+}
+
 cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   const GemmTilePlan tp = plan_logits_gemm(p.B, p.N);
+  // a CTA pair splits the prediction rows by slot halves: needs an even slot count per
+  // tile and 16-row halves (whole swizzle atoms on both sides)
+  const int CG = (tp.Ni % 2 == 0 && (tp.BB * tp.Ni) % 32 == 0) ? 2 : 1;
   GemmArgs g{};
   g.z = p.z;
   g.Vhp = p.Vhp;
   g.ldb = p.ldb;
   g.zmax = p.zmax;
+  g.octet = p.z_octet ? 1 : 0;
   g.bias = p.lm_bias;
   g.err = p.ctrl;
   g.B = p.B;
@@ -334,11 +491,12 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   g.BB = tp.BB;
   g.Ni = tp.Ni;
   g.n_bt = tp.n_bt;
-  g.bn_mma = tp.bn_mma;
+  g.bn_mma = CG == 2 ? tp.BB * tp.Ni : tp.bn_mma;
   g.n_tiles = tp.n_it * tp.n_bt;
-  g.v_tiles = (p.Vh + kBlockV - 1) / kBlockV;
+  g.v_tiles = (p.Vh + kBlockV * CG - 1) / (kBlockV * CG);
+  g.zm_tiles = (int)(p.Vhp / kBlockV);
   g.num_kb = (p.H + kBlockK - 1) / kBlockK;
-  const uint32_t stage_bytes = kStageA + (uint32_t)g.bn_mma * kBlockK * 2;
+  const uint32_t stage_bytes = kStageA + (uint32_t)(g.bn_mma / CG) * kBlockK * 2;
   const size_t smem_budget = 220 * 1024 - (4 * 32 * 33 + 2 * 4 * 256) * sizeof(float);
   g.stages = (int)std::min<size_t>(8, (smem_budget - 1024 - 256) / stage_bytes);
   // 32-column TMEM loads may run past the last valid column of an accumulator, so
@@ -364,10 +522,10 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   }
   {
     // hidden [B, L_in, H] viewed as (h, block, slot) so that a box lands slot-major with
-    // the blocks of one slot contiguous
+    // the blocks of one slot contiguous; a pair member loads half of the tile's slots
     cuuint64_t dims[3] = {(cuuint64_t)p.H, (cuuint64_t)p.B, (cuuint64_t)p.L_in};
     cuuint64_t strides[2] = {(cuuint64_t)p.L_in * p.H * 2, (cuuint64_t)p.H * 2};
-    cuuint32_t box[3] = {kBlockK, (cuuint32_t)g.BB, (cuuint32_t)g.Ni};
+    cuuint32_t box[3] = {kBlockK, (cuuint32_t)g.BB, (cuuint32_t)(g.Ni / CG)};
     cuuint32_t es[3] = {1, 1, 1};
     if (encode(&tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)p.hidden, dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -375,12 +533,9 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
         CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(logits_gemm_tc,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = CG == 2 ? launch_gemm<2>(tm_w, tm_h, g, smem, p.stream)
+                          : launch_gemm<1>(tm_w, tm_h, g, smem, p.stream);
   if (e != cudaSuccess) return e;
-  const int tiles = g.v_tiles * g.n_tiles;
-  const int grid = std::min(tiles, sm_count());
-  logits_gemm_tc<<<grid, kThreads, smem, p.stream>>>(tm_w, tm_h, g);
   return cudaGetLastError();
 }
 

@@ -41,10 +41,19 @@ struct ProposePlan {
   const float* cnorm;   // prepared head: column norms of markov_w2 [Vhp]
   const float* cnmax;   // prepared head: per-tile maxima of cnorm [Vhp / 128]
   const unsigned* w1max;  // prepared head: max row norm of markov_w1 (float bits)
-  int32_t* cand_v;      // pruned chain: candidate head rows [N][B][cap]
+  int32_t* cand_v;      // pruned chain: candidate head rows of each slot [N][B][cap]
   float* cand_z;        //               their base logits
-  int32_t* cand_n;      //               candidate counts [N][B] (zeroed per call)
-  float* z;             // base logits [N][Vhp][ldb]: slot, head row, block (fastest)
+  int32_t* cand_n;      //               candidate counts [N][B]
+  int32_t* prev_v;      //               head rows that can be the previous slot's
+                        //               argmax [N][B][cap_a] (slot 0: the anchor)
+  int32_t* prev_n;      //               their counts [N][B]
+  int32_t* amax;        //               argmax head row given each previous row
+                        //               [N][B][cap_a]
+  int32_t* tk_id;       //               top-k tokens given each previous row
+  float* tk_val;        //               [N][B][cap_a][k], and their values
+  float* z;             // base logits: [N][Vhp][ldb] (slot, head row, block fastest), or
+                        // [N][Vhp / 8][ldb][8] when z_octet (see z_octet_index)
+  bool z_octet;
   size_t Vhp, ldb;      // head rows rounded up to whole 128-row tiles; blocks rounded to 4
   size_t ldz;           // row stride of zc
   float* zc;            // corrected logits of the current slot [B][ldz]
@@ -53,14 +62,22 @@ struct ProposePlan {
   cudaStream_t stream;
 };
 
+// Index of base logit (slot i, head row v, block b) in the octet layout: eight
+// consecutive head rows of one block are contiguous (one 32-byte sector), and the octets
+// of all blocks for the same rows follow each other, so the lm_head GEMM writes long
+// contiguous stretches while a scan of one block's rows reads whole sectors.
+__host__ __device__ __forceinline__ size_t z_octet_index(size_t i, size_t v, size_t b,
+                                                         size_t Vhp, size_t ldb) {
+  return ((i * (Vhp / 8) + v / 8) * ldb + b) * 8 + (v % 8);
+}
+
 // Upper bound on the chain kernel's grid (one CTA per SM).
 constexpr int kChainMaxCtas = 256;
 
 // Workspace carve-up shared by the size query and the launch.  [ctrl, zero_end) is
 // cleared at the start of every call.
 struct WorkspaceLayout {
-  size_t ctrl, bar, keys, cand_n, zero_end, z, zmax, cand, zc, prev, conf, part_val, part_id,
-      total;
+  size_t ctrl, bar, keys, zero_end, z, zmax, cand, zc, prev, conf, part_val, part_id, total;
   size_t Vhp, ldb, ldz;
 };
 WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool pruned);
@@ -74,7 +91,11 @@ struct PreparedLayout {
   size_t Vhp, tiles;
 };
 PreparedLayout plan_prepared(int Vh, int r);
-size_t pruned_list_bytes(int B, int N);   // candidate lists of the pruned chain
+// Candidate lists and tables of the pruned chain; the pieces lie in this order.
+struct PrunedLists {
+  size_t cand_v, cand_z, cand_n, prev_v, prev_n, amax, tk_id, tk_val, total;
+};
+PrunedLists plan_pruned_lists(int B, int N, int k);
 cudaError_t launch_prepare_head(const void* w1, const void* w2, int V, int r, int Vh,
                                 void* prepared, cudaStream_t stream);
 cudaError_t launch_chain_pruned(const ProposePlan& p);
