@@ -41,7 +41,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kCap = 512;                    // candidate list entries per (slot, block)
 constexpr int kCapA = 16;                    // possible previous rows tabulated per slot
 constexpr int kTabC = 128;                   // candidates tabulated per slot
-constexpr int kRowsChunk = 16;               // markov_w2 rows staged at a time
+constexpr int kRowsChunk = 32;               // markov_w2 rows staged at a time
 constexpr int kMaxKeep = 33;                 // survivors of a reduction: top_k <= 32, + argmax
 // candidate buffer entries: one round of appends (kWarps tiles of kTile rows) on top of
 // the survivors of a reduction
@@ -155,73 +155,6 @@ __device__ void block_pick(const Cand* buf, int n, bool by_z, bool first, float 
   out_id = bi;
 }
 
-// Warp-wide best (value, id) among vals/ids[0..n) strictly after (pv, pid) (all when
-// first).  Called by all 32 lanes of one warp; every lane returns the result.
-__device__ __forceinline__ void warp_pick(const float* vals, const int* ids, int n, bool first,
-                                          float pv, int pid, float& out_v, int& out_id) {
-  const int lane = threadIdx.x % 32;
-  float bv = -INFINITY;
-  int bi = 0x7FFFFFFF;
-  for (int j = lane; j < n; j += 32) {
-    const float x = vals[j];
-    const int id = ids ? ids[j] : j;
-    if (!first && !better(pv, pid, x, id)) continue;
-    if (better(x, id, bv, bi)) {
-      bv = x;
-      bi = id;
-    }
-  }
-  warp_best(bv, bi);
-  out_v = bv;
-  out_id = bi;
-}
-
-// Block-wide k-th best of vals[0..n) (ids = indices), with two block barriers: every
-// warp selects the best k of its stride, then warp 0 selects from those.  -inf when
-// n < k.  Uses scratch[] (>= kWarps * k floats and ints).
-__device__ float block_kth_fast(const float* vals, int n, int k, float* sc_v, int* sc_i,
-                                float* s_out) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int nw = blockDim.x / 32;
-  // warp w covers indices [w * chunk, (w + 1) * chunk)
-  const int chunk = (n + nw - 1) / nw;
-  const int lo = min(n, warp * chunk), hi = min(n, lo + chunk);
-  float pv = 0.f;
-  int pid = 0;
-  for (int q = 0; q < k; ++q) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    for (int t = lo + lane; t < hi; t += 32)
-      if ((q == 0 || better(pv, pid, vals[t], t)) && better(vals[t], t, bv, bi)) {
-        bv = vals[t];
-        bi = t;
-      }
-    warp_best(bv, bi);
-    if (lane == 0) {
-      sc_v[warp * k + q] = bv;
-      sc_i[warp * k + q] = bi;
-    }
-    pv = bv;
-    pid = bi;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    float rv = -INFINITY;
-    pv = 0.f;
-    pid = 0;
-    for (int q = 0; q < k; ++q) {
-      float bv;
-      int bi;
-      warp_pick(sc_v, sc_i, nw * k, q == 0, pv, pid, bv, bi);
-      pv = bv;
-      pid = bi;
-      rv = bv;
-    }
-    if (lane == 0) *s_out = n < k ? -INFINITY : rv;
-  }
-  __syncthreads();
-  return *s_out;
-}
 
 // Corrected logits of every buffer entry not evaluated yet (x is NaN): one warp per
 // entry, u from shared memory, the row of markov_w2 transposed from global memory.
@@ -292,6 +225,72 @@ __device__ void reduce_buffer(Cand* buf, int* s_n, int kk, bool by_z, const floa
 
 
 // ------------------------------------------------------------------ tables
+// Bitonic sort of the warp's 32 (value, id) pairs into the candidate order: afterwards
+// lane q holds the q-th best.
+__device__ __forceinline__ void warp_sort(float& v, int& id) {
+  const int lane = threadIdx.x % 32;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
+      const int oid = __shfl_xor_sync(0xFFFFFFFFu, id, stride);
+      // blocks of `size` lanes alternate between best-first and worst-first; the lower
+      // lane of a pair keeps the better entry in a best-first block
+      const bool best_first = (lane & size) == 0 || size == 32;
+      const bool lower = (lane & stride) == 0;
+      const bool take = (best_first == lower) ? better(ov, oid, v, id) : better(v, id, ov, oid);
+      if (take) {
+        v = ov;
+        id = oid;
+      }
+    }
+  }
+}
+
+// A lower bound on the k-th largest of the values the block's threads hold (k <= 32):
+// the k-th largest of the per-thread values, which the caller made the maxima of
+// disjoint subsets.  Since those maxima are a subset of the underlying values, their
+// k-th largest never exceeds the true one; it equals it unless two of the top k share a
+// thread.  Every warp sorts its 32, then warp 0 merges the warps' best k.
+__device__ float block_kth_of_maxima(float val, int k, float* s_top, float* s_out) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  int id = lane;
+  warp_sort(val, id);
+  if (lane < k) s_top[warp * 32 + lane] = val;
+  __syncthreads();
+  if (warp == 0) {
+    int h = 0;
+    float last = -INFINITY;
+    for (int q = 0; q < k; ++q) {
+      float c = (lane < kWarps && h < k) ? s_top[lane * 32 + h] : -INFINITY;
+      int ci = lane;
+      warp_best(c, ci);
+      if (lane == ci) ++h;
+      last = c;
+    }
+    if (lane == 0) *s_out = last;
+  }
+  __syncthreads();
+  return *s_out;
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 struct TableArgs {
   const float* z;            // octet layout (z_octet_index)
   const float* zmax;         // [N][B][T]
@@ -376,8 +375,7 @@ __global__ void __launch_bounds__(kThreads)
 pruned_table(const TableArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
   const int T4 = (a.T + 3) & ~3;
-  float* s_lb = (float*)dsm;                                   // [T4] lower bounds, slot i
-  float* s_ub = s_lb + T4;                                     // [T4] upper bounds, slot i
+  float* s_ub = (float*)dsm;                                   // [T4] upper bounds, slot i
   float* s_up = s_ub + T4;                                     // [T4] upper bounds, slot i-1
   int* s_tc = (int*)(s_up + T4);                               // [T4] tiles of C(i)
   int* s_ta = s_tc + T4;                                       // [T4] tiles of A(i-1)
@@ -386,8 +384,7 @@ pruned_table(const TableArgs a) {
   float* s_x = s_cz + kCap;                                    // [kCapA][kTabC]
   __nv_bfloat16* s_w1 = (__nv_bfloat16*)(s_x + kCapA * kTabC); // [kCapA][r]
   __nv_bfloat16* s_w2 = s_w1 + (size_t)kCapA * a.r;            // [kRowsChunk][r]
-  __shared__ float s_sc_v[kWarps * 32];
-  __shared__ int s_sc_i[kWarps * 32];
+  __shared__ float s_top[kWarps * 32];
   __shared__ float s_theta, s_red[kWarps];
   __shared__ int s_ntc, s_nta, s_nc, s_na;
   __shared__ int32_t s_av[kCapA];
@@ -403,13 +400,16 @@ pruned_table(const TableArgs a) {
     s_nc = 0;
     s_na = 0;
   }
-  // ---- bounds of slot i and slot i - 1 (all warps but the last), confidence (the last)
-  float mp = -INFINITY;                              // running max of slot i-1's lower bounds
+  // ---- bounds of slot i and slot i - 1 (all warps but the last), confidence (the last);
+  //      each thread keeps the maxima of the lower bounds / tile maxima it saw
+  float mp = -INFINITY;                              // slot i-1's lower bounds
+  float mlb = -INFINITY, mzm = -INFINITY;            // slot i's lower bounds, tile maxima
   if (warp < kWarps - 1) {
     for (int t = tid; t < a.T; t += kThreads - 32) {
       const float d = umax * a.cnmax[t] * (1.f + kRelMargin) + kAbsMargin;
       const float z0 = zm[t];
-      s_lb[t] = z0 - d;
+      mlb = fmaxf(mlb, z0 - d);
+      mzm = fmaxf(mzm, z0);
       s_ub[t] = z0 + d;
       if (zp) {
         const float z1 = zp[t];
@@ -448,19 +448,14 @@ pruned_table(const TableArgs a) {
   __syncthreads();
   // ---- thresholds: rank kk of slot i's lower bounds (rank 1 when the top-k ranks base
   //      logits, which then take rank kk of the tile maxima); rank 1 of slot i-1's
-  const float theta_x =
-      block_kth_fast(s_lb, a.T, a.zrank ? 1 : a.kk, s_sc_v, s_sc_i, &s_theta);
+  const float theta_x = block_kth_of_maxima(mlb, a.zrank ? 1 : a.kk, s_top, &s_theta);
   float theta_z = INFINITY;
-  if (a.zrank) {
-    for (int t = tid; t < a.T; t += kThreads) s_lb[t] = zm[t];
-    __syncthreads();
-    theta_z = block_kth_fast(s_lb, a.T, a.kk, s_sc_v, s_sc_i, &s_theta) - kAbsMargin;
-  }
+  if (a.zrank) theta_z = block_kth_of_maxima(mzm, a.kk, s_top, &s_theta) - kAbsMargin;
   float theta1 = s_red[0];
   for (int w = 1; w < kWarps; ++w) theta1 = fmaxf(theta1, s_red[w]);
   // ---- candidate tiles of both lists
   for (int t = tid; t < a.T; t += kThreads) {
-    if (s_ub[t] >= theta_x || zm[t] >= theta_z) s_tc[atomicAdd(&s_ntc, 1)] = t;
+    if (s_ub[t] >= theta_x || (a.zrank && zm[t] >= theta_z)) s_tc[atomicAdd(&s_ntc, 1)] = t;
     if (zp && s_up[t] >= theta1) s_ta[atomicAdd(&s_nta, 1)] = t;
   }
   __syncthreads();
@@ -503,16 +498,15 @@ pruned_table(const TableArgs a) {
       flag_error(a.err, kErrBadToken);
       tok = 0;
     }
-    *reinterpret_cast<uint4*>(s_w1 + (size_t)p * a.r + q * 8) =
-        *reinterpret_cast<const uint4*>(a.w1 + (size_t)tok * a.r + q * 8);
+    cp_async16(s_w1 + (size_t)p * a.r + q * 8, a.w1 + (size_t)tok * a.r + q * 8);
   }
   for (int c0 = 0; c0 < nc; c0 += kRowsChunk) {
     const int cnt = min(kRowsChunk, nc - c0);
     for (int c = tid; c < cnt * chunks; c += kThreads) {
       const int e = c / chunks, q = c % chunks;
-      *reinterpret_cast<uint4*>(s_w2 + (size_t)e * a.r + q * 8) =
-          *reinterpret_cast<const uint4*>(a.w2t + (size_t)s_cv[c0 + e] * a.r + q * 8);
+      cp_async16(s_w2 + (size_t)e * a.r + q * 8, a.w2t + (size_t)s_cv[c0 + e] * a.r + q * 8);
     }
+    cp_async_wait_all();
     __syncthreads();
     const int pairs = na * cnt, sub = tid % 8;
     for (int q0 = 0; q0 < pairs; q0 += kThreads / 8) {
@@ -559,6 +553,19 @@ pruned_table(const TableArgs a) {
     if (lane == 0) a.amax[ib * kCapA + p] = (bi >= 0 && bi < a.Vh) ? bi : -1;
     if (!a.want_topk) continue;
     const float* rk = a.zrank ? s_cz : x;
+    if (nc <= 32) {
+      // one entry per lane: sort the warp, lane q holds the q-th
+      float v = lane < nc ? rk[lane] : -INFINITY;
+      int id = lane < nc ? s_cv[lane] : 0x7FFFFFFF;
+      warp_sort(v, id);
+      if (lane < a.k) {
+        const size_t o = (ib * kCapA + p) * a.k + lane;
+        const int row = (id >= 0 && id < a.Vh) ? id : 0;
+        a.tk_id[o] = a.d2t ? a.d2t[row] : row;
+        a.tk_val[o] = v;
+      }
+      continue;
+    }
     float pv = 0.f;
     int pid = 0;
     for (int q = 0; q < a.k; ++q) {
@@ -613,16 +620,6 @@ struct SelectArgs {
 };
 
 constexpr int kMaxSlots = 256;               // prediction slots of the bf16 path
-
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                   (uint32_t)__cvta_generic_to_shared(dst)),
-               "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
 
 // z' = z + u . w2[:, v] for buffer entries [0, n), rows read from global memory: eight
 // lanes per entry, lane `sub` taking the 8-element chunks sub, sub + 8, ... of the row.
@@ -968,7 +965,7 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
     t.ifp = p.ifp;
     t.H = p.H;
     const size_t T4 = (size_t)((T + 3) & ~3);
-    const size_t smem = sizeof(float) * 5 * T4 + (sizeof(int32_t) + sizeof(float)) * kCap +
+    const size_t smem = sizeof(float) * 4 * T4 + (sizeof(int32_t) + sizeof(float)) * kCap +
                         sizeof(float) * kCapA * kTabC +
                         sizeof(__nv_bfloat16) * (size_t)(kCapA + kRowsChunk) * p.r;
     e = cudaFuncSetAttribute(pruned_table, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
