@@ -41,6 +41,11 @@ METRIC = "drafted slots/sec (propose+verify) at B=32, V=151936"
 UNIT = "slots/s"
 FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + written) of one lm_head GEMM launch from an ncu capture of the
+# current kernel, per workload; the summary and the command are in the named file.
+GEMM_TRAFFIC = {
+    "qwen3_8b_b32": (1.302e9 + 0.290e9, "profiles/logits_gemm_qwen3_8b_b32.md"),
+}
 
 
 def _peaks():
@@ -59,7 +64,7 @@ def _algorithmic(wl, V_head):
     """Algorithmic bytes and flops of one pass (all steps), and of the lm_head GEMM."""
     es = 2 if wl.dtype == "bf16" else 4
     M, H, r, B, N, k = wl.M, wl.H, wl.r, wl.B, wl.N, wl.top_k
-    gemm_bytes = V_head * H * es + M * H * es + M * V_head * 4 * 0   # W + hidden (+bias)
+    gemm_bytes = V_head * H * es + M * H * es          # lm_head + hidden
     gemm_flops = 2.0 * M * H * V_head
     markov_flops = 2.0 * M * r * V_head
     bytes_all = (V_head * H * es + r * V_head * es + M * r * es + B * wl.L_in * H * es
@@ -380,7 +385,10 @@ def run_ours(args):
                           "peaks": peaks["_source"]},
         "roofline": {"kernel": "base logits (lm_head GEMM)", "bound": "tensor",
                      "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": None,
+                     "frac": achieved / peak_tf,
+                     "traffic": GEMM_TRAFFIC.get(wl.name, (None, None))[0],
+                     "traffic_source": GEMM_TRAFFIC.get(wl.name, (None, None))[1],
+                     "algorithmic_bytes": alg["gemm_bytes"],
                      "peak_source": f"{peaks['_source']} bf16 burst"},
         "e2e": e2e,
         "gpu_launches": K * launches,
