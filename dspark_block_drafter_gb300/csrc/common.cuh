@@ -39,6 +39,15 @@ __device__ __forceinline__ float key_value(unsigned long long k) {
   return __uint_as_float(u);
 }
 
+// 32-bit key whose signed order is the order of the floats (for integer max reductions)
+__device__ __forceinline__ int order_key32(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : i ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float order_key32_value(int k) {
+  return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF);
+}
+
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
 }

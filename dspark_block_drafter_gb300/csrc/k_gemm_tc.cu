@@ -30,6 +30,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "common.cuh"
@@ -58,6 +59,7 @@ struct GemmArgs {
   int n_bt;        // N-tiles along the blocks (the slot index is tile / n_bt)
   int bn_mma;      // MMA N (rows of the B operand per stage), multiple of 16
   int acc_stride;  // TMEM columns between the two accumulators (multiple of 32)
+  int kpb;         // 64-wide K-blocks per stage, each loaded operand one copy per stage
   int n_tiles, v_tiles, num_kb, stages;
   int zm_tiles;    // 128-row tiles of the vocabulary (zmax row length)
   uint32_t tmem_cols;
@@ -84,21 +86,22 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t b_rows = (uint32_t)g.bn_mma / CG;            // B rows staged by this CTA
-  const uint32_t b_stage = b_rows * kBlockK * 2;
+  const uint32_t b_sub = b_rows * kBlockK * 2;                 // one K-block of them
+  const uint32_t b_stage = b_sub * g.kpb;
+  const uint32_t a_stage = kStageA * g.kpb;
   uint8_t* sA = smem;
-  uint8_t* sB = sA + (size_t)g.stages * kStageA;
+  uint8_t* sB = sA + (size_t)g.stages * a_stage;
   uint64_t* full = (uint64_t*)(sB + (size_t)g.stages * b_stage);
   uint64_t* empty = full + g.stages;
   uint64_t* acc_full = empty + g.stages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint64_t* tile_bar = drain + 1;                         // epilogue warps, per tile
-  uint32_t* tmem_slot = (uint32_t*)(tile_bar + 1);
+  uint64_t* tile_bar = drain + 1;                         // epilogue warps, per tile:
+  uint64_t* tile_bar2 = tile_bar + 1;                     // maxima in / maxima out
+  uint32_t* tmem_slot = (uint32_t*)(tile_bar2 + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-  // tile maxima: a padded 32 x 32 transpose panel per epilogue warp, and the four
-  // warps' column maxima, double-buffered by tile parity
-  float* s_panel = (float*)((uint8_t*)smem + g.stages * (kStageA + b_stage) + 256);
-  float* s_cmax = s_panel + 4 * 32 * 33;                 // [2][4][256]
+  // column maxima of the tile over the four epilogue warps, as order-preserving keys
+  int* s_cmax = (int*)((uint8_t*)smem + g.stages * (a_stage + b_stage) + 256);   // [256]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0;
@@ -116,9 +119,11 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     }
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(tile_bar, 128);
+    ptx::mbar_init(tile_bar2, 128);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
+  for (int c = threadIdx.x; c < 256; c += kThreads) s_cmax[c] = INT_MIN;
   if (warp == 4 && lane == 0) {
     ptx::tma_prefetch_desc(&tm_w);
     ptx::tma_prefetch_desc(&tm_h);
@@ -151,7 +156,8 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       const int ni_half = g.Ni / CG;
-      const uint32_t tx = CG * (kStageA + (uint32_t)(g.BB * ni_half) * kBlockK * 2);
+      const uint32_t tx = CG * (a_stage + (uint32_t)(g.BB * ni_half) * kBlockK * 2 * g.kpb);
+      const int num_st = g.num_kb / g.kpb;
       uint32_t it = 0;
       bool ok = true;
       for (int tile = unit; ok && tile < num_tiles; tile += units) {
@@ -159,23 +165,36 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
         const int row_a = (vt * CG + (int)rank) * kBlockV;
         const int bcol = (nt % g.n_bt) * g.BB;
         const int slot = g.ifp + (nt / g.n_bt) * g.Ni + (int)rank * ni_half;
-        for (int kb = 0; kb < g.num_kb; ++kb, ++it) {
+        for (int st = 0; st < num_st; ++st, ++it) {
           const uint32_t s = it % g.stages, ph = (it / g.stages) & 1;
           if (!ptx::mbar_wait(&empty[s], ph ^ 1, kWaitBudget, abort_flag)) {
             ok = false;
             break;
           }
-          if (CG == 2) {
+          uint8_t* da = sA + (size_t)s * a_stage;
+          uint8_t* db = sB + (size_t)s * b_stage;
+          if (g.kpb > 1) {
+            // K-blocks st * kpb ... as the third (lm_head) / fourth (hidden) map coordinate
+            const int kc = st * g.kpb;
+            if (CG == 2) {
+              const uint32_t bar = full0 + s * 8;
+              if (leader) ptx::mbar_arrive_expect_tx(&full[s], tx);
+              ptx::tma_load_3d_pair(da, &tm_w, bar, 0, row_a, kc);
+              ptx::tma_load_4d_pair(db, &tm_h, bar, 0, bcol, slot, kc);
+            } else {
+              ptx::mbar_arrive_expect_tx(&full[s], tx);
+              ptx::tma_load_3d(da, &tm_w, &full[s], 0, row_a, kc);
+              ptx::tma_load_4d(db, &tm_h, &full[s], 0, bcol, slot, kc);
+            }
+          } else if (CG == 2) {
             const uint32_t bar = full0 + s * 8;
             if (leader) ptx::mbar_arrive_expect_tx(&full[s], tx);
-            ptx::tma_load_2d_pair(sA + (size_t)s * kStageA, &tm_w, bar, kb * kBlockK, row_a);
-            ptx::tma_load_3d_pair(sB + (size_t)s * b_stage, &tm_h, bar, kb * kBlockK, bcol,
-                                  slot);
+            ptx::tma_load_2d_pair(da, &tm_w, bar, st * kBlockK, row_a);
+            ptx::tma_load_3d_pair(db, &tm_h, bar, st * kBlockK, bcol, slot);
           } else {
             ptx::mbar_arrive_expect_tx(&full[s], tx);
-            ptx::tma_load_2d(sA + (size_t)s * kStageA, &tm_w, &full[s], kb * kBlockK, row_a);
-            ptx::tma_load_3d(sB + (size_t)s * b_stage, &tm_h, &full[s], kb * kBlockK, bcol,
-                             slot);
+            ptx::tma_load_2d(da, &tm_w, &full[s], st * kBlockK, row_a);
+            ptx::tma_load_3d(db, &tm_h, &full[s], st * kBlockK, bcol, slot);
           }
         }
       }
@@ -212,23 +231,28 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem + acc * (uint32_t)g.acc_stride;
-        for (int kb = 0; kb < g.num_kb; ++kb, ++it) {
+        const int num_st = g.num_kb / g.kpb;
+        for (int st = 0; st < num_st; ++st, ++it) {
           const uint32_t s = it % g.stages, ph = (it / g.stages) & 1;
           if (!ptx::mbar_wait(&full[s], ph, kWaitBudget, abort_flag)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_u32(sA + (size_t)s * kStageA);
-          const uint32_t b0 = ptx::smem_u32(sB + (size_t)s * b_stage);
+          for (int kc = 0; kc < g.kpb; ++kc) {
+            // one K-block: a [128 x 64] lm_head tile and a [rows x 64] hidden tile
+            const uint32_t a0 = ptx::smem_u32(sA + (size_t)s * a_stage + kc * kStageA);
+            const uint32_t b0 = ptx::smem_u32(sB + (size_t)s * b_stage + kc * b_sub);
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k) {
-            if (CG == 2)
-              ptx::mma_f16_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
-                                ptx::desc_kmajor_sw128(b0 + k * 32), idesc, (kb | k) != 0);
-            else
-              ptx::mma_f16(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
-                           ptx::desc_kmajor_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+            for (int k = 0; k < kBlockK / 16; ++k) {
+              const uint32_t accum = (st | kc | k) != 0;
+              if (CG == 2)
+                ptx::mma_f16_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
+                                  ptx::desc_kmajor_sw128(b0 + k * 32), idesc, accum);
+              else
+                ptx::mma_f16(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
+                             ptx::desc_kmajor_sw128(b0 + k * 32), idesc, accum);
+            }
           }
           if (CG == 2)
             ptx::mma_commit_pair_multicast(&empty[s], 0x3);
@@ -272,23 +296,21 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       const int v = rt * kBlockV + warp * 32 + lane;
       const bool live = v < g.Vh;
       const float bias_v = (g.bias && live) ? g.bias[v] : 0.f;
-      float* cmax = s_cmax + (local & 1) * 4 * 256;
       for (int c0 = 0; c0 < rows; c0 += 32) {
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(tmem + lane_base + acc * (uint32_t)g.acc_stride + c0, r);
         ptx::tmem_ld_wait();
         if (g.zmax) {
-          // column maxima over this warp's 32 head rows, through a transpose panel
-          float* panel = s_panel + warp * 32 * 33;
+          // column maxima over this warp's 32 head rows (one warp reduction per column,
+          // lane j keeps column j), then over the four warps through shared memory
+          int mk = INT_MIN;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            panel[j * 33 + lane] = live ? __uint_as_float(r[j]) + bias_v : -INFINITY;
-          __syncwarp();
-          float m = -INFINITY;
-#pragma unroll 8
-          for (int q = 0; q < 32; ++q) m = fmaxf(m, panel[lane * 33 + q]);
-          cmax[warp * 256 + c0 + lane] = m;
-          __syncwarp();
+          for (int j = 0; j < 32; ++j) {
+            const int m = __reduce_max_sync(
+                0xFFFFFFFFu, order_key32(live ? __uint_as_float(r[j]) + bias_v : -INFINITY));
+            if (lane == j) mk = m;
+          }
+          if (c0 + lane < rows) atomicMax(&s_cmax[c0 + lane], mk);
         }
         if (!live) continue;
         if (g.octet) {
@@ -345,15 +367,18 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
           give_up();
           break;
         }
-        if (rt * kBlockV < g.Vh) {
-          for (int c = threadIdx.x; c < rows; c += 128) {
-            const int il = c / g.BB, bl = c % g.BB;
-            if (bl < nb) {
-              const float m = fmaxf(fmaxf(cmax[c], cmax[256 + c]),
-                                    fmaxf(cmax[512 + c], cmax[768 + c]));
-              g.zmax[((size_t)(i0 + il) * g.B + bb0 + bl) * g.zm_tiles + rt] = m;
-            }
-          }
+        for (int c = threadIdx.x; c < rows; c += 128) {
+          const int il = c / g.BB, bl = c % g.BB;
+          if (bl < nb && rt * kBlockV < g.Vh)
+            g.zmax[((size_t)(i0 + il) * g.B + bb0 + bl) * g.zm_tiles + rt] =
+                order_key32_value(s_cmax[c]);
+          s_cmax[c] = INT_MIN;
+        }
+        // every key is read and reset before any warp adds the next tile's
+        ptx::mbar_arrive(tile_bar2);
+        if (!ptx::mbar_wait(tile_bar2, local & 1, kWaitBudget, abort_flag)) {
+          give_up();
+          break;
         }
       }
     }
@@ -496,19 +521,57 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   g.v_tiles = (p.Vh + kBlockV * CG - 1) / (kBlockV * CG);
   g.zm_tiles = (int)(p.Vhp / kBlockV);
   g.num_kb = (p.H + kBlockK - 1) / kBlockK;
-  const uint32_t stage_bytes = kStageA + (uint32_t)(g.bn_mma / CG) * kBlockK * 2;
-  const size_t smem_budget = 220 * 1024 - (4 * 32 * 33 + 2 * 4 * 256) * sizeof(float);
-  g.stages = (int)std::min<size_t>(8, (smem_budget - 1024 - 256) / stage_bytes);
+  // Two K-blocks per stage when H allows: each operand then arrives in one 32 KB copy
+  // per stage instead of two 16 KB ones (a copy has a fixed cost in the TMA unit).
+  // (the hidden box must then fill whole 8-row swizzle atoms, so that the second
+  // K-block's rows start where the descriptors expect them)
+  const int box_rows = g.BB * g.Ni / CG;
+  g.kpb = (p.H % (2 * kBlockK) == 0 && box_rows % 8 == 0 && box_rows * CG == g.bn_mma) ? 2 : 1;
+  const uint32_t stage_bytes =
+      (kStageA + (uint32_t)(g.bn_mma / CG) * kBlockK * 2) * (uint32_t)g.kpb;
+  // shared memory: up to 1023 bytes of alignment, the stages, 256 bytes of barriers and
+  // the column-maximum keys
+  const size_t fixed = 1024 + 256 + 256 * sizeof(int);
+  g.stages = (int)std::min<size_t>(8, ((size_t)kSmemMax - fixed) / stage_bytes);
   // 32-column TMEM loads may run past the last valid column of an accumulator, so
   // each accumulator owns a multiple of 32 columns
   g.acc_stride = (g.bn_mma + 31) / 32 * 32;
   uint32_t cols = 32;
   while (cols < 2u * (uint32_t)g.acc_stride) cols <<= 1;
   g.tmem_cols = cols;
-  const size_t smem = 1024 + (size_t)g.stages * stage_bytes + 256 +
-                      (4 * 32 * 33 + 2 * 4 * 256) * sizeof(float);
+  const size_t smem = fixed + (size_t)g.stages * stage_bytes;
 
   CUtensorMap tm_w, tm_h;
+  if (g.kpb > 1) {
+    // lm_head [V_head, H] seen as (64 columns, row, 64-column chunk), and hidden
+    // [B, L_in, H] as (64 columns, block, slot, chunk): a box of kpb chunks lands as kpb
+    // consecutive [rows x 64] tiles, the layout of kpb single K-block stages
+    {
+      cuuint64_t dims[3] = {(cuuint64_t)kBlockK, (cuuint64_t)p.Vh, (cuuint64_t)(p.H / kBlockK)};
+      cuuint64_t strides[2] = {(cuuint64_t)p.H * 2, (cuuint64_t)kBlockK * 2};
+      cuuint32_t box[3] = {kBlockK, kBlockV, (cuuint32_t)g.kpb};
+      cuuint32_t es[3] = {1, 1, 1};
+      if (encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)p.lm_head, dims, strides,
+                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+          CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    {
+      cuuint64_t dims[4] = {(cuuint64_t)kBlockK, (cuuint64_t)p.B, (cuuint64_t)p.L_in,
+                            (cuuint64_t)(p.H / kBlockK)};
+      cuuint64_t strides[3] = {(cuuint64_t)p.L_in * p.H * 2, (cuuint64_t)p.H * 2,
+                               (cuuint64_t)kBlockK * 2};
+      cuuint32_t box[4] = {kBlockK, (cuuint32_t)g.BB, (cuuint32_t)(g.Ni / CG),
+                           (cuuint32_t)g.kpb};
+      cuuint32_t es[4] = {1, 1, 1, 1};
+      if (encode(&tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void*)p.hidden, dims, strides,
+                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+          CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+  } else {
   {
     cuuint64_t dims[2] = {(cuuint64_t)p.H, (cuuint64_t)p.Vh};
     cuuint64_t strides[1] = {(cuuint64_t)p.H * 2};
@@ -532,6 +595,7 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
         CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+  }
   }
   cudaError_t e = CG == 2 ? launch_gemm<2>(tm_w, tm_h, g, smem, p.stream)
                           : launch_gemm<1>(tm_w, tm_h, g, smem, p.stream);
