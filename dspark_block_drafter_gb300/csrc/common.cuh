@@ -48,6 +48,15 @@ __device__ __forceinline__ float order_key32_value(int k) {
   return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF);
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel still runs; it must wait for that
+// kernel's completion (and memory) before touching its results.  The previous kernel
+// lets it start early by signalling.  Both are no-ops without such a launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_signal() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
 }

@@ -390,6 +390,8 @@ pruned_table(const TableArgs a) {
   __shared__ int32_t s_av[kCapA];
   const int b = blockIdx.x, i = blockIdx.y;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  pdl_signal();
+  pdl_wait();                                        // z and zmax of the lm_head GEMM
   const float umax = __uint_as_float(*a.w1max) * (1.f + kRelMargin);
   const float* zm = a.zmax + ((size_t)i * a.B + b) * a.T;
   const float* zp = i > 0 ? a.zmax + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
@@ -676,6 +678,8 @@ pruned_select(const SelectArgs a) {
   __shared__ Cand s_stage[kMaxKeep];
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  pdl_signal();
+  pdl_wait();                                        // the tables
 
   // ---- counts, then the previous rows and argmax rows of every tabulated slot
   for (int i = tid; i < a.N; i += kThreads) {
@@ -970,8 +974,8 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
                         sizeof(__nv_bfloat16) * (size_t)(kCapA + kRowsChunk) * p.r;
     e = cudaFuncSetAttribute(pruned_table, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    pruned_table<<<dim3(p.B, p.N), kThreads, smem, p.stream>>>(t);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_dependent(pruned_table, dim3(p.B, p.N), dim3(kThreads), smem, p.stream, t);
+    if (e != cudaSuccess) return e;
   }
   SelectArgs s{};
   s.z = p.z;
@@ -1008,8 +1012,7 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   const size_t smem = sizeof(float) * ((p.r + 3) & ~3) + sizeof(Cand) * kCand;
   e = cudaFuncSetAttribute(pruned_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  pruned_select<<<p.B, kThreads, smem, p.stream>>>(s);
-  return cudaGetLastError();
+  return launch_dependent(pruned_select, dim3(p.B), dim3(kThreads), smem, p.stream, s);
 }
 
 }  // namespace dspark

@@ -137,6 +137,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       ptx::tmem_relinquish();
     }
   }
+  pdl_signal();                                 // the chain's kernels may be scheduled
   ptx::tc_fence_before();
   __syncthreads();
   if (CG == 2) ptx::cluster_sync();             // the peer's barriers are initialised

@@ -73,6 +73,7 @@ verify_kernel(int B, int N, const int32_t* __restrict__ draft,
               int32_t* __restrict__ emitted) {
   const int b = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
+  pdl_wait();                                        // the draft of the proposal
   if (b >= B) return;
   const int nd = min(max(n_draft[b], 0), N);
   const int32_t* d = draft + (size_t)b * N;
@@ -115,9 +116,9 @@ cudaError_t launch_verify(int B, int N, const int32_t* draft, const int32_t* n_d
                           const int32_t* target, int32_t* accepted, int32_t* bonus,
                           int32_t* emitted, cudaStream_t stream) {
   const int warps_per_cta = 8;
-  verify_kernel<<<(B + warps_per_cta - 1) / warps_per_cta, 32 * warps_per_cta, 0, stream>>>(
-      B, N, draft, n_draft, target, accepted, bonus, emitted);
-  return cudaGetLastError();
+  return launch_dependent(verify_kernel, dim3((B + warps_per_cta - 1) / warps_per_cta),
+                          dim3(32 * warps_per_cta), 0, stream, B, N, draft, n_draft, target,
+                          accepted, bonus, emitted);
 }
 
 }  // namespace dspark

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace dspark {
 
 // Everything a proposal launch needs, resolved by the ABI layer.
@@ -109,6 +111,25 @@ struct GemmTilePlan {
 GemmTilePlan plan_logits_gemm(int B, int N);
 
 cudaError_t launch_conf(const ProposePlan& p);
+
+// Launch `kernel` on `stream` with programmatic stream serialisation, so that it may
+// start before the previous kernel on the stream has finished (it calls pdl_wait()
+// before reading that kernel's results).
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 cudaError_t launch_base_logits_tc(const ProposePlan& p);
 cudaError_t launch_base_logits_simt(const ProposePlan& p);
 cudaError_t launch_chain_simt(const ProposePlan& p);
