@@ -462,14 +462,32 @@ cudaError_t resident_units(int* out) {
 
 // Tile plan of the lm_head GEMM for B blocks of N prediction slots.
 GemmTilePlan plan_logits_gemm(int B, int N) {
-  GemmTilePlan t{};
-  t.BB = B < 256 ? B : 256;
-  const int ni_max = std::max(1, 256 / t.BB);
-  t.n_it = (N + ni_max - 1) / ni_max;
-  t.Ni = (N + t.n_it - 1) / t.n_it;                  // balanced slot chunks
-  t.n_bt = (B + t.BB - 1) / t.BB;
-  t.bn_mma = (t.BB * t.Ni + 15) / 16 * 16;
-  return t;
+  // Candidate widths BB (blocks per tile); for each, slots are split into balanced
+  // chunks of at most 256 / BB.  The cost estimate counts MMA instructions per 128 head
+  // rows (halved when the tile qualifies for CTA pairs) times the measured time of one
+  // 128 x n x 16 MMA, about 108 + 0.078 n clocks: narrow MMAs are expensive per row.
+  GemmTilePlan best{};
+  double best_cost = 0.0;
+  const int widths[] = {256, 128, 64, 32, 16, 8, 4, 2, 1};
+  for (int w : widths) {
+    const int BB = std::min(B, w);
+    if (w < 256 && BB != w) continue;                // each width once
+    GemmTilePlan t{};
+    t.BB = BB;
+    const int ni_max = std::max(1, 256 / BB);
+    t.n_it = (N + ni_max - 1) / ni_max;
+    t.Ni = (N + t.n_it - 1) / t.n_it;                // balanced slot chunks
+    t.n_bt = (B + BB - 1) / BB;
+    t.bn_mma = (BB * t.Ni + 15) / 16 * 16;
+    const bool pair = t.Ni % 2 == 0 && (BB * t.Ni) % 32 == 0;
+    const double cost =
+        (double)t.n_it * t.n_bt * (108.0 + 0.078 * t.bn_mma) / (pair ? 2.0 : 1.0);
+    if (best.BB == 0 || cost < best_cost - 1e-9) {
+      best = t;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 template <int CG>
