@@ -46,6 +46,10 @@ constexpr int kBlockK = 64;       // one 128-byte swizzle row of bf16
 constexpr uint32_t kStageA = kBlockV * kBlockK * 2;   // 16 KB
 constexpr int kThreads = 192;
 constexpr long long kWaitBudget = 2000000000ll;       // ~1 s of SM clocks
+#ifndef DSPARK_GEMM_MAX_KPB
+#define DSPARK_GEMM_MAX_KPB 2
+#endif
+constexpr int kMaxKpb = DSPARK_GEMM_MAX_KPB;          // K-blocks per stage, at most
 
 struct GemmArgs {
   float* z;
@@ -158,7 +162,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     if (lane == 0) {
       const int ni_half = g.Ni / CG;
       const uint32_t tx = CG * (a_stage + (uint32_t)(g.BB * ni_half) * kBlockK * 2 * g.kpb);
-      const int num_st = g.num_kb / g.kpb;
+      const int num_st = (g.num_kb + g.kpb - 1) / g.kpb;
       uint32_t it = 0;
       bool ok = true;
       for (int tile = unit; ok && tile < num_tiles; tile += units) {
@@ -232,7 +236,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem + acc * (uint32_t)g.acc_stride;
-        const int num_st = g.num_kb / g.kpb;
+        const int num_st = (g.num_kb + g.kpb - 1) / g.kpb;
         for (int st = 0; st < num_st; ++st, ++it) {
           const uint32_t s = it % g.stages, ph = (it / g.stages) & 1;
           if (!ptx::mbar_wait(&full[s], ph, kWaitBudget, abort_flag)) {
@@ -241,6 +245,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
           }
           ptx::tc_fence_after();
           for (int kc = 0; kc < g.kpb; ++kc) {
+            if (st * g.kpb + kc >= g.num_kb) break;      // past H: zeros, nothing to add
             // one K-block: a [128 x 64] lm_head tile and a [rows x 64] hidden tile
             const uint32_t a0 = ptx::smem_u32(sA + (size_t)s * a_stage + kc * kStageA);
             const uint32_t b0 = ptx::smem_u32(sB + (size_t)s * b_stage + kc * b_sub);
@@ -543,14 +548,21 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   // Two K-blocks per stage when H allows: each operand then arrives in one 32 KB copy
   // per stage instead of two 16 KB ones (a copy has a fixed cost in the TMA unit).
   // (the hidden box must then fill whole 8-row swizzle atoms, so that the second
-  // K-block's rows start where the descriptors expect them)
-  const int box_rows = g.BB * g.Ni / CG;
-  g.kpb = (p.H % (2 * kBlockK) == 0 && box_rows % 8 == 0 && box_rows * CG == g.bn_mma) ? 2 : 1;
-  const uint32_t stage_bytes =
-      (kStageA + (uint32_t)(g.bn_mma / CG) * kBlockK * 2) * (uint32_t)g.kpb;
+  // K-block's rows start where the descriptors expect them).  A last stage reaching past
+  // H loads zeros there, which add nothing.
   // shared memory: up to 1023 bytes of alignment, the stages, 256 bytes of barriers and
   // the column-maximum keys
   const size_t fixed = 1024 + 256 + 256 * sizeof(int);
+  const int box_rows = g.BB * g.Ni / CG;
+  const uint32_t kblock_bytes = kStageA + (uint32_t)(g.bn_mma / CG) * kBlockK * 2;
+  g.kpb = 1;
+  if (p.H % kBlockK == 0 && box_rows % 8 == 0 && box_rows * CG == g.bn_mma)
+    for (int c = kMaxKpb; c > 1; --c)
+      if (g.num_kb >= c && ((size_t)kSmemMax - fixed) / (kblock_bytes * c) >= 2) {
+        g.kpb = c;
+        break;
+      }
+  const uint32_t stage_bytes = kblock_bytes * (uint32_t)g.kpb;
   g.stages = (int)std::min<size_t>(8, ((size_t)kSmemMax - fixed) / stage_bytes);
   // 32-column TMEM loads may run past the last valid column of an accumulator, so
   // each accumulator owns a multiple of 32 columns
