@@ -320,18 +320,19 @@ struct TableArgs {
 
 // Rows of the listed tiles whose upper bound reaches theta_x or whose base logit reaches
 // theta_z, appended in any order to s_v (and s_z): at most cap are kept, *s_cnt counts
-// them all.  One warp per tile, four rows a lane; each warp loads two tiles before it
+// them all.  One warp per tile, four rows a lane; each warp loads four tiles before it
 // looks at them.  zrow(v) = z + z_octet_index(slot, v, block).
 __device__ void scan_rows(const float* z, size_t i, size_t b, size_t Vhp, size_t ldb,
                           const int* s_tiles, int ntiles, const float* cnorm, float umax,
                           float theta_x, float theta_z, int Vh, int32_t* s_v, float* s_z,
                           int cap, int* s_cnt) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  for (int j0 = warp; j0 < ntiles; j0 += 2 * kWarps) {
-    float4 z4[2], c4[2];
-    int v0[2];
+  constexpr int kTilesPerRound = 4;
+  for (int j0 = warp; j0 < ntiles; j0 += kTilesPerRound * kWarps) {
+    float4 z4[kTilesPerRound], c4[kTilesPerRound];
+    int v0[kTilesPerRound];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kTilesPerRound; ++h) {
       const int j = j0 + h * kWarps;
       v0[h] = j < ntiles ? s_tiles[j] * kTile + lane * 4 : -1;
       if (v0[h] >= 0) {
@@ -340,7 +341,7 @@ __device__ void scan_rows(const float* z, size_t i, size_t b, size_t Vhp, size_t
       }
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kTilesPerRound; ++h) {
       if (j0 + h * kWarps >= ntiles) break;         // warp-uniform
       const float zq[4] = {z4[h].x, z4[h].y, z4[h].z, z4[h].w};
       const float cq[4] = {c4[h].x, c4[h].y, c4[h].z, c4[h].w};
@@ -407,16 +408,31 @@ pruned_table(const TableArgs a) {
   float mp = -INFINITY;                              // slot i-1's lower bounds
   float mlb = -INFINITY, mzm = -INFINITY;            // slot i's lower bounds, tile maxima
   if (warp < kWarps - 1) {
-    for (int t = tid; t < a.T; t += kThreads - 32) {
-      const float d = umax * a.cnmax[t] * (1.f + kRelMargin) + kAbsMargin;
-      const float z0 = zm[t];
-      mlb = fmaxf(mlb, z0 - d);
-      mzm = fmaxf(mzm, z0);
-      s_ub[t] = z0 + d;
-      if (zp) {
-        const float z1 = zp[t];
-        s_up[t] = z1 + d;
-        mp = fmaxf(mp, z1 - d);
+    // loads of up to kBoundsUnroll tiles per thread are issued before any is used
+    constexpr int kBoundsUnroll = 8;
+    const int stride = kThreads - 32;
+    for (int t0 = tid; t0 < a.T; t0 += kBoundsUnroll * stride) {
+      float c[kBoundsUnroll], z0[kBoundsUnroll], z1[kBoundsUnroll];
+#pragma unroll
+      for (int u = 0; u < kBoundsUnroll; ++u) {
+        const int t = t0 + u * stride;
+        const bool in = t < a.T;
+        c[u] = in ? a.cnmax[t] : 0.f;
+        z0[u] = in ? zm[t] : -INFINITY;
+        z1[u] = (in && zp) ? zp[t] : -INFINITY;
+      }
+#pragma unroll
+      for (int u = 0; u < kBoundsUnroll; ++u) {
+        const int t = t0 + u * stride;
+        if (t >= a.T) break;
+        const float d = umax * c[u] * (1.f + kRelMargin) + kAbsMargin;
+        mlb = fmaxf(mlb, z0[u] - d);
+        mzm = fmaxf(mzm, z0[u]);
+        s_ub[t] = z0[u] + d;
+        if (zp) {
+          s_up[t] = z1[u] + d;
+          mp = fmaxf(mp, z1[u] - d);
+        }
       }
     }
   } else if (a.w_conf) {
@@ -668,7 +684,7 @@ pruned_select(const SelectArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
   float* s_u = (float*)dsm;                                    // [r]
   Cand* buf = (Cand*)(s_u + ((a.r + 3) & ~3));                 // [kCand]
-  __shared__ int s_nc[kMaxSlots], s_na[kMaxSlots], s_pi[kMaxSlots];
+  __shared__ int s_nc[kMaxSlots], s_na[kMaxSlots], s_pi[kMaxSlots], s_row[kMaxSlots];
   __shared__ int32_t s_av[kMaxSlots][kCapA], s_am[kMaxSlots][kCapA];
   __shared__ float s_conf[kMaxSlots];
   __shared__ float s_red_v[kWarps];
@@ -719,7 +735,7 @@ pruned_select(const SelectArgs a) {
       if (row < 0 || row >= a.Vh) break;
       if (lane == 0) {
         s_pi[step] = pi;
-        a.draft[(size_t)b * a.N + step] = a.d2t ? a.d2t[row] : row;
+        s_row[step] = row;                           // drafted after the walk
       }
       prev = row;
     }
@@ -747,7 +763,7 @@ pruned_select(const SelectArgs a) {
           const int row = s_am[step][pi];
           if (row >= 0 && row < a.Vh) {
             s_prev = row;
-            a.draft[(size_t)b * a.N + step] = a.d2t ? a.d2t[row] : row;
+            s_row[step] = row;
           } else {
             pi = -1;
           }
@@ -814,7 +830,7 @@ pruned_select(const SelectArgs a) {
     block_pick(buf, nsel, false, true, 0.f, 0, av, ai, s_red_v, s_red_i);
     if (ai < 0 || ai >= a.Vh) ai = 0;                  // only if every value was NaN
     if (tid == 0) {
-      a.draft[(size_t)b * a.N + step] = a.d2t ? a.d2t[ai] : ai;
+      s_row[step] = ai;
       s_prev = ai;
     }
     if (a.want_topk) {
@@ -837,6 +853,11 @@ pruned_select(const SelectArgs a) {
     __syncthreads();
   }
 
+  // ---- the draft: every slot's chosen head row as a token
+  for (int i = tid; i < a.N; i += kThreads) {
+    const int row = s_row[i];
+    a.draft[(size_t)b * a.N + i] = a.d2t ? a.d2t[row] : row;
+  }
   // ---- top-k of the looked-up slots: the entries stored for the chosen previous row
   if (a.want_topk) {
     for (int e = tid; e < a.N * a.k; e += kThreads) {
