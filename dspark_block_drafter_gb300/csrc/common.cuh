@@ -19,7 +19,8 @@ __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162flo
 
 // Candidate order: larger value first, and among equal values the lower id first.
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
+  // bitwise, not short-circuit: no branch, so warps do not diverge on it
+  return (va > vb) | ((va == vb) & (ia < ib));
 }
 
 // 64-bit key whose unsigned order is the candidate order above: the float is mapped

@@ -38,6 +38,7 @@ namespace {
 constexpr int kTile = 128;
 constexpr int kThreads = 256;                // threads of both kernels
 constexpr int kWarps = kThreads / 32;
+static_assert((kWarps & (kWarps - 1)) == 0 && kWarps <= 32, "warp count: a power of two");
 constexpr int kCap = 512;                    // candidate list entries per (slot, block)
 constexpr int kCapA = 16;                    // possible previous rows tabulated per slot
 constexpr int kTabC = 128;                   // candidates tabulated per slot
@@ -237,13 +238,12 @@ __device__ __forceinline__ void warp_sort(float& v, int& id) {
       const int oid = __shfl_xor_sync(0xFFFFFFFFu, id, stride);
       // blocks of `size` lanes alternate between best-first and worst-first; the lower
       // lane of a pair keeps the better entry in a best-first block
-      const bool best_first = (lane & size) == 0 || size == 32;
+      const bool best_first = ((lane & size) == 0) | (size == 32);
       const bool lower = (lane & stride) == 0;
-      const bool take = (best_first == lower) ? better(ov, oid, v, id) : better(v, id, ov, oid);
-      if (take) {
-        v = ov;
-        id = oid;
-      }
+      const bool ob = better(ov, oid, v, id), mb = better(v, id, ov, oid);
+      const bool take = (best_first == lower) ? ob : mb;
+      v = take ? ov : v;
+      id = take ? oid : id;
     }
   }
 }
@@ -255,18 +255,42 @@ __device__ __forceinline__ void warp_sort(float& v, int& id) {
 // thread.  Every warp sorts its 32, then warp 0 merges the warps' best k.
 __device__ float block_kth_of_maxima(float val, int k, float* s_top, float* s_out) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (k == 1) {
+    // the largest: a plain block maximum
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) val = fmaxf(val, __shfl_xor_sync(0xFFFFFFFFu, val, o));
+    if (lane == 0) s_top[warp] = val;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = s_top[0];
+      for (int w = 1; w < kWarps; ++w) m = fmaxf(m, s_top[w]);
+      *s_out = m;
+    }
+    __syncthreads();
+    return *s_out;
+  }
   int id = lane;
   warp_sort(val, id);
   if (lane < k) s_top[warp * 32 + lane] = val;
   __syncthreads();
   if (warp == 0) {
+    // k rounds over the heads of the warps' sorted lists (lanes 0 .. kWarps-1)
     int h = 0;
     float last = -INFINITY;
     for (int q = 0; q < k; ++q) {
       float c = (lane < kWarps && h < k) ? s_top[lane * 32 + h] : -INFINITY;
       int ci = lane;
-      warp_best(c, ci);
-      if (lane == ci) ++h;
+#pragma unroll
+      for (int o = kWarps / 2; o > 0; o >>= 1) {
+        const float oc = __shfl_xor_sync(0xFFFFFFFFu, c, o);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, ci, o);
+        const bool t = better(oc, oi, c, ci);
+        c = t ? oc : c;
+        ci = t ? oi : ci;
+      }
+      c = __shfl_sync(0xFFFFFFFFu, c, 0);            // lanes >= kWarps ran their own
+      ci = __shfl_sync(0xFFFFFFFFu, ci, 0);          // groups; lane 0's group is the one
+      h += (lane == ci);
       last = c;
     }
     if (lane == 0) *s_out = last;
@@ -318,49 +342,65 @@ struct TableArgs {
   int B, N, V, Vh, T, r, k, kk, zrank, want_topk, L_in, ifp, H;
 };
 
-// Rows of the listed tiles whose upper bound reaches theta_x or whose base logit reaches
-// theta_z, appended in any order to s_v (and s_z): at most cap are kept, *s_cnt counts
-// them all.  One warp per tile, four rows a lane; each warp loads four tiles before it
-// looks at them.  zrow(v) = z + z_octet_index(slot, v, block).
-__device__ void scan_rows(const float* z, size_t i, size_t b, size_t Vhp, size_t ldb,
-                          const int* s_tiles, int ntiles, const float* cnorm, float umax,
-                          float theta_x, float theta_z, int Vh, int32_t* s_v, float* s_z,
-                          int cap, int* s_cnt) {
+// One list of candidate tiles of a (slot, block) row of z: rows whose upper bound
+// reaches theta_x or whose base logit reaches theta_z go to s_v (and s_z, when given):
+// at most cap are kept, *s_cnt counts them all.
+struct RowScan {
+  size_t slot;
+  const int* tiles;
+  int ntiles;
+  float theta_x, theta_z;
+  int32_t* s_v;
+  float* s_z;
+  int cap;
+  int* s_cnt;
+};
+
+// Both lists of a (slot, block) in one pass: one warp per tile, four rows a lane, and
+// each warp loads four tiles (of either list) before it looks at them, so the rows of
+// both lists cost one round of memory latency.  zrow(v) = z + z_octet_index(slot, v, b).
+__device__ void scan_rows(const float* z, size_t b, size_t Vhp, size_t ldb, const float* cnorm,
+                          float umax, int Vh, const RowScan& l0, const RowScan& l1) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   constexpr int kTilesPerRound = 4;
+  const int ntiles = l0.ntiles + l1.ntiles;
   for (int j0 = warp; j0 < ntiles; j0 += kTilesPerRound * kWarps) {
     float4 z4[kTilesPerRound], c4[kTilesPerRound];
     int v0[kTilesPerRound];
 #pragma unroll
     for (int h = 0; h < kTilesPerRound; ++h) {
       const int j = j0 + h * kWarps;
-      v0[h] = j < ntiles ? s_tiles[j] * kTile + lane * 4 : -1;
-      if (v0[h] >= 0) {
-        z4[h] = *reinterpret_cast<const float4*>(z + z_octet_index(i, v0[h], b, Vhp, ldb));
+      v0[h] = -1;
+      if (j < ntiles) {
+        const RowScan& l = j < l0.ntiles ? l0 : l1;
+        v0[h] = l.tiles[j < l0.ntiles ? j : j - l0.ntiles] * kTile + lane * 4;
+        z4[h] = *reinterpret_cast<const float4*>(z + z_octet_index(l.slot, v0[h], b, Vhp, ldb));
         c4[h] = *reinterpret_cast<const float4*>(cnorm + v0[h]);
       }
     }
 #pragma unroll
     for (int h = 0; h < kTilesPerRound; ++h) {
-      if (j0 + h * kWarps >= ntiles) break;         // warp-uniform
+      const int j = j0 + h * kWarps;
+      if (j >= ntiles) break;                        // warp-uniform
+      const RowScan& l = j < l0.ntiles ? l0 : l1;
       const float zq[4] = {z4[h].x, z4[h].y, z4[h].z, z4[h].w};
       const float cq[4] = {c4[h].x, c4[h].y, c4[h].z, c4[h].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int v = v0[h] + q;
         const bool take =
-            v < Vh && (zq[q] + umax * cq[q] * (1.f + kRelMargin) + kAbsMargin >= theta_x ||
-                       zq[q] >= theta_z);
+            (v < Vh) & ((zq[q] + umax * cq[q] * (1.f + kRelMargin) + kAbsMargin >= l.theta_x) |
+                        (zq[q] >= l.theta_z));
         const unsigned m = __ballot_sync(0xFFFFFFFFu, take);
         if (m == 0) continue;
         int base = 0;
-        if (lane == 0) base = atomicAdd(s_cnt, __popc(m));
+        if (lane == 0) base = atomicAdd(l.s_cnt, __popc(m));
         base = __shfl_sync(0xFFFFFFFFu, base, 0);
         if (take) {
           const int slot = base + __popc(m & ((1u << lane) - 1));
-          if (slot < cap) {
-            s_v[slot] = v;
-            if (s_z) s_z[slot] = zq[q];
+          if (slot < l.cap) {
+            l.s_v[slot] = v;
+            if (l.s_z) l.s_z[slot] = zq[q];
           }
         }
       }
@@ -478,12 +518,13 @@ pruned_table(const TableArgs a) {
   }
   __syncthreads();
   // ---- their rows
-  scan_rows(a.z, i, b, a.Vhp, a.ldb, s_tc, s_ntc, a.cnorm, umax, theta_x, theta_z, a.Vh, s_cv,
-            s_cz, kCap, &s_nc);
-  if (zp) {
-    scan_rows(a.z, i - 1, b, a.Vhp, a.ldb, s_ta, s_nta, a.cnorm, umax, theta1, INFINITY, a.Vh,
-              s_av, nullptr, kCapA, &s_na);
-  } else if (tid == 0) {
+  {
+    const RowScan lc{(size_t)i, s_tc, s_ntc, theta_x, theta_z, s_cv, s_cz, kCap, &s_nc};
+    const RowScan lp{zp ? (size_t)(i - 1) : 0, s_ta, zp ? s_nta : 0, theta1, INFINITY,
+                     s_av, nullptr, kCapA, &s_na};
+    scan_rows(a.z, b, a.Vhp, a.ldb, a.cnorm, umax, a.Vh, lc, lp);
+  }
+  if (!zp && tid == 0) {
     int p = a.anchors[b];
     if (p < 0 || p >= a.V) {
       flag_error(a.err, kErrBadToken);
