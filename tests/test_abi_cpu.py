@@ -77,6 +77,13 @@ def test_workspace_size_and_validation(lib):
     assert ds.dspark_propose_workspace_size(_cfg(dtype=1, H=60), _head()) == 0
     assert ds.dspark_propose_workspace_size(_cfg(dtype=1), _head(lm_head=0x1002)) == 0
     assert ds.dspark_propose_workspace_size(_cfg(dtype=1), _head()) > 0
+    # the bf16 path takes at most 256 prediction slots and a Markov rank of at most 512
+    assert ds.dspark_propose_workspace_size(_cfg(dtype=1, L_in=256), _head()) > 0
+    assert ds.dspark_propose_workspace_size(_cfg(dtype=1, L_in=257), _head()) == 0
+    assert ds.dspark_propose_workspace_size(_cfg(dtype=1, L_in=257, sample_from_anchor=0),
+                                            _head()) > 0
+    assert ds.dspark_propose_workspace_size(_cfg(dtype=1, r=512), _head()) > 0
+    assert ds.dspark_propose_workspace_size(_cfg(dtype=1, r=520), _head()) == 0
 
 
 def test_propose_rejects_before_launch(lib):

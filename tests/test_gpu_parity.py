@@ -164,3 +164,51 @@ def test_full_size_workload(name):
             g, _ = gpu_propose(wl, hd, bt, form, chain=chain)
             rep = compare(wl, hd, bt, o, g, form)
             assert rep["failures"] == [], (form, chain, rep)
+
+
+# ------------------------------------------------------------------ plan and limit edges
+@pytest.mark.parametrize("H", [192, 320])
+@pytest.mark.parametrize("chain", CHAINS)
+def test_ragged_last_k_stage(H, chain):
+    # H/64 odd: stages of two K-blocks end with one whose second half lies past H
+    run_case(_small(B=32, L_in=8, H=H, V=2048), chain=chain)
+
+
+@pytest.mark.parametrize("chain", CHAINS)
+def test_blocks_beyond_one_tile(chain):
+    # more than 256 blocks: several block tiles, the last one ragged
+    run_case(_small(B=300, L_in=2, H=64, V=512, r=16, top_k=2), chain=chain)
+
+
+@pytest.mark.parametrize("chain", CHAINS)
+def test_bonus_layout_six_slots(chain):
+    # the 1+N layout with 6 prediction slots and 64 blocks (32-block tiles of 6 slots)
+    run_case(_small(B=64, L_in=7, sample_from_anchor=False, H=128, V=1024, r=32, top_k=1),
+             chain=chain)
+
+
+@pytest.mark.parametrize("chain", CHAINS)
+def test_most_slots(chain):
+    # 256 prediction slots: the longest chain the bf16 path takes
+    run_case(_small(B=2, L_in=256, H=64, V=512, r=16, top_k=3), chain=chain)
+
+
+@pytest.mark.parametrize("chain", CHAINS)
+def test_largest_rank(chain):
+    # Markov rank 512: the largest the bf16 path takes
+    run_case(_small(B=8, L_in=4, H=64, V=512, r=512, top_k=4), chain=chain)
+
+
+def test_bad_anchor_sets_device_status_pruned():
+    import dspark_block_drafter_gb300 as ds
+    from dspark_block_drafter_gb300 import torch_io as tio
+    wl = _small(r=32)
+    hd, bt = make_head(wl), make_batch(wl)
+    bt["anchors"][2] = -3
+    cfg = tio.make_config(wl.B, wl.L_in, wl.H, wl.V, wl.r, wl.top_k, True, wl.conf_min, "bf16")
+    head = tio.head_to_device(hd).prepare(cfg)
+    out = tio.Outputs.allocate(wl.B, wl.N, wl.top_k, wl.V)
+    ws = tio.workspace_for(cfg, head)
+    tio.propose(cfg, head, tio.to_device(bt["hidden"]), tio.to_device(bt["anchors"]), out, ws)
+    assert tio.device_status(ws) == ds._abi.DSPARK_ERR_DEVICE
+    assert tio.device_status(ws) == 0
