@@ -83,7 +83,15 @@ __device__ __forceinline__ void ntile_extent(const GemmArgs& g, int nt, int& i0,
 // shares a 256-row tile with M = 256 pair MMAs (cta_group::2): each CTA stages its
 // 128 lm_head rows and half of the prediction rows, the leader (rank 0) issues the MMAs,
 // and each CTA's TMEM receives its own 128 rows of the result.
-template <int CG>
+//
+// PM = 1 (pairs whose N-tile holds exactly 256 prediction rows): the same staged tiles
+// enter the MMA the other way round, the prediction rows as M and the pair's 256 lm_head
+// rows as N, so that a TMEM lane holds one prediction row across 256 head rows.  The
+// epilogue then takes each 128-row tile maximum within one thread and stores each z
+// octet (8 head rows of one prediction row, 32 contiguous bytes) with one instruction:
+// far fewer instructions than the PM = 0 epilogue, which matters because the MMA thread
+// shares the SM's issue and memory pipes with it.
+template <int CG, int PM>
 __global__ void __launch_bounds__(kThreads, 1)
 logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_h, const GemmArgs g) {
@@ -163,7 +171,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       const int ni_half = g.Ni / CG;
       const uint32_t tx = CG * (a_stage + (uint32_t)(g.BB * ni_half) * kBlockK * 2 * g.kpb);
       const int num_st = (g.num_kb + g.kpb - 1) / g.kpb;
-      uint32_t it = 0;
+      uint32_t it = 0, s = 0, ph = 0;          // stages issued; ring slot and phase
       bool ok = true;
       for (int tile = unit; ok && tile < num_tiles; tile += units) {
         const int vt = tile / g.n_tiles, nt = tile % g.n_tiles;
@@ -171,7 +179,6 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
         const int bcol = (nt % g.n_bt) * g.BB;
         const int slot = g.ifp + (nt / g.n_bt) * g.Ni + (int)rank * ni_half;
         for (int st = 0; st < num_st; ++st, ++it) {
-          const uint32_t s = it % g.stages, ph = (it / g.stages) & 1;
           if (!ptx::mbar_wait(&empty[s], ph ^ 1, kWaitBudget, abort_flag)) {
             ok = false;
             break;
@@ -201,6 +208,10 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
             ptx::tma_load_2d(da, &tm_w, &full[s], st * kBlockK, row_a);
             ptx::tma_load_3d(db, &tm_h, &full[s], st * kBlockK, bcol, slot);
           }
+          if (++s == (uint32_t)g.stages) {
+            s = 0;
+            ph ^= 1;
+          }
         }
       }
       if (!ok) {
@@ -221,8 +232,15 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
-      uint32_t it = 0, local = 0;
+      // The tensor pipe holds only a couple of MMAs ahead of this thread, so whatever
+      // the thread does between two stages' MMAs (the barrier wait, the commit, the loop)
+      // leaves the pipe idle once it takes longer than those: keep it short, with the
+      // ring position counted incrementally and the usual two K-blocks per stage issued
+      // as one straight run.
+      uint32_t s = 0, ph = 0, local = 0;
       bool ok = true;
+      const int num_st = (g.num_kb + g.kpb - 1) / g.kpb;
+      const uint32_t a_base = ptx::smem_u32(sA), b_base = ptx::smem_u32(sB);
       for (int tile = unit; ok && tile < num_tiles; tile += units, ++local) {
         int i0, ni, bb0, nb;
         ntile_extent(g, tile % g.n_tiles, i0, ni, bb0, nb);
@@ -236,34 +254,62 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem + acc * (uint32_t)g.acc_stride;
-        const int num_st = (g.num_kb + g.kpb - 1) / g.kpb;
-        for (int st = 0; st < num_st; ++st, ++it) {
-          const uint32_t s = it % g.stages, ph = (it / g.stages) & 1;
-          if (!ptx::mbar_wait(&full[s], ph, kWaitBudget, abort_flag)) {
-            ok = false;
-            break;
+        // one K-block: a [128 x 64] lm_head tile and a [rows x 64] hidden tile, as four
+        // K = 16 MMAs (the descriptors' start addresses advance by 32 bytes = 2 units)
+        auto kblock = [&](uint32_t a0, uint32_t b0, bool first) {
+          const uint64_t da = ptx::desc_kmajor_sw128(PM ? b0 : a0);
+          const uint64_t db = ptx::desc_kmajor_sw128(PM ? a0 : b0);
+#pragma unroll
+          for (int k = 0; k < kBlockK / 16; ++k) {
+            const uint32_t accum = (first && k == 0) ? 0u : 1u;
+            if (CG == 2)
+              ptx::mma_f16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, accum);
+            else
+              ptx::mma_f16(d_tmem, da + 2 * k, db + 2 * k, idesc, accum);
           }
-          ptx::tc_fence_after();
-          for (int kc = 0; kc < g.kpb; ++kc) {
-            if (st * g.kpb + kc >= g.num_kb) break;      // past H: zeros, nothing to add
-            // one K-block: a [128 x 64] lm_head tile and a [rows x 64] hidden tile
-            const uint32_t a0 = ptx::smem_u32(sA + (size_t)s * a_stage + kc * kStageA);
-            const uint32_t b0 = ptx::smem_u32(sB + (size_t)s * b_stage + kc * b_sub);
+        };
+        bool ready = false;            // this stage's full barrier was seen complete already
+        for (int st = 0; st < num_st; ++st) {
+          if (!ready) {
+            if (!ptx::mbar_wait(&full[s], ph, kWaitBudget, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+          }
+          ready = false;
+          const uint32_t a_st = a_base + s * a_stage, b_st = b_base + s * b_stage;
+          const uint32_t s_next = s + 1 == (uint32_t)g.stages ? 0 : s + 1;
+          const uint32_t ph_next = s_next == 0 ? ph ^ 1 : ph;
+          const int nk = min(g.kpb, g.num_kb - st * g.kpb);   // past H: nothing to add
+          if (nk == 2) {
+            kblock(a_st, b_st, st == 0);
+            // look at the next stage's barrier while the pipe still holds MMAs of this
+            // one (a test that does not block), so that the stage change costs nothing
+            // when the copies are in already
+            const uint64_t da = ptx::desc_kmajor_sw128(PM ? b_st + b_sub : a_st + kStageA);
+            const uint64_t db = ptx::desc_kmajor_sw128(PM ? a_st + kStageA : b_st + b_sub);
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k) {
-              const uint32_t accum = (st | kc | k) != 0;
+              if (k == kBlockK / 16 - 1 && st + 1 < num_st) {
+                ready = ptx::mbar_test_wait(&full[s_next], ph_next);
+                if (ready) ptx::tc_fence_after();
+              }
               if (CG == 2)
-                ptx::mma_f16_pair(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
-                                  ptx::desc_kmajor_sw128(b0 + k * 32), idesc, accum);
+                ptx::mma_f16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, 1u);
               else
-                ptx::mma_f16(d_tmem, ptx::desc_kmajor_sw128(a0 + k * 32),
-                             ptx::desc_kmajor_sw128(b0 + k * 32), idesc, accum);
+                ptx::mma_f16(d_tmem, da + 2 * k, db + 2 * k, idesc, 1u);
             }
+          } else {
+            for (int kc = 0; kc < nk; ++kc)
+              kblock(a_st + kc * kStageA, b_st + kc * b_sub, st == 0 && kc == 0);
           }
           if (CG == 2)
             ptx::mma_commit_pair_multicast(&empty[s], 0x3);
           else
             ptx::mma_commit(&empty[s]);
+          s = s_next;
+          ph = ph_next;
         }
         if (ok) {
           if (CG == 2)
@@ -279,6 +325,67 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       else
         ptx::mma_commit(drain);
       ptx::mbar_wait(drain, 0, kWaitBudget, nullptr);
+    }
+  } else if (PM) {
+    // ---------------------------------------------------------------- epilogue (PM = 1)
+    // Thread = one prediction row of this CTA (its TMEM lane); columns = the pair's 256
+    // lm_head rows, 128 per tile maximum.
+    uint32_t local = 0;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int p = warp * 32 + lane;
+    const int il = p / g.BB, bl = p - il * g.BB;     // slot and block within this CTA's half
+    const size_t oct_step = g.ldb * 8;               // floats between consecutive row octets
+    for (int tile = unit; tile < num_tiles; tile += units, ++local) {
+      const int vt = tile / g.n_tiles;
+      int i0, ni, bb0, nb;
+      ntile_extent(g, tile % g.n_tiles, i0, ni, bb0, nb);
+      const int islot = (int)rank * (g.Ni / CG) + il;   // slot within the N-tile
+      const bool live = islot < ni && bl < nb;
+      const int i = i0 + islot, b = bb0 + bl;
+      const uint32_t acc = local & 1, aph = (local >> 1) & 1;
+      const bool ok = __all_sync(0xFFFFFFFFu,
+                                 ptx::mbar_wait(&acc_full[acc], aph, kWaitBudget, abort_flag));
+      if (!ok) {
+        give_up();
+        break;
+      }
+      ptx::tc_fence_after();
+      // z_octet_index(i, v, b) = zrow + (v / 8) * oct_step + v % 8
+      float* zrow = live ? g.z + ((size_t)i * (g.Vhp / 8) * g.ldb + (size_t)b) * 8 : g.z;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const int rt = vt * 2 + half;               // the 128-row tile of these columns
+        float m = -INFINITY;
+#pragma unroll 1
+        for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(tmem + lane_base + acc * (uint32_t)g.acc_stride + c0, r);
+          ptx::tmem_ld_wait();
+          const int v0 = vt * 256 + c0;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int v = v0 + 8 * q;                 // an octet: all in or all past the head
+            if (v >= g.Vh) break;
+            float x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(r[8 * q + j]);
+            if (g.bias) {
+              const float4 b0 = __ldg(reinterpret_cast<const float4*>(g.bias + v));
+              const float4 b1 = __ldg(reinterpret_cast<const float4*>(g.bias + v + 4));
+              x[0] += b0.x; x[1] += b0.y; x[2] += b0.z; x[3] += b0.w;
+              x[4] += b1.x; x[5] += b1.y; x[6] += b1.z; x[7] += b1.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m = fmaxf(m, x[j]);
+            if (live) ptx::st_global_v8(zrow + (size_t)(v >> 3) * oct_step, x);
+          }
+        }
+        if (g.zmax && live && rt * kBlockV < g.Vh)
+          g.zmax[((size_t)i * g.B + b) * g.zm_tiles + rt] = m;
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(acc_empty0 + acc * 8);   // the leader's barrier
     }
   } else {
     // ---------------------------------------------------------------- epilogue
@@ -435,7 +542,7 @@ cudaError_t resident_units(int* out) {
     *out = cached[dev];
     return cudaSuccess;
   }
-  auto kern = logits_gemm_tc<CG>;
+  auto kern = logits_gemm_tc<CG, 0>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
   if (e != cudaSuccess) return e;
   int sms = 0;
@@ -495,7 +602,7 @@ GemmTilePlan plan_logits_gemm(int B, int N) {
   return best;
 }
 
-template <int CG>
+template <int CG, int PM>
 cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_h, const GemmArgs& g,
                         size_t smem, cudaStream_t stream) {
   if (smem > (size_t)kSmemMax) return cudaErrorInvalidValue;
@@ -515,7 +622,24 @@ cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_h, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, logits_gemm_tc<CG>, tm_w, tm_h, g);
+  if (PM) {
+    // the PM form has the same resources; it needs its own shared-memory opt-in, once
+    // per device
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e2 = cudaGetDevice(&dev);
+    if (e2 != cudaSuccess) return e2;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+      e2 = cudaFuncSetAttribute(logits_gemm_tc<CG, PM>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+      if (e2 != cudaSuccess) return e2;
+      done[dev] = true;
+    }
+  }
+  return cudaLaunchKernelEx(&cfg, logits_gemm_tc<CG, PM>, tm_w, tm_h, g);
 }
 
 cudaError_t launch_base_logits_tc(const ProposePlan& p) {
@@ -628,8 +752,13 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
       return cudaErrorInvalidValue;
   }
   }
-  cudaError_t e = CG == 2 ? launch_gemm<2>(tm_w, tm_h, g, smem, p.stream)
-                          : launch_gemm<1>(tm_w, tm_h, g, smem, p.stream);
+  // prediction rows on M when the pair's N-tile is exactly 256 of them (z in the octet
+  // layout, which the PM epilogue writes)
+  const bool pm = CG == 2 && g.BB * g.Ni == 256 && g.octet &&
+                  ((uintptr_t)p.lm_bias & 15) == 0;   // 16-byte bias loads
+  cudaError_t e = CG == 2 ? (pm ? launch_gemm<2, 1>(tm_w, tm_h, g, smem, p.stream)
+                                : launch_gemm<2, 0>(tm_w, tm_h, g, smem, p.stream))
+                          : launch_gemm<1, 0>(tm_w, tm_h, g, smem, p.stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

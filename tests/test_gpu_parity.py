@@ -212,3 +212,26 @@ def test_bad_anchor_sets_device_status_pruned():
     tio.propose(cfg, head, tio.to_device(bt["hidden"]), tio.to_device(bt["anchors"]), out, ws)
     assert tio.device_status(ws) == ds._abi.DSPARK_ERR_DEVICE
     assert tio.device_status(ws) == 0
+
+
+# ------------------------------------------------------------------ pair tiles of exactly
+# 256 prediction rows, which the lm_head GEMM runs with the prediction rows on the MMA's M
+@pytest.mark.parametrize("H", [256, 200, 320])
+def test_pm_tiles_h_stages(H):
+    # H = 256: two K-blocks per stage; 200: one per stage; 320: a ragged last stage
+    run_case(_small(B=32, L_in=8, H=H, V=1000, r=16, top_k=3), chain="pruned")
+
+
+def test_pm_tiles_ragged_slots_and_blocks():
+    # 15 slots in chunks of 8 and 7; 70 blocks in tiles of 64 and 6
+    run_case(_small(B=32, L_in=15, H=128, V=2048, r=16, top_k=2), chain="pruned")
+    run_case(_small(B=70, L_in=4, H=128, V=1024, r=16, top_k=2), chain="pruned")
+
+
+@pytest.mark.parametrize("form", ["full", "d2t"])
+@pytest.mark.parametrize("sfa", [True, False])
+def test_pm_tiles_reduced_vocab(form, sfa):
+    wl = _small(B=32, L_in=9 if not sfa else 8, H=128, n_emit=304, sample_from_anchor=sfa, V=1024)
+    g, o, rep = run_case(wl, form, chain="pruned")
+    emit = set(make_head(wl)["emit_rows"].tolist())
+    assert set(g["draft"].ravel().tolist()) <= emit
