@@ -268,38 +268,17 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
               ptx::mma_f16(d_tmem, da + 2 * k, db + 2 * k, idesc, accum);
           }
         };
-        bool ready = false;            // this stage's full barrier was seen complete already
         for (int st = 0; st < num_st; ++st) {
-          if (!ready) {
-            if (!ptx::mbar_wait(&full[s], ph, kWaitBudget, abort_flag)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
+          if (!ptx::mbar_wait(&full[s], ph, kWaitBudget, abort_flag)) {
+            ok = false;
+            break;
           }
-          ready = false;
+          ptx::tc_fence_after();
           const uint32_t a_st = a_base + s * a_stage, b_st = b_base + s * b_stage;
-          const uint32_t s_next = s + 1 == (uint32_t)g.stages ? 0 : s + 1;
-          const uint32_t ph_next = s_next == 0 ? ph ^ 1 : ph;
           const int nk = min(g.kpb, g.num_kb - st * g.kpb);   // past H: nothing to add
           if (nk == 2) {
             kblock(a_st, b_st, st == 0);
-            // look at the next stage's barrier while the pipe still holds MMAs of this
-            // one (a test that does not block), so that the stage change costs nothing
-            // when the copies are in already
-            const uint64_t da = ptx::desc_kmajor_sw128(PM ? b_st + b_sub : a_st + kStageA);
-            const uint64_t db = ptx::desc_kmajor_sw128(PM ? a_st + kStageA : b_st + b_sub);
-#pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k) {
-              if (k == kBlockK / 16 - 1 && st + 1 < num_st) {
-                ready = ptx::mbar_test_wait(&full[s_next], ph_next);
-                if (ready) ptx::tc_fence_after();
-              }
-              if (CG == 2)
-                ptx::mma_f16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, 1u);
-              else
-                ptx::mma_f16(d_tmem, da + 2 * k, db + 2 * k, idesc, 1u);
-            }
+            kblock(a_st + kStageA, b_st + b_sub, false);
           } else {
             for (int kc = 0; kc < nk; ++kc)
               kblock(a_st + kc * kStageA, b_st + kc * b_sub, st == 0 && kc == 0);
@@ -308,8 +287,10 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
             ptx::mma_commit_pair_multicast(&empty[s], 0x3);
           else
             ptx::mma_commit(&empty[s]);
-          s = s_next;
-          ph = ph_next;
+          if (++s == (uint32_t)g.stages) {
+            s = 0;
+            ph ^= 1;
+          }
         }
         if (ok) {
           if (CG == 2)
