@@ -38,10 +38,14 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
   w.ctrl = take(256);
   w.bar = take(sizeof(unsigned) * (size_t)((B + 31) / 32));
   w.keys = take(sizeof(unsigned long long) * (size_t)N * B);
+  // the maxima of the lower bounds with which the GEMM leaves tiles of z out start from
+  // zero (below every key) in every pass
+  if (pruned) w.zbound = take(sizeof(uint32_t) * (size_t)N * B * k);
   w.zero_end = off;
   w.z = take(sizeof(float) * (size_t)N * w.Vhp * w.ldb);
   if (pruned) {
     w.zmax = take(sizeof(float) * (size_t)N * B * (w.Vhp / 128));
+    w.zwritten = take((size_t)N * B * (w.Vhp / 128));
     w.cand = take(plan_pruned_lists(B, N, k).total);
   }
   if (dtype == DSPARK_F32) {          // the CUDA-core chain keeps one corrected row per block
@@ -195,6 +199,14 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
     p.tk_id = (int32_t*)(lists + ll.tk_id);
     p.tk_val = (float*)(lists + ll.tk_val);
     p.z_octet = true;           // the candidate scans read one block's rows of z
+    // Tiles of z that provably cannot hold a slot's top k are left out by the GEMM when
+    // it runs with the prediction rows on M and the top-k ranks corrected logits.
+    const bool want_topk = out->topk_ids || out->topk_vals;
+    if (logits_gemm_pm(cfg->B, N, true, head->lm_bias) && (!want_topk || cfg->topk_markov)) {
+      p.zbound = (uint32_t*)(ws + wl.zbound);
+      p.zwritten = (uint8_t*)(ws + wl.zwritten);
+      p.zbound_k = want_topk ? cfg->top_k : 1;
+    }
   }
 
   cudaError_t e;

@@ -48,8 +48,8 @@ constexpr int kMaxKeep = 33;                 // survivors of a reduction: top_k 
 // the survivors of a reduction
 constexpr int kCand = kWarps * kTile + 64;
 static_assert(kCand >= kWarps * kTile + kMaxKeep, "candidate buffer too small");
-constexpr float kRelMargin = 1.0f / 1024;    // fp32 rounding margins of the bounds
-constexpr float kAbsMargin = 1e-4f;
+constexpr float kRelMargin = kPrunedRelMargin;    // fp32 rounding margins of the bounds
+constexpr float kAbsMargin = kPrunedAbsMargin;
 
 // ------------------------------------------------------------------ preparation
 // w2t[v][k] = w2[k][v] through 32 x 32 shared-memory tiles.
@@ -318,6 +318,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 struct TableArgs {
   const float* z;            // octet layout (z_octet_index)
   const float* zmax;         // [N][B][T]
+  const uint8_t* zw;         // [N][B][T]: 0 where the GEMM left the tile's z out, or NULL
   size_t Vhp, ldb;
   const float* cnorm;        // [Vhp]
   const float* cnmax;        // [T]
@@ -511,10 +512,14 @@ pruned_table(const TableArgs a) {
   if (a.zrank) theta_z = block_kth_of_maxima(mzm, a.kk, s_top, &s_theta) - kAbsMargin;
   float theta1 = s_red[0];
   for (int w = 1; w < kWarps; ++w) theta1 = fmaxf(theta1, s_red[w]);
-  // ---- candidate tiles of both lists
+  // ---- candidate tiles of both lists.  A tile the GEMM left out of z had an upper bound
+  //      below a lower bound of this rank's threshold, so it holds no candidate either.
+  const uint8_t* wi = a.zw ? a.zw + ((size_t)i * a.B + b) * a.T : nullptr;
+  const uint8_t* wp = (a.zw && zp) ? a.zw + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
   for (int t = tid; t < a.T; t += kThreads) {
-    if (s_ub[t] >= theta_x || (a.zrank && zm[t] >= theta_z)) s_tc[atomicAdd(&s_ntc, 1)] = t;
-    if (zp && s_up[t] >= theta1) s_ta[atomicAdd(&s_nta, 1)] = t;
+    if ((s_ub[t] >= theta_x || (a.zrank && zm[t] >= theta_z)) && (!wi || wi[t]))
+      s_tc[atomicAdd(&s_ntc, 1)] = t;
+    if (zp && s_up[t] >= theta1 && (!wp || wp[t])) s_ta[atomicAdd(&s_nta, 1)] = t;
   }
   __syncthreads();
   // ---- their rows
@@ -655,6 +660,8 @@ pruned_table(const TableArgs a) {
 // ------------------------------------------------------------------ the walk
 struct SelectArgs {
   const float* z;            // octet layout (read only to evaluate every row)
+  const uint8_t* zw;         // [N][B][T]: 0 where the GEMM left the tile's z out, or NULL
+  int T;
   size_t Vhp, ldb;
   const __nv_bfloat16* w1;   // [V][r]
   const __nv_bfloat16* w2t;  // [Vhp][r]
@@ -853,8 +860,11 @@ pruned_select(const SelectArgs a) {
         const int base = s_nfull;
         __syncthreads();
         for (int j = tid; j < cnt; j += kThreads) {
-          buf[base + j].v = v0 + j;
-          buf[base + j].z = a.z[z_octet_index(step, v0 + j, b, a.Vhp, a.ldb)];
+          const int v = v0 + j;
+          // rows of a tile the GEMM left out cannot reach this slot's top k
+          const bool in = !a.zw || a.zw[((size_t)step * a.B + b) * a.T + v / kTile];
+          buf[base + j].v = v;
+          buf[base + j].z = in ? a.z[z_octet_index(step, v, b, a.Vhp, a.ldb)] : -INFINITY;
           buf[base + j].x = NAN;
         }
         __syncthreads();
@@ -995,6 +1005,7 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
     TableArgs t{};
     t.z = p.z;
     t.zmax = p.zmax;
+    t.zw = p.zwritten;
     t.Vhp = p.Vhp;
     t.ldb = p.ldb;
     t.cnorm = p.cnorm;
@@ -1041,6 +1052,8 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   }
   SelectArgs s{};
   s.z = p.z;
+  s.zw = p.zwritten;
+  s.T = T;
   s.Vhp = p.Vhp;
   s.ldb = p.ldb;
   s.w1 = (const __nv_bfloat16*)p.w1;

@@ -55,6 +55,13 @@ struct GemmArgs {
   float* z;
   size_t Vhp, ldb;
   float* zmax;     // [N][B][zm_tiles] per-tile maxima of z, or NULL
+  // Tiles of z that cannot matter (PM = 1 only; zbound_k = 0 stores every tile): see the
+  // PM = 1 epilogue.
+  uint32_t* zbound;        // [N][B][zbound_k] maxima of tile lower bounds (order keys)
+  uint8_t* zwritten;       // [N][B][zm_tiles]
+  const float* cnmax;      // [zm_tiles] largest markov_w2 column norm of each tile
+  const unsigned* w1max;   // largest markov_w1 row norm (float bits)
+  int zbound_k;
   int octet;       // z layout: [N][Vhp / 8][ldb][8] (1) or [N][Vhp][ldb] (0)
   const float* bias;
   uint32_t* err;
@@ -311,11 +318,24 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     // ---------------------------------------------------------------- epilogue (PM = 1)
     // Thread = one prediction row of this CTA (its TMEM lane); columns = the pair's 256
     // lm_head rows, 128 per tile maximum.
+    //
+    // Leaving out tiles of z (zbound_k > 0).  With the Markov term bounded by
+    // |markov_w1[p] . markov_w2[:, v]| <= Umax cn[v] (Cauchy-Schwarz), a tile T of this
+    // row holds a corrected logit >= lb[T] = zmax[T] - Umax cmax[T] and none above
+    // ub[T] = zmax[T] + Umax cmax[T].  Every thread posts lb[T] into one of zbound_k
+    // maxima (T mod zbound_k): the smallest of those maxima is a lower bound of
+    // zbound_k distinct tiles' lb, hence of the zbound_k-th largest corrected logit.  A
+    // tile whose ub stays below it can hold none of the top zbound_k (nor the argmax):
+    // its z is not stored, and zwritten says so to the chain.
     uint32_t local = 0;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int p = warp * 32 + lane;
     const int il = p / g.BB, bl = p - il * g.BB;     // slot and block within this CTA's half
     const size_t oct_step = g.ldb * 8;               // floats between consecutive row octets
+    const int K = g.zbound_k;
+    const float umax = K > 0 ? __uint_as_float(*g.w1max) * (1.f + kPrunedRelMargin) : 0.f;
+    // a key of the same order as the float, 0 below every float
+    auto ukey = [](float f) { return (uint32_t)order_key32(f) ^ 0x80000000u; };
     for (int tile = unit; tile < num_tiles; tile += units, ++local) {
       const int vt = tile / g.n_tiles;
       int i0, ni, bb0, nb;
@@ -333,9 +353,19 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       ptx::tc_fence_after();
       // z_octet_index(i, v, b) = zrow + (v / 8) * oct_step + v % 8
       float* zrow = live ? g.z + ((size_t)i * (g.Vhp / 8) * g.ldb + (size_t)b) * 8 : g.z;
+      uint32_t* bound = (K > 0 && live) ? g.zbound + ((size_t)i * g.B + b) * K : nullptr;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         const int rt = vt * 2 + half;               // the 128-row tile of these columns
+        const bool tile_in = rt * kBlockV < g.Vh;
+        // the current threshold (read first, so that its latency hides behind the TMEM
+        // loads; any value read is a valid bound, they only grow)
+        uint32_t th = 0;
+        if (bound && tile_in) {
+          th = 0xFFFFFFFFu;
+          for (int j = 0; j < K; ++j) th = min(th, __ldcg(bound + j));
+        }
+        // this tile's maximum, with the bias
         float m = -INFINITY;
 #pragma unroll 1
         for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
@@ -358,11 +388,45 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) m = fmaxf(m, x[j]);
-            if (live) ptx::st_global_v8(zrow + (size_t)(v >> 3) * oct_step, x);
+            if (live && K == 0) ptx::st_global_v8(zrow + (size_t)(v >> 3) * oct_step, x);
           }
         }
-        if (g.zmax && live && rt * kBlockV < g.Vh)
-          g.zmax[((size_t)i * g.B + b) * g.zm_tiles + rt] = m;
+        bool store = live && tile_in;
+        if (live && tile_in) {
+          if (bound) {
+            const float d = umax * g.cnmax[rt] * (1.f + kPrunedRelMargin) + kPrunedAbsMargin;
+            store = ukey(m + d) >= th;
+            atomicMax(bound + rt % K, ukey(m - d));
+          }
+          if (g.zmax) g.zmax[((size_t)i * g.B + b) * g.zm_tiles + rt] = m;
+          if (g.zwritten) g.zwritten[((size_t)i * g.B + b) * g.zm_tiles + rt] = store ? 1 : 0;
+        }
+        // the stores, from a second read of TMEM (a collective of the warp: every lane
+        // takes part when any of them stores)
+        if (K > 0 && __any_sync(0xFFFFFFFFu, store)) {
+#pragma unroll 1
+          for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(tmem + lane_base + acc * (uint32_t)g.acc_stride + c0, r);
+            ptx::tmem_ld_wait();
+            const int v0 = vt * 256 + c0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int v = v0 + 8 * q;
+              if (v >= g.Vh) break;
+              float x[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(r[8 * q + j]);
+              if (g.bias) {
+                const float4 b0 = __ldg(reinterpret_cast<const float4*>(g.bias + v));
+                const float4 b1 = __ldg(reinterpret_cast<const float4*>(g.bias + v + 4));
+                x[0] += b0.x; x[1] += b0.y; x[2] += b0.z; x[3] += b0.w;
+                x[4] += b1.x; x[5] += b1.y; x[6] += b1.z; x[7] += b1.w;
+              }
+              if (store) ptx::st_global_v8(zrow + (size_t)(v >> 3) * oct_step, x);
+            }
+          }
+        }
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -553,6 +617,14 @@ cudaError_t resident_units(int* out) {
 
 }  // namespace
 
+// Prediction rows on M when the pair's N-tile is exactly 256 of them (z in the octet
+// layout, which the PM epilogue writes; 16-byte bias loads).
+bool logits_gemm_pm(int B, int N, bool z_octet, const float* lm_bias) {
+  const GemmTilePlan tp = plan_logits_gemm(B, N);
+  const bool pair = tp.Ni % 2 == 0 && (tp.BB * tp.Ni) % 32 == 0;
+  return pair && tp.BB * tp.Ni == 256 && z_octet && ((uintptr_t)lm_bias & 15) == 0;
+}
+
 // Tile plan of the lm_head GEMM for B blocks of N prediction slots.
 GemmTilePlan plan_logits_gemm(int B, int N) {
   // Candidate widths BB (blocks per tile); for each, slots are split into balanced
@@ -632,6 +704,11 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   const int CG = (tp.Ni % 2 == 0 && (tp.BB * tp.Ni) % 32 == 0) ? 2 : 1;
   GemmArgs g{};
   g.z = p.z;
+  g.zbound = p.zbound;
+  g.zwritten = p.zwritten;
+  g.cnmax = p.cnmax;
+  g.w1max = p.w1max;
+  g.zbound_k = p.zbound_k;
   g.Vhp = p.Vhp;
   g.ldb = p.ldb;
   g.zmax = p.zmax;
@@ -733,10 +810,9 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
       return cudaErrorInvalidValue;
   }
   }
-  // prediction rows on M when the pair's N-tile is exactly 256 of them (z in the octet
-  // layout, which the PM epilogue writes)
-  const bool pm = CG == 2 && g.BB * g.Ni == 256 && g.octet &&
-                  ((uintptr_t)p.lm_bias & 15) == 0;   // 16-byte bias loads
+  const bool pm = logits_gemm_pm(p.B, p.N, p.z_octet, p.lm_bias);
+  // only the PM form leaves tiles out (and writes zwritten)
+  if ((p.zbound_k > 0 || p.zwritten) && !pm) return cudaErrorInvalidValue;
   cudaError_t e = CG == 2 ? (pm ? launch_gemm<2, 1>(tm_w, tm_h, g, smem, p.stream)
                                 : launch_gemm<2, 0>(tm_w, tm_h, g, smem, p.stream))
                           : launch_gemm<1, 0>(tm_w, tm_h, g, smem, p.stream);

@@ -53,6 +53,11 @@ struct ProposePlan {
                         //               [N][B][cap_a]
   int32_t* tk_id;       //               top-k tokens given each previous row
   float* tk_val;        //               [N][B][cap_a][k], and their values
+  uint32_t* zbound;     //               [N][B][zbound_k] maxima of the tiles' lower bounds
+                        //               (unsigned order keys; tile t goes to t % zbound_k)
+  uint8_t* zwritten;    //               [N][B][Vhp / 128] whether the GEMM stored the
+                        //               tile's z (NULL: it stored every tile)
+  int zbound_k;         //               0: the GEMM stores every tile
   float* z;             // base logits: [N][Vhp][ldb] (slot, head row, block fastest), or
                         // [N][Vhp / 8][ldb][8] when z_octet (see z_octet_index)
   bool z_octet;
@@ -79,7 +84,8 @@ constexpr int kChainMaxCtas = 256;
 // Workspace carve-up shared by the size query and the launch.  [ctrl, zero_end) is
 // cleared at the start of every call.
 struct WorkspaceLayout {
-  size_t ctrl, bar, keys, zero_end, z, zmax, cand, zc, prev, conf, part_val, part_id, total;
+  size_t ctrl, bar, keys, zbound, zero_end, z, zmax, zwritten, cand, zc, prev, conf, part_val,
+      part_id, total;
   size_t Vhp, ldb, ldz;
 };
 WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool pruned);
@@ -98,6 +104,15 @@ struct PrunedLists {
   size_t cand_v, cand_z, cand_n, prev_v, prev_n, amax, tk_id, tk_val, total;
 };
 PrunedLists plan_pruned_lists(int B, int N, int k);
+
+// Rounding margins of the pruned chain's bounds (relative to the Markov bound, and
+// absolute), shared by the chain and the lm_head GEMM, which prunes with the same bounds.
+constexpr float kPrunedRelMargin = 1.0f / 1024;
+constexpr float kPrunedAbsMargin = 1e-4f;
+
+// Whether the lm_head GEMM runs with the prediction rows on M for these sizes (the form
+// that can leave out tiles of z that cannot matter, see logits_gemm_tc).
+bool logits_gemm_pm(int B, int N, bool z_octet, const float* lm_bias);
 cudaError_t launch_prepare_head(const void* w1, const void* w2, int V, int r, int Vh,
                                 void* prepared, cudaStream_t stream);
 cudaError_t launch_chain_pruned(const ProposePlan& p);

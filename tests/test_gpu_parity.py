@@ -235,3 +235,28 @@ def test_pm_tiles_reduced_vocab(form, sfa):
     g, o, rep = run_case(wl, form, chain="pruned")
     emit = set(make_head(wl)["emit_rows"].tolist())
     assert set(g["draft"].ravel().tolist()) <= emit
+
+
+# ------------------------------------------------------------------ z tiles left out by the
+# GEMM (pair tiles of 256 prediction rows, top-k over corrected logits)
+@pytest.mark.parametrize("weight_std", [0.05, 1.0])
+def test_pm_skip_markov_scale(weight_std):
+    # a small Markov term leaves most tiles out; a large one keeps most of them
+    run_case(_small(B=32, L_in=8, H=128, V=4096, r=32, top_k=4, weight_std=weight_std,
+                    seed=911), chain="pruned")
+
+
+def test_pm_skip_without_topk_outputs():
+    # no top-k asked: the bound is of rank 1
+    from gpu_cases import gpu_propose, oracle_run, compare
+    wl = _small(B=32, L_in=8, H=128, V=4096, r=32, top_k=4, seed=912)
+    hd, bt = make_head(wl), make_batch(wl)
+    g, _ = gpu_propose(wl, hd, bt, want_topk=False, chain="pruned")
+    rep = compare(wl, hd, bt, oracle_run(wl, hd, bt), g)
+    assert rep["failures"] == [], rep
+
+
+def test_pm_no_skip_for_base_logit_topk():
+    # top-k of the base logits: every tile is stored
+    run_case(_small(B=32, L_in=8, H=128, V=2048, r=32, top_k=6, topk_markov=False),
+             chain="pruned")
