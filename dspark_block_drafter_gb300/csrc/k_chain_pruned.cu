@@ -413,7 +413,9 @@ __device__ void scan_rows(const float* z, size_t b, size_t Vhp, size_t ldb, cons
 // that can be the argmax of slot i - 1 (bound of rank 1; slot 0: the anchor), z' exactly
 // for every pair in A(i - 1) x C(i), and from it, for each possible previous row, the
 // argmax and the top-k of slot i.  Also the slot's confidence.
-__global__ void __launch_bounds__(kThreads)
+// Four CTAs per SM (at most 64 registers a thread), so that the B x N CTAs of the
+// Qwen3-8B-shaped batch (512) run in one wave on 152 SMs.
+__global__ void __launch_bounds__(kThreads, 4)
 pruned_table(const TableArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
   const int T4 = (a.T + 3) & ~3;
@@ -437,6 +439,10 @@ pruned_table(const TableArgs a) {
   const float umax = __uint_as_float(*a.w1max) * (1.f + kRelMargin);
   const float* zm = a.zmax + ((size_t)i * a.B + b) * a.T;
   const float* zp = i > 0 ? a.zmax + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
+  // Tiles the GEMM left out of z had an upper bound below a lower bound of their slot's
+  // threshold, so they hold no candidate: their upper bounds are set to -inf here.
+  const uint8_t* wi = a.zw ? a.zw + ((size_t)i * a.B + b) * a.T : nullptr;
+  const uint8_t* wp = (a.zw && zp) ? a.zw + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
 
   if (tid == 0) {
     s_ntc = 0;
@@ -454,6 +460,7 @@ pruned_table(const TableArgs a) {
     const int stride = kThreads - 32;
     for (int t0 = tid; t0 < a.T; t0 += kBoundsUnroll * stride) {
       float c[kBoundsUnroll], z0[kBoundsUnroll], z1[kBoundsUnroll];
+      unsigned w0 = 0, w1 = 0;                       // bit u: tile t0 + u * stride stored
 #pragma unroll
       for (int u = 0; u < kBoundsUnroll; ++u) {
         const int t = t0 + u * stride;
@@ -461,6 +468,8 @@ pruned_table(const TableArgs a) {
         c[u] = in ? a.cnmax[t] : 0.f;
         z0[u] = in ? zm[t] : -INFINITY;
         z1[u] = (in && zp) ? zp[t] : -INFINITY;
+        w0 |= (unsigned)(!(in && wi) || wi[t] != 0) << u;
+        w1 |= (unsigned)(!(in && wp) || wp[t] != 0) << u;
       }
 #pragma unroll
       for (int u = 0; u < kBoundsUnroll; ++u) {
@@ -469,9 +478,9 @@ pruned_table(const TableArgs a) {
         const float d = umax * c[u] * (1.f + kRelMargin) + kAbsMargin;
         mlb = fmaxf(mlb, z0[u] - d);
         mzm = fmaxf(mzm, z0[u]);
-        s_ub[t] = z0[u] + d;
+        s_ub[t] = (w0 >> u) & 1 ? z0[u] + d : -INFINITY;
         if (zp) {
-          s_up[t] = z1[u] + d;
+          s_up[t] = (w1 >> u) & 1 ? z1[u] + d : -INFINITY;
           mp = fmaxf(mp, z1[u] - d);
         }
       }
@@ -512,14 +521,10 @@ pruned_table(const TableArgs a) {
   if (a.zrank) theta_z = block_kth_of_maxima(mzm, a.kk, s_top, &s_theta) - kAbsMargin;
   float theta1 = s_red[0];
   for (int w = 1; w < kWarps; ++w) theta1 = fmaxf(theta1, s_red[w]);
-  // ---- candidate tiles of both lists.  A tile the GEMM left out of z had an upper bound
-  //      below a lower bound of this rank's threshold, so it holds no candidate either.
-  const uint8_t* wi = a.zw ? a.zw + ((size_t)i * a.B + b) * a.T : nullptr;
-  const uint8_t* wp = (a.zw && zp) ? a.zw + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
+  // ---- candidate tiles of both lists
   for (int t = tid; t < a.T; t += kThreads) {
-    if ((s_ub[t] >= theta_x || (a.zrank && zm[t] >= theta_z)) && (!wi || wi[t]))
-      s_tc[atomicAdd(&s_ntc, 1)] = t;
-    if (zp && s_up[t] >= theta1 && (!wp || wp[t])) s_ta[atomicAdd(&s_nta, 1)] = t;
+    if (s_ub[t] >= theta_x || (a.zrank && zm[t] >= theta_z)) s_tc[atomicAdd(&s_ntc, 1)] = t;
+    if (zp && s_up[t] >= theta1) s_ta[atomicAdd(&s_nta, 1)] = t;
   }
   __syncthreads();
   // ---- their rows

@@ -260,3 +260,17 @@ def test_pm_no_skip_for_base_logit_topk():
     # top-k of the base logits: every tile is stored
     run_case(_small(B=32, L_in=8, H=128, V=2048, r=32, top_k=6, topk_markov=False),
              chain="pruned")
+
+
+def test_pm_skip_with_every_row_fallback():
+    # Zero hidden states and a +4 bias on the first 640 of 4096 rows: every hot row ties on
+    # z, so the candidate lists overflow and each slot is evaluated over every row, while
+    # the 27 cold tiles sit far below the threshold and are left out of z.
+    wl = _small(B=32, L_in=8, H=128, V=4096, r=32, top_k=4, seed=913)
+    hd, bt = make_head(wl), make_batch(wl)
+    bt["hidden"] = np.zeros_like(bt["hidden"])
+    bias = np.zeros(wl.V, np.float32)
+    bias[:640] = 4.0
+    hd["lm_bias"] = bias
+    g, o, rep = run_case(wl, hd=hd, bt=bt, chain="pruned")
+    assert (g["draft"] < 640).all()
