@@ -57,7 +57,7 @@ struct GemmArgs {
   float* zmax;     // [N][B][zm_tiles] per-tile maxima of z, or NULL
   // Tiles of z that cannot matter (PM = 1 only; zbound_k = 0 stores every tile): see the
   // PM = 1 epilogue.
-  uint32_t* zbound;        // [N][B][zbound_k] maxima of tile lower bounds (order keys)
+  uint32_t* zbound;        // [N][zbound_k][B] maxima of tile lower bounds (order keys)
   uint8_t* zwritten;       // [N][B][zm_tiles]
   const float* cnmax;      // [zm_tiles] largest markov_w2 column norm of each tile
   const unsigned* w1max;   // largest markov_w1 row norm (float bits)
@@ -353,18 +353,21 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       ptx::tc_fence_after();
       // z_octet_index(i, v, b) = zrow + (v / 8) * oct_step + v % 8
       float* zrow = live ? g.z + ((size_t)i * (g.Vhp / 8) * g.ldb + (size_t)b) * 8 : g.z;
-      uint32_t* bound = (K > 0 && live) ? g.zbound + ((size_t)i * g.B + b) * K : nullptr;
+      // this row's maxima sit B apart, so that a warp's consecutive blocks read and
+      // update them in whole sectors
+      uint32_t* bound = (K > 0 && live) ? g.zbound + (size_t)i * K * g.B + b : nullptr;
+      // the current threshold, read once for both 128-row tiles (first, so that its
+      // latency hides behind the TMEM loads; any value read is a valid bound, they only
+      // grow)
+      uint32_t th = 0;
+      if (bound && vt * 2 * kBlockV < g.Vh) {
+        th = 0xFFFFFFFFu;
+        for (int j = 0; j < K; ++j) th = min(th, __ldcg(bound + (size_t)j * g.B));
+      }
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         const int rt = vt * 2 + half;               // the 128-row tile of these columns
         const bool tile_in = rt * kBlockV < g.Vh;
-        // the current threshold (read first, so that its latency hides behind the TMEM
-        // loads; any value read is a valid bound, they only grow)
-        uint32_t th = 0;
-        if (bound && tile_in) {
-          th = 0xFFFFFFFFu;
-          for (int j = 0; j < K; ++j) th = min(th, __ldcg(bound + j));
-        }
         // this tile's maximum, with the bias
         float m = -INFINITY;
 #pragma unroll 1
@@ -396,7 +399,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
           if (bound) {
             const float d = umax * g.cnmax[rt] * (1.f + kPrunedRelMargin) + kPrunedAbsMargin;
             store = ukey(m + d) >= th;
-            atomicMax(bound + rt % K, ukey(m - d));
+            atomicMax(bound + (size_t)(rt % K) * g.B, ukey(m - d));
           }
           if (g.zmax) g.zmax[((size_t)i * g.B + b) * g.zm_tiles + rt] = m;
           if (g.zwritten) g.zwritten[((size_t)i * g.B + b) * g.zm_tiles + rt] = store ? 1 : 0;
