@@ -40,7 +40,10 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
   w.keys = take(sizeof(unsigned long long) * (size_t)N * B);
   // the maxima of the lower bounds with which the GEMM leaves tiles of z out start from
   // zero (below every key) in every pass
-  if (pruned) w.zbound = take(sizeof(uint32_t) * (size_t)N * B * k);
+  if (pruned) {
+    w.zbound = take(sizeof(uint32_t) * (size_t)N * B * k);
+    w.walk_done = take(sizeof(int32_t) * (size_t)B);
+  }
   w.zero_end = off;
   w.z = take(sizeof(float) * (size_t)N * w.Vhp * w.ldb);
   if (pruned) {
@@ -199,6 +202,7 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
     p.tk_id = (int32_t*)(lists + ll.tk_id);
     p.tk_val = (float*)(lists + ll.tk_val);
     p.z_octet = true;           // the candidate scans read one block's rows of z
+    p.walk_done = (int32_t*)(ws + wl.walk_done);
     // Tiles of z that provably cannot hold a slot's top k are left out by the GEMM when
     // it runs with the prediction rows on M and the top-k ranks corrected logits.
     const bool want_topk = out->topk_ids || out->topk_vals;
@@ -256,7 +260,7 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK || !out) return -1;
   if (cfg->dtype == DSPARK_F32) return 1 + 1 + 2 * N;   // confidence, GEMM, 2 per slot
-  if (use_pruned(cfg, head) && !out->logits) return 3;  // GEMM, tables, walk
+  if (use_pruned(cfg, head) && !out->logits) return 2;  // GEMM; tables with the walk
   const bool topk = out->topk_ids || out->topk_vals;
   return 1 /* confidence */ + 1 /* GEMM */ + (cfg->B + 31) / 32 /* chain, 32 blocks each */ +
          (topk ? 1 : 0);

@@ -340,6 +340,7 @@ struct TableArgs {
   int32_t* tk_id;            // [N][B][kCapA][k]: top-k tokens given each prev row
   float* tk_val;             // [N][B][kCapA][k]
   uint32_t* err;
+  int* walk_done;            // [B], zero at the start of the pass: table CTAs done per block
   int B, N, V, Vh, T, r, k, kk, zrank, want_topk, L_in, ifp, H;
 };
 
@@ -405,259 +406,6 @@ __device__ void scan_rows(const float* z, size_t b, size_t Vhp, size_t ldb, cons
           }
         }
       }
-    }
-  }
-}
-
-// One CTA per (block, slot i): candidate rows C(i) (bound of rank kk), the rows A(i - 1)
-// that can be the argmax of slot i - 1 (bound of rank 1; slot 0: the anchor), z' exactly
-// for every pair in A(i - 1) x C(i), and from it, for each possible previous row, the
-// argmax and the top-k of slot i.  Also the slot's confidence.
-// Four CTAs per SM (at most 64 registers a thread), so that the B x N CTAs of the
-// Qwen3-8B-shaped batch (512) run in one wave on 152 SMs.
-__global__ void __launch_bounds__(kThreads, 4)
-pruned_table(const TableArgs a) {
-  extern __shared__ __align__(16) uint8_t dsm[];
-  const int T4 = (a.T + 3) & ~3;
-  float* s_ub = (float*)dsm;                                   // [T4] upper bounds, slot i
-  float* s_up = s_ub + T4;                                     // [T4] upper bounds, slot i-1
-  int* s_tc = (int*)(s_up + T4);                               // [T4] tiles of C(i)
-  int* s_ta = s_tc + T4;                                       // [T4] tiles of A(i-1)
-  int32_t* s_cv = (int32_t*)(s_ta + T4);                       // [kCap]
-  float* s_cz = (float*)(s_cv + kCap);                         // [kCap]
-  float* s_x = s_cz + kCap;                                    // [kCapA][kTabC]
-  __nv_bfloat16* s_w1 = (__nv_bfloat16*)(s_x + kCapA * kTabC); // [kCapA][r]
-  __nv_bfloat16* s_w2 = s_w1 + (size_t)kCapA * a.r;            // [kRowsChunk][r]
-  __shared__ float s_top[kWarps * 32];
-  __shared__ float s_theta, s_red[kWarps];
-  __shared__ int s_ntc, s_nta, s_nc, s_na;
-  __shared__ int32_t s_av[kCapA];
-  const int b = blockIdx.x, i = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  pdl_signal();
-  pdl_wait();                                        // z and zmax of the lm_head GEMM
-  const float umax = __uint_as_float(*a.w1max) * (1.f + kRelMargin);
-  const float* zm = a.zmax + ((size_t)i * a.B + b) * a.T;
-  const float* zp = i > 0 ? a.zmax + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
-  // Tiles the GEMM left out of z had an upper bound below a lower bound of their slot's
-  // threshold, so they hold no candidate: their upper bounds are set to -inf here.
-  const uint8_t* wi = a.zw ? a.zw + ((size_t)i * a.B + b) * a.T : nullptr;
-  const uint8_t* wp = (a.zw && zp) ? a.zw + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
-
-  if (tid == 0) {
-    s_ntc = 0;
-    s_nta = 0;
-    s_nc = 0;
-    s_na = 0;
-  }
-  // ---- bounds of slot i and slot i - 1 (all warps but the last), confidence (the last);
-  //      each thread keeps the maxima of the lower bounds / tile maxima it saw
-  float mp = -INFINITY;                              // slot i-1's lower bounds
-  float mlb = -INFINITY, mzm = -INFINITY;            // slot i's lower bounds, tile maxima
-  if (warp < kWarps - 1) {
-    // loads of up to kBoundsUnroll tiles per thread are issued before any is used
-    constexpr int kBoundsUnroll = 8;
-    const int stride = kThreads - 32;
-    for (int t0 = tid; t0 < a.T; t0 += kBoundsUnroll * stride) {
-      float c[kBoundsUnroll], z0[kBoundsUnroll], z1[kBoundsUnroll];
-      unsigned w0 = 0, w1 = 0;                       // bit u: tile t0 + u * stride stored
-#pragma unroll
-      for (int u = 0; u < kBoundsUnroll; ++u) {
-        const int t = t0 + u * stride;
-        const bool in = t < a.T;
-        c[u] = in ? a.cnmax[t] : 0.f;
-        z0[u] = in ? zm[t] : -INFINITY;
-        z1[u] = (in && zp) ? zp[t] : -INFINITY;
-        w0 |= (unsigned)(!(in && wi) || wi[t] != 0) << u;
-        w1 |= (unsigned)(!(in && wp) || wp[t] != 0) << u;
-      }
-#pragma unroll
-      for (int u = 0; u < kBoundsUnroll; ++u) {
-        const int t = t0 + u * stride;
-        if (t >= a.T) break;
-        const float d = umax * c[u] * (1.f + kRelMargin) + kAbsMargin;
-        mlb = fmaxf(mlb, z0[u] - d);
-        mzm = fmaxf(mzm, z0[u]);
-        s_ub[t] = (w0 >> u) & 1 ? z0[u] + d : -INFINITY;
-        if (zp) {
-          s_up[t] = (w1 >> u) & 1 ? z1[u] + d : -INFINITY;
-          mp = fmaxf(mp, z1[u] - d);
-        }
-      }
-    }
-  } else if (a.w_conf) {
-    // sigmoid(h . w_conf + b_conf) (llama.cpp commit 6fed9f6, "spec: add confidence-based
-    // draft pruning for DSpark")
-    const __nv_bfloat16* h = a.hidden + ((size_t)b * a.L_in + a.ifp + i) * a.H;
-    float acc = 0.f;
-    int c0 = 0;
-    if ((a.H % 8) == 0 && ((uintptr_t)h % 16) == 0 && ((uintptr_t)a.w_conf % 16) == 0) {
-      const uint4* h4 = reinterpret_cast<const uint4*>(h);
-      const uint4* w4 = reinterpret_cast<const uint4*>(a.w_conf);
-      const int n4 = a.H / 8;
-#pragma unroll 4
-      for (int q = lane; q < n4; q += 32) {
-        const uint4 hv = h4[q], wv = w4[q];
-        const __nv_bfloat16* he = reinterpret_cast<const __nv_bfloat16*>(&hv);
-        const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&wv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc = fmaf(to_f32(he[e]), to_f32(we[e]), acc);
-      }
-      c0 = a.H;
-    }
-    for (int c = c0 + lane; c < a.H; c += 32) acc = fmaf(to_f32(h[c]), to_f32(a.w_conf[c]), acc);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    if (lane == 0) a.conf[(size_t)b * a.N + i] = 1.f / (1.f + expf(-(acc + a.b_conf)));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xFFFFFFFFu, mp, o));
-  if (lane == 0) s_red[warp] = mp;
-  __syncthreads();
-  // ---- thresholds: rank kk of slot i's lower bounds (rank 1 when the top-k ranks base
-  //      logits, which then take rank kk of the tile maxima); rank 1 of slot i-1's
-  const float theta_x = block_kth_of_maxima(mlb, a.zrank ? 1 : a.kk, s_top, &s_theta);
-  float theta_z = INFINITY;
-  if (a.zrank) theta_z = block_kth_of_maxima(mzm, a.kk, s_top, &s_theta) - kAbsMargin;
-  float theta1 = s_red[0];
-  for (int w = 1; w < kWarps; ++w) theta1 = fmaxf(theta1, s_red[w]);
-  // ---- candidate tiles of both lists
-  for (int t = tid; t < a.T; t += kThreads) {
-    if (s_ub[t] >= theta_x || (a.zrank && zm[t] >= theta_z)) s_tc[atomicAdd(&s_ntc, 1)] = t;
-    if (zp && s_up[t] >= theta1) s_ta[atomicAdd(&s_nta, 1)] = t;
-  }
-  __syncthreads();
-  // ---- their rows
-  {
-    const RowScan lc{(size_t)i, s_tc, s_ntc, theta_x, theta_z, s_cv, s_cz, kCap, &s_nc};
-    const RowScan lp{zp ? (size_t)(i - 1) : 0, s_ta, zp ? s_nta : 0, theta1, INFINITY,
-                     s_av, nullptr, kCapA, &s_na};
-    scan_rows(a.z, b, a.Vhp, a.ldb, a.cnorm, umax, a.Vh, lc, lp);
-  }
-  if (!zp && tid == 0) {
-    int p = a.anchors[b];
-    if (p < 0 || p >= a.V) {
-      flag_error(a.err, kErrBadToken);
-      p = 0;
-    }
-    s_av[0] = p;                                     // slot 0: the anchor (a token)
-    s_na = 1;
-  }
-  __syncthreads();
-  // ---- the lists
-  const int nc = s_nc, na = s_na;
-  const size_t ib = (size_t)i * a.B + b;
-  for (int j = tid; j < min(nc, kCap); j += kThreads) {
-    a.cand_v[ib * kCap + j] = s_cv[j];
-    a.cand_z[ib * kCap + j] = s_cz[j];
-  }
-  for (int j = tid; j < min(na, kCapA); j += kThreads) a.prev_v[ib * kCapA + j] = s_av[j];
-  if (tid == 0) {
-    a.cand_n[ib] = nc;
-    a.prev_n[ib] = na;
-  }
-  if (nc < 1 || nc > kTabC || na < 1 || na > kCapA) return;   // evaluated on the fly later
-  // ---- z' = z + markov_w1[p] . w2[:, v] for every p in A(i - 1), v in C(i): eight lanes
-  //      per pair, the same summation order as the on-the-fly evaluation
-  const int chunks = a.r / 8;                        // r % 8 == 0 on this path
-  for (int c = tid; c < na * chunks; c += kThreads) {
-    const int p = c / chunks, q = c % chunks;
-    int tok = (i == 0 || !a.d2t) ? s_av[p] : a.d2t[s_av[p]];
-    if (tok < 0 || tok >= a.V) {
-      flag_error(a.err, kErrBadToken);
-      tok = 0;
-    }
-    cp_async16(s_w1 + (size_t)p * a.r + q * 8, a.w1 + (size_t)tok * a.r + q * 8);
-  }
-  for (int c0 = 0; c0 < nc; c0 += kRowsChunk) {
-    const int cnt = min(kRowsChunk, nc - c0);
-    for (int c = tid; c < cnt * chunks; c += kThreads) {
-      const int e = c / chunks, q = c % chunks;
-      cp_async16(s_w2 + (size_t)e * a.r + q * 8, a.w2t + (size_t)s_cv[c0 + e] * a.r + q * 8);
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    const int pairs = na * cnt, sub = tid % 8;
-    for (int q0 = 0; q0 < pairs; q0 += kThreads / 8) {
-      const int pr = q0 + tid / 8;
-      float s0 = 0.f, s1 = 0.f;
-      if (pr < pairs) {
-        const __nv_bfloat16* u = s_w1 + (size_t)(pr / cnt) * a.r;
-        const __nv_bfloat16* w = s_w2 + (size_t)(pr % cnt) * a.r;
-        for (int ch = sub; ch < chunks; ch += 8) {
-          const uint4 ru = *reinterpret_cast<const uint4*>(u + ch * 8);
-          const uint4 rw = *reinterpret_cast<const uint4*>(w + ch * 8);
-          const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&ru);
-          const __nv_bfloat162* pw = reinterpret_cast<const __nv_bfloat162*>(&rw);
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float2 fu = __bfloat1622float2(pu[h]), fw = __bfloat1622float2(pw[h]);
-            s0 = fmaf(fu.x, fw.x, s0);
-            s1 = fmaf(fu.y, fw.y, s1);
-          }
-        }
-      }
-      float s = s0 + s1;
-      s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
-      s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
-      s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
-      if (pr < pairs && sub == 0) {
-        const int e = pr % cnt;
-        s_x[(pr / cnt) * kTabC + c0 + e] = s_cz[c0 + e] + s;
-      }
-    }
-    __syncthreads();
-  }
-  // ---- for each possible previous row: the argmax (the next previous row) and the top-k
-  for (int p = warp; p < na; p += kWarps) {
-    const float* x = s_x + p * kTabC;
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    for (int c = lane; c < nc; c += 32)
-      if (better(x[c], s_cv[c], bv, bi)) {
-        bv = x[c];
-        bi = s_cv[c];
-      }
-    warp_best(bv, bi);
-    if (lane == 0) a.amax[ib * kCapA + p] = (bi >= 0 && bi < a.Vh) ? bi : -1;
-    if (!a.want_topk) continue;
-    const float* rk = a.zrank ? s_cz : x;
-    if (nc <= 32) {
-      // one entry per lane: sort the warp, lane q holds the q-th
-      float v = lane < nc ? rk[lane] : -INFINITY;
-      int id = lane < nc ? s_cv[lane] : 0x7FFFFFFF;
-      warp_sort(v, id);
-      if (lane < a.k) {
-        const size_t o = (ib * kCapA + p) * a.k + lane;
-        const int row = (id >= 0 && id < a.Vh) ? id : 0;
-        a.tk_id[o] = a.d2t ? a.d2t[row] : row;
-        a.tk_val[o] = v;
-      }
-      continue;
-    }
-    float pv = 0.f;
-    int pid = 0;
-    for (int q = 0; q < a.k; ++q) {
-      bv = -INFINITY;
-      bi = 0x7FFFFFFF;
-      for (int c = lane; c < nc; c += 32) {
-        const float val = rk[c];
-        const int id = s_cv[c];
-        if (q > 0 && !better(pv, pid, val, id)) continue;
-        if (better(val, id, bv, bi)) {
-          bv = val;
-          bi = id;
-        }
-      }
-      warp_best(bv, bi);
-      if (lane == 0) {
-        const size_t o = (ib * kCapA + p) * a.k + q;
-        const int row = (bi >= 0 && bi < a.Vh) ? bi : 0;
-        a.tk_id[o] = a.d2t ? a.d2t[row] : row;
-        a.tk_val[o] = bv;
-      }
-      pv = bv;
-      pid = bi;
     }
   }
 }
@@ -728,27 +476,39 @@ __device__ void evaluate_list(Cand* buf, int n, const float* s_u, const __nv_bfl
   }
 }
 
-// One CTA per block walks its N slots.  A tabulated slot is a lookup: the previous row's
-// index in A(i - 1), then the argmax stored for it; warp 0 walks those alone.  A slot
-// without a table (a list that overflowed, too many previous rows, a previous row not
-// found) is evaluated on the fly by the whole CTA, over every row if need be.
-__global__ void __launch_bounds__(kThreads)
-pruned_select(const SelectArgs a) {
-  extern __shared__ __align__(16) uint8_t dsm[];
+// Shared memory of the walk of one block, carved from the CTA's dynamic shared memory.
+// (All of it overlays the tables' shared memory, which the walk no longer needs, so that
+// the kernel's static shared memory stays small: four CTAs must fit an SM.)
+__host__ __device__ inline size_t walk_smem_bytes(int r, int N) {
+  return sizeof(float) * ((r + 3) & ~3) + sizeof(Cand) * (kCand + kMaxKeep) +
+         sizeof(int) * 4 * (size_t)N + sizeof(int32_t) * 2 * (size_t)N * kCapA +
+         sizeof(float) * (size_t)N + sizeof(float) * kWarps + sizeof(int) * kWarps +
+         sizeof(int) * (3 + kMaxKeep);
+}
+
+// The walk of block b over its N slots, by the whole CTA (the last of the block's table
+// CTAs to finish).  A tabulated slot is a lookup: the previous row's index in A(i - 1),
+// then the argmax stored for it; warp 0 walks those alone.  A slot without a table (a
+// list that overflowed, too many previous rows, a previous row not found) is evaluated
+// on the fly by the whole CTA, over every row if need be.
+__device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
   float* s_u = (float*)dsm;                                    // [r]
   Cand* buf = (Cand*)(s_u + ((a.r + 3) & ~3));                 // [kCand]
-  __shared__ int s_nc[kMaxSlots], s_na[kMaxSlots], s_pi[kMaxSlots], s_row[kMaxSlots];
-  __shared__ int32_t s_av[kMaxSlots][kCapA], s_am[kMaxSlots][kCapA];
-  __shared__ float s_conf[kMaxSlots];
-  __shared__ float s_red_v[kWarps];
-  __shared__ int s_red_i[kWarps];
-  __shared__ int s_nfull, s_prev, s_stop;
-  __shared__ int s_keep[kMaxKeep];
-  __shared__ Cand s_stage[kMaxKeep];
-  const int b = blockIdx.x;
+  Cand* s_stage = buf + kCand;                                 // [kMaxKeep]
+  int* s_nc = (int*)(s_stage + kMaxKeep);                      // [N] each
+  int* s_na = s_nc + a.N;
+  int* s_pi = s_na + a.N;
+  int* s_row = s_pi + a.N;
+  int32_t (*s_av)[kCapA] = reinterpret_cast<int32_t (*)[kCapA]>(s_row + a.N);   // [N][kCapA]
+  int32_t (*s_am)[kCapA] = s_av + a.N;
+  float* s_conf = reinterpret_cast<float*>(s_am + a.N);        // [N]
+  float* s_red_v = s_conf + a.N;                               // [kWarps]
+  int* s_red_i = reinterpret_cast<int*>(s_red_v + kWarps);     // [kWarps]
+  int* s_keep = s_red_i + kWarps;                              // [kMaxKeep]
+  int& s_nfull = s_keep[kMaxKeep];
+  int& s_prev = s_keep[kMaxKeep + 1];
+  int& s_stop = s_keep[kMaxKeep + 2];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  pdl_signal();
-  pdl_wait();                                        // the tables
 
   // ---- counts, then the previous rows and argmax rows of every tabulated slot
   for (int i = tid; i < a.N; i += kThreads) {
@@ -940,6 +700,273 @@ pruned_select(const SelectArgs a) {
   }
 }
 
+// One CTA per (block, slot i): candidate rows C(i) (bound of rank kk), the rows A(i - 1)
+// that can be the argmax of slot i - 1 (bound of rank 1; slot 0: the anchor), z' exactly
+// for every pair in A(i - 1) x C(i), and from it, for each possible previous row, the
+// argmax and the top-k of slot i.  Also the slot's confidence.
+// Four CTAs per SM (at most 64 registers a thread), so that the B x N CTAs of the
+// Qwen3-8B-shaped batch (512) run in one wave on 152 SMs.
+__global__ void __launch_bounds__(kThreads, 4)
+pruned_table(const TableArgs a, const SelectArgs sel) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  const int T4 = (a.T + 3) & ~3;
+  float* s_ub = (float*)dsm;                                   // [T4] upper bounds, slot i
+  float* s_up = s_ub + T4;                                     // [T4] upper bounds, slot i-1
+  int* s_tc = (int*)(s_up + T4);                               // [T4] tiles of C(i)
+  int* s_ta = s_tc + T4;                                       // [T4] tiles of A(i-1)
+  int32_t* s_cv = (int32_t*)(s_ta + T4);                       // [kCap]
+  float* s_cz = (float*)(s_cv + kCap);                         // [kCap]
+  float* s_x = s_cz + kCap;                                    // [kCapA][kTabC]
+  __nv_bfloat16* s_w1 = (__nv_bfloat16*)(s_x + kCapA * kTabC); // [kCapA][r]
+  __nv_bfloat16* s_w2 = s_w1 + (size_t)kCapA * a.r;            // [kRowsChunk][r]
+  __shared__ float s_top[kWarps * 32];
+  __shared__ float s_theta, s_red[kWarps];
+  __shared__ int s_ntc, s_nta, s_nc, s_na;
+  __shared__ int32_t s_av[kCapA];
+  const int b = blockIdx.x, i = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  pdl_signal();
+  pdl_wait();                                        // z and zmax of the lm_head GEMM
+  const float umax = __uint_as_float(*a.w1max) * (1.f + kRelMargin);
+  const float* zm = a.zmax + ((size_t)i * a.B + b) * a.T;
+  const float* zp = i > 0 ? a.zmax + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
+  // Tiles the GEMM left out of z had an upper bound below a lower bound of their slot's
+  // threshold, so they hold no candidate: their upper bounds are set to -inf here.
+  const uint8_t* wi = a.zw ? a.zw + ((size_t)i * a.B + b) * a.T : nullptr;
+  const uint8_t* wp = (a.zw && zp) ? a.zw + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
+
+  if (tid == 0) {
+    s_ntc = 0;
+    s_nta = 0;
+    s_nc = 0;
+    s_na = 0;
+  }
+  // ---- bounds of slot i and slot i - 1 (all warps but the last), confidence (the last);
+  //      each thread keeps the maxima of the lower bounds / tile maxima it saw
+  float mp = -INFINITY;                              // slot i-1's lower bounds
+  float mlb = -INFINITY, mzm = -INFINITY;            // slot i's lower bounds, tile maxima
+  if (warp < kWarps - 1) {
+    // loads of up to kBoundsUnroll tiles per thread are issued before any is used
+    constexpr int kBoundsUnroll = 8;
+    const int stride = kThreads - 32;
+    for (int t0 = tid; t0 < a.T; t0 += kBoundsUnroll * stride) {
+      float c[kBoundsUnroll], z0[kBoundsUnroll], z1[kBoundsUnroll];
+      unsigned w0 = 0, w1 = 0;                       // bit u: tile t0 + u * stride stored
+#pragma unroll
+      for (int u = 0; u < kBoundsUnroll; ++u) {
+        const int t = t0 + u * stride;
+        const bool in = t < a.T;
+        c[u] = in ? a.cnmax[t] : 0.f;
+        z0[u] = in ? zm[t] : -INFINITY;
+        z1[u] = (in && zp) ? zp[t] : -INFINITY;
+        w0 |= (unsigned)(!(in && wi) || wi[t] != 0) << u;
+        w1 |= (unsigned)(!(in && wp) || wp[t] != 0) << u;
+      }
+#pragma unroll
+      for (int u = 0; u < kBoundsUnroll; ++u) {
+        const int t = t0 + u * stride;
+        if (t >= a.T) break;
+        const float d = umax * c[u] * (1.f + kRelMargin) + kAbsMargin;
+        mlb = fmaxf(mlb, z0[u] - d);
+        mzm = fmaxf(mzm, z0[u]);
+        s_ub[t] = (w0 >> u) & 1 ? z0[u] + d : -INFINITY;
+        if (zp) {
+          s_up[t] = (w1 >> u) & 1 ? z1[u] + d : -INFINITY;
+          mp = fmaxf(mp, z1[u] - d);
+        }
+      }
+    }
+  } else if (a.w_conf) {
+    // sigmoid(h . w_conf + b_conf) (llama.cpp commit 6fed9f6, "spec: add confidence-based
+    // draft pruning for DSpark")
+    const __nv_bfloat16* h = a.hidden + ((size_t)b * a.L_in + a.ifp + i) * a.H;
+    float acc = 0.f;
+    int c0 = 0;
+    if ((a.H % 8) == 0 && ((uintptr_t)h % 16) == 0 && ((uintptr_t)a.w_conf % 16) == 0) {
+      const uint4* h4 = reinterpret_cast<const uint4*>(h);
+      const uint4* w4 = reinterpret_cast<const uint4*>(a.w_conf);
+      const int n4 = a.H / 8;
+#pragma unroll 4
+      for (int q = lane; q < n4; q += 32) {
+        const uint4 hv = h4[q], wv = w4[q];
+        const __nv_bfloat16* he = reinterpret_cast<const __nv_bfloat16*>(&hv);
+        const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&wv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(to_f32(he[e]), to_f32(we[e]), acc);
+      }
+      c0 = a.H;
+    }
+    for (int c = c0 + lane; c < a.H; c += 32) acc = fmaf(to_f32(h[c]), to_f32(a.w_conf[c]), acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (lane == 0) a.conf[(size_t)b * a.N + i] = 1.f / (1.f + expf(-(acc + a.b_conf)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xFFFFFFFFu, mp, o));
+  if (lane == 0) s_red[warp] = mp;
+  __syncthreads();
+  // ---- thresholds: rank kk of slot i's lower bounds (rank 1 when the top-k ranks base
+  //      logits, which then take rank kk of the tile maxima); rank 1 of slot i-1's
+  const float theta_x = block_kth_of_maxima(mlb, a.zrank ? 1 : a.kk, s_top, &s_theta);
+  float theta_z = INFINITY;
+  if (a.zrank) theta_z = block_kth_of_maxima(mzm, a.kk, s_top, &s_theta) - kAbsMargin;
+  float theta1 = s_red[0];
+  for (int w = 1; w < kWarps; ++w) theta1 = fmaxf(theta1, s_red[w]);
+  // ---- candidate tiles of both lists
+  for (int t = tid; t < a.T; t += kThreads) {
+    if (s_ub[t] >= theta_x || (a.zrank && zm[t] >= theta_z)) s_tc[atomicAdd(&s_ntc, 1)] = t;
+    if (zp && s_up[t] >= theta1) s_ta[atomicAdd(&s_nta, 1)] = t;
+  }
+  __syncthreads();
+  // ---- their rows
+  {
+    const RowScan lc{(size_t)i, s_tc, s_ntc, theta_x, theta_z, s_cv, s_cz, kCap, &s_nc};
+    const RowScan lp{zp ? (size_t)(i - 1) : 0, s_ta, zp ? s_nta : 0, theta1, INFINITY,
+                     s_av, nullptr, kCapA, &s_na};
+    scan_rows(a.z, b, a.Vhp, a.ldb, a.cnorm, umax, a.Vh, lc, lp);
+  }
+  if (!zp && tid == 0) {
+    int p = a.anchors[b];
+    if (p < 0 || p >= a.V) {
+      flag_error(a.err, kErrBadToken);
+      p = 0;
+    }
+    s_av[0] = p;                                     // slot 0: the anchor (a token)
+    s_na = 1;
+  }
+  __syncthreads();
+  // ---- the lists
+  const int nc = s_nc, na = s_na;
+  const size_t ib = (size_t)i * a.B + b;
+  for (int j = tid; j < min(nc, kCap); j += kThreads) {
+    a.cand_v[ib * kCap + j] = s_cv[j];
+    a.cand_z[ib * kCap + j] = s_cz[j];
+  }
+  for (int j = tid; j < min(na, kCapA); j += kThreads) a.prev_v[ib * kCapA + j] = s_av[j];
+  if (tid == 0) {
+    a.cand_n[ib] = nc;
+    a.prev_n[ib] = na;
+  }
+  // (a slot without a table is evaluated on the fly by the walk)
+  if (nc >= 1 && nc <= kTabC && na >= 1 && na <= kCapA) {
+    // ---- z' = z + markov_w1[p] . w2[:, v] for every p in A(i - 1), v in C(i): eight lanes
+    //      per pair, the same summation order as the on-the-fly evaluation
+    const int chunks = a.r / 8;                        // r % 8 == 0 on this path
+    for (int c = tid; c < na * chunks; c += kThreads) {
+      const int p = c / chunks, q = c % chunks;
+      int tok = (i == 0 || !a.d2t) ? s_av[p] : a.d2t[s_av[p]];
+      if (tok < 0 || tok >= a.V) {
+        flag_error(a.err, kErrBadToken);
+        tok = 0;
+      }
+      cp_async16(s_w1 + (size_t)p * a.r + q * 8, a.w1 + (size_t)tok * a.r + q * 8);
+    }
+    for (int c0 = 0; c0 < nc; c0 += kRowsChunk) {
+      const int cnt = min(kRowsChunk, nc - c0);
+      for (int c = tid; c < cnt * chunks; c += kThreads) {
+        const int e = c / chunks, q = c % chunks;
+        cp_async16(s_w2 + (size_t)e * a.r + q * 8, a.w2t + (size_t)s_cv[c0 + e] * a.r + q * 8);
+      }
+      cp_async_wait_all();
+      __syncthreads();
+      const int pairs = na * cnt, sub = tid % 8;
+      for (int q0 = 0; q0 < pairs; q0 += kThreads / 8) {
+        const int pr = q0 + tid / 8;
+        float s0 = 0.f, s1 = 0.f;
+        if (pr < pairs) {
+          const __nv_bfloat16* u = s_w1 + (size_t)(pr / cnt) * a.r;
+          const __nv_bfloat16* w = s_w2 + (size_t)(pr % cnt) * a.r;
+          for (int ch = sub; ch < chunks; ch += 8) {
+            const uint4 ru = *reinterpret_cast<const uint4*>(u + ch * 8);
+            const uint4 rw = *reinterpret_cast<const uint4*>(w + ch * 8);
+            const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&ru);
+            const __nv_bfloat162* pw = reinterpret_cast<const __nv_bfloat162*>(&rw);
+  #pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float2 fu = __bfloat1622float2(pu[h]), fw = __bfloat1622float2(pw[h]);
+              s0 = fmaf(fu.x, fw.x, s0);
+              s1 = fmaf(fu.y, fw.y, s1);
+            }
+          }
+        }
+        float s = s0 + s1;
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, 4);
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+        if (pr < pairs && sub == 0) {
+          const int e = pr % cnt;
+          s_x[(pr / cnt) * kTabC + c0 + e] = s_cz[c0 + e] + s;
+        }
+      }
+      __syncthreads();
+    }
+    // ---- for each possible previous row: the argmax (the next previous row) and the top-k
+    for (int p = warp; p < na; p += kWarps) {
+      const float* x = s_x + p * kTabC;
+      float bv = -INFINITY;
+      int bi = 0x7FFFFFFF;
+      for (int c = lane; c < nc; c += 32)
+        if (better(x[c], s_cv[c], bv, bi)) {
+          bv = x[c];
+          bi = s_cv[c];
+        }
+      warp_best(bv, bi);
+      if (lane == 0) a.amax[ib * kCapA + p] = (bi >= 0 && bi < a.Vh) ? bi : -1;
+      if (!a.want_topk) continue;
+      const float* rk = a.zrank ? s_cz : x;
+      if (nc <= 32) {
+        // one entry per lane: sort the warp, lane q holds the q-th
+        float v = lane < nc ? rk[lane] : -INFINITY;
+        int id = lane < nc ? s_cv[lane] : 0x7FFFFFFF;
+        warp_sort(v, id);
+        if (lane < a.k) {
+          const size_t o = (ib * kCapA + p) * a.k + lane;
+          const int row = (id >= 0 && id < a.Vh) ? id : 0;
+          a.tk_id[o] = a.d2t ? a.d2t[row] : row;
+          a.tk_val[o] = v;
+        }
+        continue;
+      }
+      float pv = 0.f;
+      int pid = 0;
+      for (int q = 0; q < a.k; ++q) {
+        bv = -INFINITY;
+        bi = 0x7FFFFFFF;
+        for (int c = lane; c < nc; c += 32) {
+          const float val = rk[c];
+          const int id = s_cv[c];
+          if (q > 0 && !better(pv, pid, val, id)) continue;
+          if (better(val, id, bv, bi)) {
+            bv = val;
+            bi = id;
+          }
+        }
+        warp_best(bv, bi);
+        if (lane == 0) {
+          const size_t o = (ib * kCapA + p) * a.k + q;
+          const int row = (bi >= 0 && bi < a.Vh) ? bi : 0;
+          a.tk_id[o] = a.d2t ? a.d2t[row] : row;
+          a.tk_val[o] = bv;
+        }
+        pv = bv;
+        pid = bi;
+      }
+    }
+  }
+  // ---- the last of the block's N CTAs to get here walks the block (the others' lists
+  //      and tables are in global memory by then)
+  __shared__ int s_last;
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.walk_done + b, 1) == a.N - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  walk_block(sel, b, dsm);
+}
+
 }  // namespace
 
 PreparedLayout plan_prepared(int Vh, int r) {
@@ -1004,57 +1031,48 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   const bool want_topk = p.topk_ids || p.topk_vals;
   const int kk = want_topk ? p.k : 1;
   const int zrank = (want_topk && !p.topk_markov) ? 1 : 0;
-  if (!p.z_octet || p.N > kMaxSlots || p.r % 8 != 0) return cudaErrorInvalidValue;
-  cudaError_t e;
-  {
-    TableArgs t{};
-    t.z = p.z;
-    t.zmax = p.zmax;
-    t.zw = p.zwritten;
-    t.Vhp = p.Vhp;
-    t.ldb = p.ldb;
-    t.cnorm = p.cnorm;
-    t.cnmax = p.cnmax;
-    t.w1max = p.w1max;
-    t.w1 = (const __nv_bfloat16*)p.w1;
-    t.w2t = p.w2t;
-    t.anchors = p.anchors;
-    t.d2t = p.d2t;
-    t.hidden = (const __nv_bfloat16*)p.hidden;
-    t.w_conf = (const __nv_bfloat16*)p.w_conf;
-    t.b_conf = p.b_conf;
-    t.conf = p.conf ? p.conf : p.conf_ws;
-    t.cand_v = p.cand_v;
-    t.cand_z = p.cand_z;
-    t.cand_n = p.cand_n;
-    t.prev_v = p.prev_v;
-    t.prev_n = p.prev_n;
-    t.amax = p.amax;
-    t.tk_id = p.tk_id;
-    t.tk_val = p.tk_val;
-    t.err = p.ctrl;
-    t.B = p.B;
-    t.N = p.N;
-    t.V = p.V;
-    t.Vh = p.Vh;
-    t.T = T;
-    t.r = p.r;
-    t.k = p.k;
-    t.kk = kk;
-    t.zrank = zrank;
-    t.want_topk = want_topk ? 1 : 0;
-    t.L_in = p.L_in;
-    t.ifp = p.ifp;
-    t.H = p.H;
-    const size_t T4 = (size_t)((T + 3) & ~3);
-    const size_t smem = sizeof(float) * 4 * T4 + (sizeof(int32_t) + sizeof(float)) * kCap +
-                        sizeof(float) * kCapA * kTabC +
-                        sizeof(__nv_bfloat16) * (size_t)(kCapA + kRowsChunk) * p.r;
-    e = cudaFuncSetAttribute(pruned_table, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(pruned_table, dim3(p.B, p.N), dim3(kThreads), smem, p.stream, t);
-    if (e != cudaSuccess) return e;
-  }
+  if (!p.z_octet || p.N > kMaxSlots || p.r % 8 != 0 || !p.walk_done)
+    return cudaErrorInvalidValue;
+  TableArgs t{};
+  t.z = p.z;
+  t.zmax = p.zmax;
+  t.zw = p.zwritten;
+  t.Vhp = p.Vhp;
+  t.ldb = p.ldb;
+  t.cnorm = p.cnorm;
+  t.cnmax = p.cnmax;
+  t.w1max = p.w1max;
+  t.w1 = (const __nv_bfloat16*)p.w1;
+  t.w2t = p.w2t;
+  t.anchors = p.anchors;
+  t.d2t = p.d2t;
+  t.hidden = (const __nv_bfloat16*)p.hidden;
+  t.w_conf = (const __nv_bfloat16*)p.w_conf;
+  t.b_conf = p.b_conf;
+  t.conf = p.conf ? p.conf : p.conf_ws;
+  t.cand_v = p.cand_v;
+  t.cand_z = p.cand_z;
+  t.cand_n = p.cand_n;
+  t.prev_v = p.prev_v;
+  t.prev_n = p.prev_n;
+  t.amax = p.amax;
+  t.tk_id = p.tk_id;
+  t.tk_val = p.tk_val;
+  t.err = p.ctrl;
+  t.walk_done = p.walk_done;
+  t.B = p.B;
+  t.N = p.N;
+  t.V = p.V;
+  t.Vh = p.Vh;
+  t.T = T;
+  t.r = p.r;
+  t.k = p.k;
+  t.kk = kk;
+  t.zrank = zrank;
+  t.want_topk = want_topk ? 1 : 0;
+  t.L_in = p.L_in;
+  t.ifp = p.ifp;
+  t.H = p.H;
   SelectArgs s{};
   s.z = p.z;
   s.zw = p.zwritten;
@@ -1089,10 +1107,16 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   s.kk = kk;
   s.zrank = zrank;
   s.want_topk = want_topk ? 1 : 0;
-  const size_t smem = sizeof(float) * ((p.r + 3) & ~3) + sizeof(Cand) * kCand;
-  e = cudaFuncSetAttribute(pruned_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the tables' shared memory, or the walk's when it needs more
+  const size_t T4 = (size_t)((T + 3) & ~3);
+  const size_t table_smem = sizeof(float) * 4 * T4 + (sizeof(int32_t) + sizeof(float)) * kCap +
+                            sizeof(float) * kCapA * kTabC +
+                            sizeof(__nv_bfloat16) * (size_t)(kCapA + kRowsChunk) * p.r;
+  const size_t smem = std::max(table_smem, walk_smem_bytes(p.r, p.N));
+  cudaError_t e =
+      cudaFuncSetAttribute(pruned_table, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_dependent(pruned_select, dim3(p.B), dim3(kThreads), smem, p.stream, s);
+  return launch_dependent(pruned_table, dim3(p.B, p.N), dim3(kThreads), smem, p.stream, t, s);
 }
 
 }  // namespace dspark

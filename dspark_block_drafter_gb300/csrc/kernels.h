@@ -58,6 +58,7 @@ struct ProposePlan {
   uint8_t* zwritten;    //               [N][B][Vhp / 128] whether the GEMM stored the
                         //               tile's z (NULL: it stored every tile)
   int zbound_k;         //               0: the GEMM stores every tile
+  int32_t* walk_done;   //               [B] table CTAs finished per block (zeroed per pass)
   float* z;             // base logits: [N][Vhp][ldb] (slot, head row, block fastest), or
                         // [N][Vhp / 8][ldb][8] when z_octet (see z_octet_index)
   bool z_octet;
@@ -84,7 +85,7 @@ constexpr int kChainMaxCtas = 256;
 // Workspace carve-up shared by the size query and the launch.  [ctrl, zero_end) is
 // cleared at the start of every call.
 struct WorkspaceLayout {
-  size_t ctrl, bar, keys, zbound, zero_end, z, zmax, zwritten, cand, zc, prev, conf, part_val,
+  size_t ctrl, bar, keys, zbound, walk_done, zero_end, z, zmax, zwritten, cand, zc, prev, conf, part_val,
       part_id, total;
   size_t Vhp, ldb, ldz;
 };
