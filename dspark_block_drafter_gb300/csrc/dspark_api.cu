@@ -328,21 +328,51 @@ dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head
   auto d2h = [&](void* dst, size_t off, size_t bytes) {
     return cudaMemcpyAsync(dst, ws + off, bytes, cudaMemcpyDeviceToHost, cs);
   };
-  if ((e = h2d(s.hidden, hidden_h, es * B * cfg->L_in * cfg->H)) != cudaSuccess ||
-      (e = h2d(s.anchors, anchors_h, 4 * B)) != cudaSuccess ||
-      (e = h2d(s.target, target_h, 4 * B * (N + 1))) != cudaSuccess)
+  // Page-locked host buffers that the GPU can address (cudaHostAlloc / cudaHostRegister
+  // with a device mapping) are read and written by the kernels in place: each small copy
+  // costs more in fixed overhead than its bytes.  The hidden states, the one large
+  // input, still go by copy (the TMA loads of the GEMM need device memory).
+  auto device_view = [](const void* h) -> void* {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+  };
+  if ((e = h2d(s.hidden, hidden_h, es * B * cfg->L_in * cfg->H)) != cudaSuccess)
     return cuda_fail(e, "host-to-device copy");
+  const int32_t* anchors_d = (const int32_t*)device_view(anchors_h);
+  const int32_t* target_d = (const int32_t*)device_view(target_h);
+  if (!anchors_d) {
+    if ((e = h2d(s.anchors, anchors_h, 4 * B)) != cudaSuccess)
+      return cuda_fail(e, "host-to-device copy");
+    anchors_d = (const int32_t*)(ws + s.anchors);
+  }
+  if (!target_d) {
+    if ((e = h2d(s.target, target_h, 4 * B * (N + 1))) != cudaSuccess)
+      return cuda_fail(e, "host-to-device copy");
+    target_d = (const int32_t*)(ws + s.target);
+  }
+  // outputs: in place when every one of them is addressable, else staged and copied
+  void* out_d[6] = {device_view(draft_h), device_view(n_draft_h), device_view(accepted_h),
+                    device_view(bonus_h), topk_ids_h ? device_view(topk_ids_h) : nullptr,
+                    topk_vals_h ? device_view(topk_vals_h) : nullptr};
+  const bool in_place = out_d[0] && out_d[1] && out_d[2] && out_d[3] &&
+                        (!topk_ids_h || out_d[4]) && (!topk_vals_h || out_d[5]);
   dspark_outputs o{};
-  o.draft = (int32_t*)(ws + s.draft);
-  o.n_draft = (int32_t*)(ws + s.n_draft);
-  o.topk_ids = topk_ids_h ? (int32_t*)(ws + s.tk_ids) : nullptr;
-  o.topk_vals = topk_vals_h ? (float*)(ws + s.tk_vals) : nullptr;
-  st = propose_impl(cfg, head, ws + s.hidden, (const int32_t*)(ws + s.anchors), &o, workspace,
-                    base, stream, nullptr);
+  o.draft = in_place ? (int32_t*)out_d[0] : (int32_t*)(ws + s.draft);
+  o.n_draft = in_place ? (int32_t*)out_d[1] : (int32_t*)(ws + s.n_draft);
+  o.topk_ids = !topk_ids_h ? nullptr : in_place ? (int32_t*)out_d[4] : (int32_t*)(ws + s.tk_ids);
+  o.topk_vals = !topk_vals_h ? nullptr : in_place ? (float*)out_d[5] : (float*)(ws + s.tk_vals);
+  int32_t* accepted_d = in_place ? (int32_t*)out_d[2] : (int32_t*)(ws + s.accepted);
+  int32_t* bonus_d = in_place ? (int32_t*)out_d[3] : (int32_t*)(ws + s.bonus);
+  st = propose_impl(cfg, head, ws + s.hidden, anchors_d, &o, workspace, base, stream, nullptr);
   if (st != DSPARK_OK) return st;
-  st = dspark_verify(cfg->B, N, o.draft, o.n_draft, (const int32_t*)(ws + s.target),
-                     (int32_t*)(ws + s.accepted), (int32_t*)(ws + s.bonus), nullptr, stream);
+  st = dspark_verify(cfg->B, N, o.draft, o.n_draft, target_d, accepted_d, bonus_d, nullptr,
+                     stream);
   if (st != DSPARK_OK) return st;
+  if (in_place) return DSPARK_OK;
   if ((e = d2h(draft_h, s.draft, 4 * B * N)) != cudaSuccess ||
       (e = d2h(n_draft_h, s.n_draft, 4 * B)) != cudaSuccess ||
       (e = d2h(accepted_h, s.accepted, 4 * B)) != cudaSuccess ||

@@ -216,9 +216,13 @@ size_t dspark_step_host_workspace_size(const dspark_config* cfg, const dspark_he
  * accepted_h, bonus_h host [B] int32
  * topk_ids_h / topk_vals_h host [B, N, top_k] or NULL
  *
- * All copies are cudaMemcpyAsync on `stream`; for them to overlap, the host buffers
- * should be page-locked.  The call returns once everything is queued: synchronise
- * `stream` before reading the outputs.
+ * hidden_h is copied with cudaMemcpyAsync on `stream`.  The other buffers are read or
+ * written by the kernels in place when they are page-locked host memory the device can
+ * address (cudaHostAlloc, or cudaHostRegister with a mapping; cudaPointerGetAttributes
+ * reports them as host memory with a device pointer); otherwise they too are copied
+ * through workspace staging.  Page-locked buffers throughout are the fast case.  The
+ * call returns once everything is queued: synchronise `stream` before reading the
+ * outputs.
  */
 dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head,
                                const void* hidden_h, const int32_t* anchors_h,
