@@ -274,3 +274,11 @@ def test_pm_skip_with_every_row_fallback():
     hd["lm_bias"] = bias
     g, o, rep = run_case(wl, hd=hd, bt=bt, chain="pruned")
     assert (g["draft"] < 640).all()
+
+
+# ------------------------------------------------------------------ slot counts that do not
+# fill 256-row tiles (7 and 6 slots; one, two and three block tiles)
+@pytest.mark.parametrize("B,L_in,sfa", [(32, 7, True), (64, 7, False), (96, 7, False)])
+def test_odd_slot_counts_pruned(B, L_in, sfa):
+    run_case(_small(B=B, L_in=L_in, sample_from_anchor=sfa, H=128, V=2048, r=16, top_k=3),
+             chain="pruned")
