@@ -41,7 +41,7 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
   // the maxima of the lower bounds with which the GEMM leaves tiles of z out start from
   // zero (below every key) in every pass
   if (pruned) {
-    w.zbound = take(sizeof(uint32_t) * (size_t)N * B * k);
+    w.zbound = take(sizeof(uint32_t) * (size_t)N * B * 2 * k);   // up to two maxima per rank
     w.walk_done = take(sizeof(int32_t) * (size_t)B);
   }
   w.zero_end = off;

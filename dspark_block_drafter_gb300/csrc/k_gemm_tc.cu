@@ -45,6 +45,12 @@ constexpr int kBlockV = 128;      // MMA M: head rows per tile
 constexpr int kBlockK = 64;       // one 128-byte swizzle row of bf16
 constexpr uint32_t kStageA = kBlockV * kBlockK * 2;   // 16 KB
 constexpr int kThreads = 192;
+#ifndef DSPARK_GEMM_BUCKET_X
+#define DSPARK_GEMM_BUCKET_X 2
+#endif
+// Per (slot, block) row, the GEMM keeps zbound_k x kBucketX maxima of tile lower bounds
+// (when zbound_k <= 8), of which the zbound_k-th largest bounds the threshold.
+constexpr int kBucketX = DSPARK_GEMM_BUCKET_X;
 constexpr long long kWaitBudget = 2000000000ll;       // ~1 s of SM clocks
 #ifndef DSPARK_GEMM_MAX_KPB
 #define DSPARK_GEMM_MAX_KPB 2
@@ -57,7 +63,8 @@ struct GemmArgs {
   float* zmax;     // [N][B][zm_tiles] per-tile maxima of z, or NULL
   // Tiles of z that cannot matter (PM = 1 only; zbound_k = 0 stores every tile): see the
   // PM = 1 epilogue.
-  uint32_t* zbound;        // [N][zbound_k][B] maxima of tile lower bounds (order keys)
+  uint32_t* zbound;        // [N][NB][B] maxima of tile lower bounds (order keys), NB =
+                           // zbound_k x kBucketX for zbound_k <= 8, else zbound_k
   uint8_t* zwritten;       // [N][B][zm_tiles]
   const float* cnmax;      // [zm_tiles] largest markov_w2 column norm of each tile
   const unsigned* w1max;   // largest markov_w1 row norm (float bits)
@@ -333,6 +340,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     const int il = p / g.BB, bl = p - il * g.BB;     // slot and block within this CTA's half
     const size_t oct_step = g.ldb * 8;               // floats between consecutive row octets
     const int K = g.zbound_k;
+    const int NB = K <= 8 ? K * kBucketX : K;        // maxima kept per row
     const float umax = K > 0 ? __uint_as_float(*g.w1max) * (1.f + kPrunedRelMargin) : 0.f;
     // a key of the same order as the float, 0 below every float
     auto ukey = [](float f) { return (uint32_t)order_key32(f) ^ 0x80000000u; };
@@ -355,14 +363,31 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       float* zrow = live ? g.z + ((size_t)i * (g.Vhp / 8) * g.ldb + (size_t)b) * 8 : g.z;
       // this row's maxima sit B apart, so that a warp's consecutive blocks read and
       // update them in whole sectors
-      uint32_t* bound = (K > 0 && live) ? g.zbound + (size_t)i * K * g.B + b : nullptr;
+      uint32_t* bound = (K > 0 && live) ? g.zbound + (size_t)i * NB * g.B + b : nullptr;
       // the current threshold, read once for both 128-row tiles (first, so that its
       // latency hides behind the TMEM loads; any value read is a valid bound, they only
       // grow)
       uint32_t th = 0;
       if (bound && vt * 2 * kBlockV < g.Vh) {
-        th = 0xFFFFFFFFu;
-        for (int j = 0; j < K; ++j) th = min(th, __ldcg(bound + (size_t)j * g.B));
+        if (NB == K) {
+          th = 0xFFFFFFFFu;
+          for (int j = 0; j < K; ++j) th = min(th, __ldcg(bound + (size_t)j * g.B));
+        } else {
+          // the K-th largest of the NB maxima (K <= 8): a descending top 8 by insertion
+          uint32_t top[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          for (int j = 0; j < NB; ++j) {
+            uint32_t x = __ldcg(bound + (size_t)j * g.B);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t hi = max(top[q], x);
+              x = min(top[q], x);
+              top[q] = hi;
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q == K - 1) th = top[q];
+        }
       }
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -399,7 +424,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
           if (bound) {
             const float d = umax * g.cnmax[rt] * (1.f + kPrunedRelMargin) + kPrunedAbsMargin;
             store = ukey(m + d) >= th;
-            atomicMax(bound + (size_t)(rt % K) * g.B, ukey(m - d));
+            atomicMax(bound + (size_t)(rt % NB) * g.B, ukey(m - d));
           }
           if (g.zmax) g.zmax[((size_t)i * g.B + b) * g.zm_tiles + rt] = m;
           if (g.zwritten) g.zwritten[((size_t)i * g.B + b) * g.zm_tiles + rt] = store ? 1 : 0;

@@ -53,8 +53,8 @@ struct ProposePlan {
                         //               [N][B][cap_a]
   int32_t* tk_id;       //               top-k tokens given each previous row
   float* tk_val;        //               [N][B][cap_a][k], and their values
-  uint32_t* zbound;     //               [N][zbound_k][B] maxima of the tiles' lower bounds
-                        //               (unsigned order keys; tile t goes to t % zbound_k)
+  uint32_t* zbound;     //               [N][2 zbound_k][B] room for the maxima of the tiles'
+                        //               lower bounds (unsigned order keys)
   uint8_t* zwritten;    //               [N][B][Vhp / 128] whether the GEMM stored the
                         //               tile's z (NULL: it stored every tile)
   int zbound_k;         //               0: the GEMM stores every tile
