@@ -14,12 +14,16 @@
 // rows A(i - 1) that can be the previous slot's argmax (theta of rank 1); the previous
 // token of slot i is the head row chosen in slot i - 1, which lies in A(i - 1) (slot 0:
 // the anchor).  It then evaluates z' exactly (fp32) for every pair of a possible previous
-// row and a candidate: a small table.  The sequential walk over the slots, one CTA per
-// block, is left with table lookups and a warp-wide argmax per slot; top-k follows for
-// all slots in parallel.  The bounds carry a margin for fp32 rounding, so every
-// selection equals that of evaluating every row.  Where a list or a table would not fit
-// (loose bounds), the walk evaluates that slot on the fly, over every row if need be, so
-// the pruning only changes the cost, never the result.
+// row and a candidate: a small table.  The sequential walk over a block's slots, run by
+// the last of the block's CTAs to finish its table, is left with table lookups per slot;
+// the top-k of the rows taken is copied from the tables.  The bounds carry a margin for
+// fp32 rounding, so every selection equals that of evaluating every row.  Where a list
+// or a table would not fit (loose bounds), the walk evaluates that slot on the fly, over
+// every row if need be, so the pruning only changes the cost, never the result.
+//
+// The lm_head GEMM applies the same bounds to leave out tiles of z that cannot reach a
+// slot's top k (zwritten says which); such a tile counts here as one whose upper bound
+// is -inf.
 //
 // One-time preparation (dspark_prepare_head) stores markov_w2 transposed ([V_head][r],
 // a row's Markov weights contiguous), the column norms cn, their per-tile maxima and
@@ -36,7 +40,7 @@ namespace dspark {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 256;                // threads of both kernels
+constexpr int kThreads = 256;                // threads of the kernels
 constexpr int kWarps = kThreads / 32;
 static_assert((kWarps & (kWarps - 1)) == 0 && kWarps <= 32, "warp count: a power of two");
 constexpr int kCap = 512;                    // candidate list entries per (slot, block)
