@@ -3,19 +3,21 @@
 //   z[i][v][b] = sum_h hidden[b, ifp + i, h] * lm_head[v, h] + lm_bias[v]
 //
 // (llama.cpp commit 6fed9f6, "spec: add DSpark speculative decoding": logits(i) of the
-// proposal formula.)  The GEMM runs "swap-AB": the MMA's M dimension is the vocabulary
-// (128 head rows per tile), its N dimension the prediction rows of Ni slots x BB blocks
-// (blocks fastest, up to 256), so a small batch still fills the instruction.  The
-// output keeps the blocks of one (slot, head row) contiguous, so each thread stores
-// runs of 16 bytes and the chain reads them back the same way.
+// proposal formula.)  A tile is 128 (or, for a CTA pair, 256) head rows by an N-tile of
+// Ni slots x BB blocks (blocks fastest, up to 256 prediction rows).  By default the GEMM
+// runs "swap-AB": the MMA's M dimension is the head rows and its N dimension the
+// prediction rows, so a small batch still fills the instruction.  The pruned chain's
+// octet layout of z keeps 8 head rows of one (slot, block) in one 32-byte sector; the
+// dense chain's layout keeps the blocks of one (slot, head row) contiguous.
 //
 // Persistent and warp-specialised, one CTA per SM:
 //   warp 4      TMA producer: lm_head tile [128 x 64] and hidden tile [Ni, BB, 64] per
-//               K-block into a ring of shared-memory stages (128-byte swizzle)
-//   warp 5      MMA issuer: 4 x tcgen05.mma (K = 16) per stage into a TMEM accumulator;
+//               K-block (two K-blocks per copy when H allows) into a ring of
+//               shared-memory stages (128-byte swizzle)
+//   warp 5      MMA issuer: tcgen05.mma (K = 16) per K-block into a TMEM accumulator;
 //               tcgen05.commit frees the stage, and the accumulator when the tile ends
-//   warps 0-3   epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 head rows), + bias,
-//               fp32 stores of z (16-byte runs of blocks per thread)
+//   warps 0-3   epilogue: tcgen05.ld of their 32 TMEM lanes, + bias, fp32 stores of z,
+//               per-tile maxima for the pruned chain
 // Two TMEM accumulators alternate so that the epilogue of one tile overlaps the MMAs of
 // the next.  Tiles are ordered vocabulary-major: CTAs that run side by side share the
 // same lm_head tile through L2, so lm_head streams from HBM once.
@@ -25,7 +27,10 @@
 // lm_head rows and half of the hidden rows, so a pair moves two thirds of the bytes
 // through shared memory and L2 that two single CTAs would.  The leader (rank 0) posts
 // the byte count of both halves on its own barrier, both CTAs' copies count against it,
-// the leader issues the MMAs, and the commits arrive in both CTAs.
+// the leader issues the MMAs, and the commits arrive in both CTAs.  A pair whose N-tile
+// is exactly 256 prediction rows runs the other way round (PM = 1, see logits_gemm_tc):
+// one prediction row per epilogue thread, and tiles of z that cannot reach a slot's top
+// k are not stored.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
