@@ -30,7 +30,8 @@ from .dspark_oracle import (MASK_BIAS_LIMIT, argmax_lowest, corrected_logits, to
 
 def check_propose(oracle_out: dict, *, anchors, markov_w1, markov_w2, top_k: int,
                   topk_markov: bool, conf_min: float, gpu: dict, tol: float,
-                  head_rows=None, lm_bias=None, max_report: int = 20) -> dict:
+                  head_rows=None, lm_bias=None, max_report: int = 20,
+                  skip_truncated: bool = False) -> dict:
     """Compare GPU proposal outputs with the oracle.
 
     ``oracle_out`` is the dict of :func:`oracle.propose` (its base logits are used).
@@ -41,6 +42,9 @@ def check_propose(oracle_out: dict, *, anchors, markov_w1, markov_w2, top_k: int
     ``lm_bias`` (the full-vocabulary bias, or None) marks masked rows: their logits are
     about -1e9, where fp32 spacing is 64, so for them the check is only that the GPU
     value stays at or below the mask limit.
+    ``skip_truncated``: the GPU ran the adaptive block length.  Slots before the GPU's
+    own n_draft[b] are checked as usual (n_draft itself as below); after it, the draft
+    and top-k ids must read -1 and the top-k values NaN.
     Returns {"failures": [...], "near_ties": int, "slots": int}.
     """
     z = oracle_out["base_logits"]
@@ -58,9 +62,19 @@ def check_propose(oracle_out: dict, *, anchors, markov_w1, markov_w2, top_k: int
     g_ids = gpu.get("topk_ids")
     g_vals = gpu.get("topk_vals")
     g_logits = gpu.get("logits")
+    g_nd = np.asarray(gpu["n_draft"]).astype(np.int64)
     for b in range(B):
         prev = int(anchors[b])
         for i in range(N):
+            if skip_truncated and i >= g_nd[b]:
+                # past the cut: nothing drafted
+                if int(g_draft[b, i]) != -1:
+                    fail(f"draft[{b},{i}]={int(g_draft[b, i])} past n_draft={g_nd[b]}, not -1")
+                if g_ids is not None and np.any(np.asarray(g_ids[b, i]) != -1):
+                    fail(f"topk_ids[{b},{i}] past n_draft={g_nd[b]} not all -1")
+                if g_vals is not None and not np.all(np.isnan(np.asarray(g_vals[b, i]))):
+                    fail(f"topk_vals[{b},{i}] past n_draft={g_nd[b]} not all NaN")
+                continue
             zc = corrected_logits(z[b, i], markov_w1, w2, prev)
             g = int(g_draft[b, i])
             if not 0 <= g < V:
@@ -116,7 +130,6 @@ def check_propose(oracle_out: dict, *, anchors, markov_w1, markov_w2, top_k: int
     # confidence and truncation
     o_conf = oracle_out.get("conf")
     g_conf = gpu.get("conf")
-    g_nd = np.asarray(gpu["n_draft"]).astype(np.int64)
     if o_conf is not None and g_conf is not None:
         g_conf = np.asarray(g_conf, np.float64)
         d = np.abs(g_conf - o_conf)

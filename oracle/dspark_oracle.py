@@ -197,15 +197,32 @@ def greedy_chain(z_b: np.ndarray, w1, w2_f64: np.ndarray, anchor: int,
     return tok, ids, vals, zc
 
 
+def blank_past_cut(draft, tk_ids, tk_vals, n_draft) -> None:
+    """Adaptive block length: the slots of block b from n_draft[b] on are not drafted
+    (draft and top-k ids -1, top-k values NaN), in place."""
+    for b in range(draft.shape[0]):
+        cut = int(n_draft[b])
+        draft[b, cut:] = -1
+        tk_ids[b, cut:] = -1
+        tk_vals[b, cut:] = np.nan
+
+
 def propose(hidden, anchors, lm_head, markov_w1, markov_w2, *, L_in: int,
             sample_from_anchor: bool, top_k: int, conf_min: float,
             lm_bias=None, w_conf=None, b_conf: float = 0.0,
-            topk_markov: bool = True, return_logits: bool = False) -> dict:
+            topk_markov: bool = True, return_logits: bool = False,
+            skip_truncated: bool = False) -> dict:
     """The whole proposal of a batch: base logits, chain, top-k, confidence, truncation.
 
     Returns a dict with draft [B, N], topk_ids / topk_vals [B, N, k], conf [B, N]
     (None without a confidence head), n_draft [B], base logits z [B, N, V] and, when
     asked, the corrected logits [B, N, V].
+
+    ``skip_truncated``: the confidence-gated adaptive block length.  Truncation cuts a
+    block at its first slot below conf_min ([dflash-log], confidence-based draft
+    pruning) and verify reads nothing past that cut, so the slots after it need not be
+    drafted at all: their draft and top-k ids read -1 and their top-k values NaN.  The
+    slots before the cut, the confidences and n_draft are those of the full proposal.
     """
     N, ifp = block_layout(L_in, sample_from_anchor)
     z = base_logits(hidden, lm_head, lm_bias, ifp, N)
@@ -229,6 +246,8 @@ def propose(hidden, anchors, lm_head, markov_w1, markov_w2, *, L_in: int,
     else:
         conf = None
         n_draft = np.full(B, N, np.int64)
+    if skip_truncated:
+        blank_past_cut(draft, tk_ids, tk_vals, n_draft)
     return dict(draft=draft, topk_ids=tk_ids, topk_vals=tk_vals, conf=conf,
                 n_draft=n_draft, base_logits=z, logits=zc_all, N=N,
                 i_first_pred=ifp)

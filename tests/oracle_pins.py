@@ -166,6 +166,49 @@ def pin_brute_force_variants():
     pin_brute_force_tiny("bf16", True, True)
 
 
+def pin_adaptive_block_length():
+    """skip_truncated: slots before the confidence cut are the brute-force proposal's,
+    slots from the cut on read -1 (top-k values NaN), and verify cannot tell the two
+    apart, since it reads nothing past the cut."""
+    from workloads import Workload, make_head, make_batch
+    wl = Workload("ad", B=4, L_in=5, H=8, V=64, r=4, top_k=3, sample_from_anchor=True,
+                  conf_min=0.5, dtype="f32", weight_std=0.5, conf_std=0.5, seed=78)
+    hd = make_head(wl)
+    bt = make_batch(wl)
+    # hidden column 0 and a one-hot w_conf put block b's cut at slot cuts[b]
+    cuts = [0, 2, 4, 5]
+    hidden = np.array(bt["hidden"], np.float32)
+    w_conf = np.zeros(wl.H, np.float32)
+    w_conf[0] = 1.0
+    for b, c in enumerate(cuts):
+        hidden[b, :, 0] = 2.0
+        if c < wl.L_in:
+            hidden[b, c, 0] = -2.0
+    kw = dict(L_in=wl.L_in, sample_from_anchor=True, top_k=3, conf_min=0.5, w_conf=w_conf)
+    o = O.propose(hidden, bt["anchors"], hd["lm_head"], hd["markov_w1"], hd["markov_w2"],
+                  skip_truncated=True, **kw)
+    full = O.propose(hidden, bt["anchors"], hd["lm_head"], hd["markov_w1"],
+                     hd["markov_w2"], **kw)
+    d, tk = _brute_force_propose(hidden, bt["anchors"], hd["lm_head"], hd["markov_w1"],
+                                 hd["markov_w2"], None, wl.L_in, True, 3)
+    assert o["n_draft"].tolist() == cuts
+    for b, c in enumerate(cuts):
+        assert o["draft"][b, :c].tolist() == d[b][:c]
+        assert (o["draft"][b, c:] == -1).all()
+        assert (o["topk_ids"][b, c:] == -1).all() and np.isnan(o["topk_vals"][b, c:]).all()
+        for i in range(c):
+            assert o["topk_ids"][b, i].tolist() == tk[b][i][0]
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        target = rng.integers(0, wl.V, (wl.B, wl.N + 1))
+        target[:, :2] = np.where(rng.uniform(size=(wl.B, 2)) < 0.7,
+                                 np.maximum(full["draft"][:, :2], 0), target[:, :2])
+        a1, b1, e1 = O.verify(o["draft"], o["n_draft"], target)
+        a2, b2, e2 = O.verify(full["draft"], full["n_draft"], target)
+        assert a1.tolist() == a2.tolist() and b1.tolist() == b2.tolist()
+        assert np.array_equal(e1, e2)
+
+
 # ------------------------------------------------------------ special cases / forms
 def pin_zero_markov_is_plain_argmax():
     """w1 = w2 = 0 reduces DSpark to the plain lm_head argmax (DFlash's projection)."""
@@ -367,4 +410,5 @@ ALL_PINS = [
     pin_chain_consistency, pin_single_slot, pin_masked_rows_never_emitted,
     pin_confidence_closed_forms, pin_truncation_positions, pin_verify_brute_force,
     pin_verify_planted_mismatch, pin_bf16_upcast, pin_bonus_slot_unused,
+    pin_adaptive_block_length,
 ]

@@ -127,3 +127,33 @@ def test_masked_rows_only_need_to_stay_masked():
     logits[1, 2, 1] += 0.1           # an emittable row off by more than tol
     rep = check.check_propose(o, gpu=g, **kw)
     assert any("off by" in f for f in rep["failures"])
+
+
+def _adaptive(gpu, o):
+    # the GPU's adaptive output: blanked past the (oracle's) cut
+    from oracle import dspark_oracle as O
+    g = {k: (None if v is None else np.array(v)) for k, v in gpu.items() if k != "logits"}
+    g["topk_vals"] = g["topk_vals"].astype(np.float32)
+    O.blank_past_cut(g["draft"], g["topk_ids"], g["topk_vals"], g["n_draft"])
+    return g
+
+
+def test_adaptive_block_length_passes_and_flags():
+    o, gpu, kw = _case(seed=8)
+    assert (o["n_draft"] < 5).any()                 # some block is cut
+    g = _adaptive(gpu, o)
+    assert check.check_propose(o, gpu=g, skip_truncated=True, **kw)["failures"] == []
+    # the same output checked as a full proposal fails (slots past the cut read -1)
+    assert check.check_propose(o, gpu=g, **kw)["failures"]
+    b = int(np.flatnonzero(o["n_draft"] < 5)[0])
+    cut = int(o["n_draft"][b])
+    bad = {k: v.copy() for k, v in g.items()}
+    bad["draft"][b, cut] = 3                        # a token past the cut
+    assert check.check_propose(o, gpu=bad, skip_truncated=True, **kw)["failures"]
+    bad = {k: v.copy() for k, v in g.items()}
+    bad["topk_vals"][b, cut, 0] = 1.0               # a value past the cut
+    assert check.check_propose(o, gpu=bad, skip_truncated=True, **kw)["failures"]
+    if cut > 0:
+        bad = {k: v.copy() for k, v in g.items()}
+        bad["draft"][b, cut - 1] = -1               # a slot before the cut left blank
+        assert check.check_propose(o, gpu=bad, skip_truncated=True, **kw)["failures"]

@@ -67,6 +67,7 @@ _orig_verify = O.verify
 _orig_layout = O.block_layout
 _orig_base = O.base_logits
 _orig_conf = O.confidence
+_orig_blank = O.blank_past_cut
 
 
 MUTATIONS = {
@@ -96,6 +97,10 @@ MUTATIONS = {
                                 lambda h, W, bias, ifp, N, chunk=16384:
                                 _orig_base(h, np.asarray(W)[:, ::-1], bias, ifp, N, chunk)),
     "verify_ignores_ndraft": ("verify", _verify_no_ndraft),
+    "adaptive_cut_one_late": ("blank_past_cut",
+                              lambda d, i, v, nd: _orig_blank(d, i, v, np.asarray(nd) + 1)),
+    "adaptive_cut_one_early": ("blank_past_cut",
+                               lambda d, i, v, nd: _orig_blank(d, i, v, np.maximum(np.asarray(nd) - 1, 0))),
     "verify_bonus_off_by_one": ("verify", _verify_bonus_next),
     "upcast_truncates": ("upcast",
                          lambda a: (np.asarray(a).astype(np.float32).astype(np.float16).astype(np.float64)
