@@ -30,7 +30,7 @@ c_ptr = ctypes.c_void_p
 class dspark_config(ctypes.Structure):
     _fields_ = [("B", c_i32), ("L_in", c_i32), ("H", c_i32), ("V", c_i32), ("r", c_i32),
                 ("top_k", c_i32), ("sample_from_anchor", c_i32), ("topk_markov", c_i32),
-                ("conf_min", ctypes.c_float), ("dtype", c_i32)]
+                ("conf_min", ctypes.c_float), ("dtype", c_i32), ("skip_truncated", c_i32)]
 
 
 class dspark_head(ctypes.Structure):

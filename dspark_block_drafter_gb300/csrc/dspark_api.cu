@@ -81,6 +81,8 @@ static dspark_status validate(const dspark_config* c, const dspark_head* h, int*
     return fail(DSPARK_ERR_INVALID_ARG, "sample_from_anchor must be 0 or 1");
   if (c->topk_markov != 0 && c->topk_markov != 1)
     return fail(DSPARK_ERR_INVALID_ARG, "topk_markov must be 0 or 1");
+  if (c->skip_truncated != 0 && c->skip_truncated != 1)
+    return fail(DSPARK_ERR_INVALID_ARG, "skip_truncated must be 0 or 1");
   if (c->dtype != DSPARK_F32 && c->dtype != DSPARK_BF16)
     return fail(DSPARK_ERR_INVALID_ARG, "dtype must be DSPARK_F32 or DSPARK_BF16");
   if (!c->sample_from_anchor && c->L_in < 2)
@@ -119,7 +121,7 @@ static dspark_status validate(const dspark_config* c, const dspark_head* h, int*
 
 using namespace dspark;
 
-static_assert(sizeof(dspark_config) == 40, "dspark_config layout");
+static_assert(sizeof(dspark_config) == 44, "dspark_config layout");
 static_assert(sizeof(dspark_head) == 72, "dspark_head layout");
 static_assert(sizeof(dspark_outputs) == 48, "dspark_outputs layout");
 
@@ -152,6 +154,10 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   if (cfg->dtype == DSPARK_BF16 && !aligned(hidden, 16))
     return fail(DSPARK_ERR_INVALID_ARG, "bf16 hidden must be 16-byte aligned");
   const bool pruned = use_pruned(cfg, head) && !out->logits;
+  if (cfg->skip_truncated && !pruned)
+    return fail(DSPARK_ERR_UNSUPPORTED,
+                "skip_truncated needs the pruned chain: bf16, a prepared head, no logits "
+                "output");
   WorkspaceLayout wl = plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype, pruned);
   if (!workspace || !aligned(workspace, 256))
     return fail(DSPARK_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
@@ -203,6 +209,7 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
     p.tk_val = (float*)(lists + ll.tk_val);
     p.z_octet = true;           // the candidate scans read one block's rows of z
     p.walk_done = (int32_t*)(ws + wl.walk_done);
+    p.skip_truncated = cfg->skip_truncated != 0;
     // Tiles of z that provably cannot hold a slot's top k are left out by the GEMM when
     // it runs with the prediction rows on M and the top-k ranks corrected logits.
     const bool want_topk = out->topk_ids || out->topk_vals;
@@ -221,8 +228,10 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   e = cudaMemsetAsync(ws + wl.ctrl, 0, wl.zero_end - wl.ctrl, p.stream);
   if (e != cudaSuccess) return cuda_fail(e, "control reset");
   if ((e = mark(DSPARK_STAGE_CONF)) != cudaSuccess) return cuda_fail(e, "event record");
-  // the pruned chain evaluates the confidence head and truncation in its own kernels
-  if (!pruned && (e = launch_conf(p)) != cudaSuccess) return cuda_fail(e, "confidence kernel");
+  // the pruned chain evaluates the confidence head and truncation in its own kernels,
+  // unless the adaptive block length needs the cuts before the GEMM
+  if ((!pruned || p.skip_truncated) && (e = launch_conf(p)) != cudaSuccess)
+    return cuda_fail(e, "confidence kernel");
   if ((e = mark(DSPARK_STAGE_LOGITS)) != cudaSuccess) return cuda_fail(e, "event record");
   e = p.dtype == DSPARK_BF16 ? launch_base_logits_tc(p) : launch_base_logits_simt(p);
   if (e != cudaSuccess) return cuda_fail(e, "base logits");
@@ -260,7 +269,8 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK || !out) return -1;
   if (cfg->dtype == DSPARK_F32) return 1 + 1 + 2 * N;   // confidence, GEMM, 2 per slot
-  if (use_pruned(cfg, head) && !out->logits) return 2;  // GEMM; tables with the walk
+  if (use_pruned(cfg, head) && !out->logits)            // GEMM; tables with the walk;
+    return cfg->skip_truncated ? 3 : 2;                 // confidence first when adaptive
   const bool topk = out->topk_ids || out->topk_vals;
   return 1 /* confidence */ + 1 /* GEMM */ + (cfg->B + 31) / 32 /* chain, 32 blocks each */ +
          (topk ? 1 : 0);

@@ -345,6 +345,8 @@ struct TableArgs {
   float* tk_val;             // [N][B][kCapA][k]
   uint32_t* err;
   int* walk_done;            // [B], zero at the start of the pass: table CTAs done per block
+  const int32_t* nd_in;      // [B] cuts computed before the chain (adaptive block length:
+                             // slots from the cut on are skipped), or NULL
   int B, N, V, Vh, T, r, k, kk, zrank, want_topk, L_in, ifp, H;
 };
 
@@ -417,6 +419,8 @@ __device__ void scan_rows(const float* z, size_t b, size_t Vhp, size_t ldb, cons
 // ------------------------------------------------------------------ the walk
 struct SelectArgs {
   const float* z;            // octet layout (read only to evaluate every row)
+  const int32_t* nd_in;      // [B] cuts computed before the chain (adaptive block length:
+                             // slots from the cut on are not drafted), or NULL
   const uint8_t* zw;         // [N][B][T]: 0 where the GEMM left the tile's z out, or NULL
   int T;
   size_t Vhp, ldb;
@@ -513,19 +517,21 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
   int& s_prev = s_keep[kMaxKeep + 1];
   int& s_stop = s_keep[kMaxKeep + 2];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  // slots to draft: all, or (adaptive block length) those before the precomputed cut
+  const int cut = a.nd_in ? min(max(a.nd_in[b], 0), a.N) : a.N;
 
   // ---- counts, then the previous rows and argmax rows of every tabulated slot
-  for (int i = tid; i < a.N; i += kThreads) {
+  for (int i = tid; i < cut; i += kThreads) {
     s_nc[i] = a.cand_n[(size_t)i * a.B + b];
     s_na[i] = a.prev_n[(size_t)i * a.B + b];
   }
-  if (a.conf)
+  if (a.conf && !a.nd_in)
     for (int i = tid; i < a.N; i += kThreads) cp_async4(&s_conf[i], a.conf + (size_t)b * a.N + i);
   __syncthreads();
   auto tabulated = [&](int i) {
     return s_nc[i] >= 1 && s_nc[i] <= kTabC && s_na[i] >= 1 && s_na[i] <= kCapA;
   };
-  for (int e = tid; e < a.N * kCapA; e += kThreads) {
+  for (int e = tid; e < cut * kCapA; e += kThreads) {
     const int i = e / kCapA, p = e % kCapA;
     if (tabulated(i) && p < s_na[i]) {
       const size_t o = ((size_t)i * a.B + b) * kCapA + p;
@@ -539,7 +545,7 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
   // ---- warp 0 walks the tabulated slots as far as it can
   if (warp == 0) {
     int prev = -1, step = 0;
-    for (; step < a.N; ++step) {
+    for (; step < cut; ++step) {
       if (!tabulated(step)) break;
       int pi = 0;
       if (step > 0) {
@@ -562,7 +568,7 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
     }
   }
   __syncthreads();
-  for (int step = s_stop; step < a.N; ++step) {
+  for (int step = s_stop; step < cut; ++step) {
     // -------- a tabulated slot whose previous row is listed: a lookup
     if (tid == 0) {
       int pi = -1;
@@ -675,24 +681,34 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
 
   // ---- the draft: every slot's chosen head row as a token
   for (int i = tid; i < a.N; i += kThreads) {
-    const int row = s_row[i];
-    a.draft[(size_t)b * a.N + i] = a.d2t ? a.d2t[row] : row;
+    int tok = -1;                                    // past the cut: not drafted
+    if (i < cut) {
+      const int row = s_row[i];
+      tok = a.d2t ? a.d2t[row] : row;
+    }
+    a.draft[(size_t)b * a.N + i] = tok;
   }
   // ---- top-k of the looked-up slots: the entries stored for the chosen previous row
   if (a.want_topk) {
     for (int e = tid; e < a.N * a.k; e += kThreads) {
       const int i = e / a.k, q = e % a.k;
+      const size_t dst = ((size_t)b * a.N + i) * a.k + q;
+      if (i >= cut) {                                // past the cut: not drafted
+        if (a.topk_ids) a.topk_ids[dst] = -1;
+        if (a.topk_vals) a.topk_vals[dst] = NAN;
+        continue;
+      }
       const int pi = s_pi[i];
       if (pi < 0) continue;                          // written by the on-the-fly step
       const size_t src = (((size_t)i * a.B + b) * kCapA + pi) * a.k + q;
-      const size_t dst = ((size_t)b * a.N + i) * a.k + q;
       if (a.topk_ids) a.topk_ids[dst] = a.tk_id[src];
       if (a.topk_vals) a.topk_vals[dst] = a.tk_val[src];
     }
   }
   // ---- truncation at the first slot whose confidence is below conf_min (llama.cpp
   //      commit 6fed9f6, "spec: add confidence-based draft pruning for DSpark")
-  if (tid == 0) {
+  //      (already computed, before the GEMM, with the adaptive block length)
+  if (tid == 0 && !a.nd_in) {
     int nd = a.N;
     if (a.conf && a.conf_min > 0.f)
       for (int i = 0; i < a.N; ++i)
@@ -710,9 +726,7 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
 // argmax and the top-k of slot i.  Also the slot's confidence.
 // Four CTAs per SM (at most 64 registers a thread), so that the B x N CTAs of the
 // Qwen3-8B-shaped batch (512) run in one wave on 152 SMs.
-__global__ void __launch_bounds__(kThreads, 4)
-pruned_table(const TableArgs a, const SelectArgs sel) {
-  extern __shared__ __align__(16) uint8_t dsm[];
+__device__ __forceinline__ void table_work(const TableArgs& a, uint8_t* dsm, int b, int i) {
   const int T4 = (a.T + 3) & ~3;
   float* s_ub = (float*)dsm;                                   // [T4] upper bounds, slot i
   float* s_up = s_ub + T4;                                     // [T4] upper bounds, slot i-1
@@ -727,10 +741,7 @@ pruned_table(const TableArgs a, const SelectArgs sel) {
   __shared__ float s_theta, s_red[kWarps];
   __shared__ int s_ntc, s_nta, s_nc, s_na;
   __shared__ int32_t s_av[kCapA];
-  const int b = blockIdx.x, i = blockIdx.y;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  pdl_signal();
-  pdl_wait();                                        // z and zmax of the lm_head GEMM
   const float umax = __uint_as_float(*a.w1max) * (1.f + kRelMargin);
   const float* zm = a.zmax + ((size_t)i * a.B + b) * a.T;
   const float* zp = i > 0 ? a.zmax + ((size_t)(i - 1) * a.B + b) * a.T : nullptr;
@@ -957,6 +968,17 @@ pruned_table(const TableArgs a, const SelectArgs sel) {
       }
     }
   }
+}
+
+__global__ void __launch_bounds__(kThreads, 4)
+pruned_table(const TableArgs a, const SelectArgs sel) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  const int b = blockIdx.x, i = blockIdx.y;
+  const int tid = threadIdx.x;
+  pdl_signal();
+  pdl_wait();                                        // z and zmax of the lm_head GEMM
+  // with the adaptive block length, a slot from the block's cut on is not drafted
+  if (!a.nd_in || i < a.nd_in[b]) table_work(a, dsm, b, i);
   // ---- the last of the block's N CTAs to get here walks the block (the others' lists
   //      and tables are in global memory by then)
   __shared__ int s_last;
@@ -1051,7 +1073,8 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   t.anchors = p.anchors;
   t.d2t = p.d2t;
   t.hidden = (const __nv_bfloat16*)p.hidden;
-  t.w_conf = (const __nv_bfloat16*)p.w_conf;
+  // (with the adaptive block length the confidences are already computed)
+  t.w_conf = p.skip_truncated ? nullptr : (const __nv_bfloat16*)p.w_conf;
   t.b_conf = p.b_conf;
   t.conf = p.conf ? p.conf : p.conf_ws;
   t.cand_v = p.cand_v;
@@ -1064,6 +1087,7 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   t.tk_val = p.tk_val;
   t.err = p.ctrl;
   t.walk_done = p.walk_done;
+  t.nd_in = p.skip_truncated ? p.n_draft : nullptr;
   t.B = p.B;
   t.N = p.N;
   t.V = p.V;
@@ -1111,6 +1135,7 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   s.kk = kk;
   s.zrank = zrank;
   s.want_topk = want_topk ? 1 : 0;
+  s.nd_in = p.skip_truncated ? p.n_draft : nullptr;
   // the tables' shared memory, or the walk's when it needs more
   const size_t T4 = (size_t)((T + 3) & ~3);
   const size_t table_smem = sizeof(float) * 4 * T4 + (sizeof(int32_t) + sizeof(float)) * kCap +

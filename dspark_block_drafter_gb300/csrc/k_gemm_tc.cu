@@ -50,6 +50,7 @@ constexpr int kBlockV = 128;      // MMA M: head rows per tile
 constexpr int kBlockK = 64;       // one 128-byte swizzle row of bf16
 constexpr uint32_t kStageA = kBlockV * kBlockK * 2;   // 16 KB
 constexpr int kThreads = 192;
+constexpr int kMaxLiveTiles = 64;     // N-tiles the adaptive block length can leave out
 #ifndef DSPARK_GEMM_BUCKET_X
 #define DSPARK_GEMM_BUCKET_X 2
 #endif
@@ -74,6 +75,8 @@ struct GemmArgs {
   const float* cnmax;      // [zm_tiles] largest markov_w2 column norm of each tile
   const unsigned* w1max;   // largest markov_w1 row norm (float bits)
   int zbound_k;
+  const int32_t* n_draft;  // [B] cuts computed before the GEMM (adaptive block length), or
+                           // NULL: every row is drafted
   int octet;       // z layout: [N][Vhp / 8][ldb][8] (1) or [N][Vhp][ldb] (0)
   const float* bias;
   uint32_t* err;
@@ -133,6 +136,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   // column maxima of the tile over the four epilogue warps, as order-preserving keys
   int* s_cmax = (int*)((uint8_t*)smem + g.stages * (a_stage + b_stage) + 256);   // [256]
+  int* s_live = s_cmax + 256;          // [1 + kMaxLiveTiles]: count, then the live N-tiles
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0;
@@ -155,6 +159,26 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     ptx::fence_barrier_init();
   }
   for (int c = threadIdx.x; c < 256; c += kThreads) s_cmax[c] = INT_MIN;
+  // Adaptive block length: an N-tile whose slots all lie at or past every one of its
+  // blocks' cuts is not computed (the cuts come from the confidence kernel, launched
+  // before this one).  Without cuts, or with more N-tiles than the list holds, all are.
+  const bool cut_tiles = g.n_draft && g.n_tiles <= kMaxLiveTiles;
+  if (warp == 2) {
+    int cnt = 0;
+    for (int nt = 0; nt < g.n_tiles; ++nt) {
+      bool live = true;
+      if (cut_tiles) {
+        int i0, ni, bb0, nb;
+        ntile_extent(g, nt, i0, ni, bb0, nb);
+        bool any = false;
+        for (int bl = lane; bl < nb; bl += 32) any |= g.n_draft[bb0 + bl] > i0;
+        live = __any_sync(0xFFFFFFFFu, any);
+        if (live && lane == 0) s_live[1 + cnt] = nt;
+      }
+      cnt += live;
+    }
+    if (lane == 0) s_live[0] = cnt;
+  }
   if (warp == 4 && lane == 0) {
     ptx::tma_prefetch_desc(&tm_w);
     ptx::tma_prefetch_desc(&tm_h);
@@ -174,7 +198,11 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
   if (CG == 2) ptx::cluster_sync();             // the peer's barriers are initialised
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int num_tiles = g.v_tiles * g.n_tiles;
+  const int n_live = s_live[0];
+  const int num_tiles = g.v_tiles * n_live;
+  // tile t: vocabulary tile t / n_live, N-tile the (t % n_live)-th live one
+  auto tile_vt = [&](int t) { return t / n_live; };
+  auto tile_nt = [&](int t) { return cut_tiles ? s_live[1 + t % n_live] : t % n_live; };
   // cluster addresses of the leader's full / acc_empty barriers (unused for CG = 1)
   const uint32_t full0 = CG == 2 ? ptx::mapa_shared(ptx::smem_u32(full), 0) : 0;
   const uint32_t acc_empty0 = CG == 2 ? ptx::mapa_shared(ptx::smem_u32(acc_empty), 0) : 0;
@@ -193,7 +221,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       uint32_t it = 0, s = 0, ph = 0;          // stages issued; ring slot and phase
       bool ok = true;
       for (int tile = unit; ok && tile < num_tiles; tile += units) {
-        const int vt = tile / g.n_tiles, nt = tile % g.n_tiles;
+        const int vt = tile_vt(tile), nt = tile_nt(tile);
         const int row_a = (vt * CG + (int)rank) * kBlockV;
         const int bcol = (nt % g.n_bt) * g.BB;
         const int slot = g.ifp + (nt / g.n_bt) * g.Ni + (int)rank * ni_half;
@@ -262,7 +290,7 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       const uint32_t a_base = ptx::smem_u32(sA), b_base = ptx::smem_u32(sB);
       for (int tile = unit; ok && tile < num_tiles; tile += units, ++local) {
         int i0, ni, bb0, nb;
-        ntile_extent(g, tile % g.n_tiles, i0, ni, bb0, nb);
+        ntile_extent(g, tile_nt(tile), i0, ni, bb0, nb);
         // rows up to the last valid slot (a pair always covers the full tile)
         const int n_mma = CG == 2 ? g.bn_mma : (ni * g.BB + 15) / 16 * 16;
         const uint32_t idesc = ptx::idesc_bf16_f32(kBlockV * CG, n_mma, 0, 0);
@@ -350,11 +378,12 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     // a key of the same order as the float, 0 below every float
     auto ukey = [](float f) { return (uint32_t)order_key32(f) ^ 0x80000000u; };
     for (int tile = unit; tile < num_tiles; tile += units, ++local) {
-      const int vt = tile / g.n_tiles;
+      const int vt = tile_vt(tile);
       int i0, ni, bb0, nb;
-      ntile_extent(g, tile % g.n_tiles, i0, ni, bb0, nb);
+      ntile_extent(g, tile_nt(tile), i0, ni, bb0, nb);
       const int islot = (int)rank * (g.Ni / CG) + il;   // slot within the N-tile
-      const bool live = islot < ni && bl < nb;
+      // (rows past their block's cut: not drafted, nothing stored)
+      const bool live = islot < ni && bl < nb && (!g.n_draft || i0 + islot < g.n_draft[bb0 + bl]);
       const int i = i0 + islot, b = bb0 + bl;
       const uint32_t acc = local & 1, aph = (local >> 1) & 1;
       const bool ok = __all_sync(0xFFFFFFFFu,
@@ -470,10 +499,10 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     uint32_t local = 0;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     for (int tile = unit; tile < num_tiles; tile += units, ++local) {
-      const int vt = tile / g.n_tiles;
+      const int vt = tile_vt(tile);
       const int rt = vt * CG + (int)rank;              // this CTA's 128-row tile
       int i0, ni, bb0, nb;
-      ntile_extent(g, tile % g.n_tiles, i0, ni, bb0, nb);
+      ntile_extent(g, tile_nt(tile), i0, ni, bb0, nb);
       const int rows = ni * g.BB;
       const uint32_t acc = local & 1, aph = (local >> 1) & 1;
       // the warp leaves together: tcgen05.ld below is a warp-collective instruction
@@ -742,6 +771,7 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   g.cnmax = p.cnmax;
   g.w1max = p.w1max;
   g.zbound_k = p.zbound_k;
+  g.n_draft = p.skip_truncated ? p.n_draft : nullptr;
   g.Vhp = p.Vhp;
   g.ldb = p.ldb;
   g.zmax = p.zmax;
@@ -767,7 +797,7 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   // H loads zeros there, which add nothing.
   // shared memory: up to 1023 bytes of alignment, the stages, 256 bytes of barriers and
   // the column-maximum keys
-  const size_t fixed = 1024 + 256 + 256 * sizeof(int);
+  const size_t fixed = 1024 + 256 + (256 + 1 + kMaxLiveTiles) * sizeof(int);
   const int box_rows = g.BB * g.Ni / CG;
   const uint32_t kblock_bytes = kStageA + (uint32_t)(g.bn_mma / CG) * kBlockK * 2;
   g.kpb = 1;

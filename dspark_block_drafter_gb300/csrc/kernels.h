@@ -59,6 +59,8 @@ struct ProposePlan {
                         //               tile's z (NULL: it stored every tile)
   int zbound_k;         //               0: the GEMM stores every tile
   int32_t* walk_done;   //               [B] table CTAs finished per block (zeroed per pass)
+  bool skip_truncated;  // adaptive block length: n_draft is computed before the GEMM and
+                        // the slots from it on are not drafted
   float* z;             // base logits: [N][Vhp][ldb] (slot, head row, block fastest), or
                         // [N][Vhp / 8][ldb][8] when z_octet (see z_octet_index)
   bool z_octet;

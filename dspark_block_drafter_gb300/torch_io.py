@@ -35,11 +35,12 @@ def to_device(a, device="cuda") -> torch.Tensor:
 
 
 def make_config(B, L_in, H, V, r, top_k, sample_from_anchor, conf_min, dtype,
-                topk_markov=True) -> _abi.dspark_config:
+                topk_markov=True, skip_truncated=False) -> _abi.dspark_config:
     return _abi.dspark_config(B=B, L_in=L_in, H=H, V=V, r=r, top_k=top_k,
                               sample_from_anchor=int(bool(sample_from_anchor)),
                               topk_markov=int(bool(topk_markov)), conf_min=float(conf_min),
-                              dtype=_DT[dtype] if isinstance(dtype, str) else int(dtype))
+                              dtype=_DT[dtype] if isinstance(dtype, str) else int(dtype),
+                              skip_truncated=int(bool(skip_truncated)))
 
 
 @dataclasses.dataclass

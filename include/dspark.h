@@ -76,6 +76,14 @@ typedef struct dspark_config {
   float conf_min;             /* truncate at the first slot with conf < conf_min;
                                  <= 0 disables truncation (n_draft = N) */
   int32_t dtype;              /* dspark_dtype of hidden, lm_head, markov_w1/w2, w_conf */
+  int32_t skip_truncated;     /* 0: every slot is drafted; n_draft only marks the cut.
+                                 1: adaptive block length -- the confidences and n_draft
+                                 are computed first, and the slots of block b from
+                                 n_draft[b] on are not drafted: draft and topk_ids read
+                                 -1 there, topk_vals NaN (llama.cpp DSpark log,
+                                 confidence-based draft pruning: verify reads nothing
+                                 past the cut).  bf16 with a prepared head and no logits
+                                 output only (DSPARK_ERR_UNSUPPORTED otherwise). */
 } dspark_config;
 
 /* The drafter head's weights (device memory, not modified). */

@@ -117,6 +117,19 @@ def test_status_strings(lib):
 
 def test_struct_layouts_match_c():
     # pointer-sized fields are 8 bytes on both hosts; the int/float fields pack as in C
-    assert ctypes.sizeof(_abi.dspark_config) == 40
+    assert ctypes.sizeof(_abi.dspark_config) == 44
     assert ctypes.sizeof(_abi.dspark_head) == 72
     assert ctypes.sizeof(_abi.dspark_outputs) == 48
+
+
+def test_skip_truncated_checked_before_launch(lib):
+    head = _head()
+    # not 0/1: invalid configuration, no workspace size
+    assert ds.dspark_propose_workspace_size(_cfg(dtype=1, skip_truncated=2), head) == 0
+    # the fp32 path has no adaptive form: refused before any launch
+    cfg = _cfg(skip_truncated=1)
+    need = ds.dspark_propose_workspace_size(cfg, head)
+    assert need > 0
+    out = _abi.dspark_outputs(draft=0x100, n_draft=0x200)
+    st = ds.dspark_propose(cfg, head, 0x4000, 0x5000, out, 0x10000, need, 0)
+    assert st == _abi.DSPARK_ERR_UNSUPPORTED
