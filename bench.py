@@ -373,6 +373,23 @@ def run_ours(args):
         other = {"chain": "dense", "value": slots / (ms_o / 1e3), "ms_per_step": ms_o,
                  "stage_us": {k: v * 1e3 for k, v in stage_o.items()}}
 
+    # the adaptive block length (skip_truncated) on the same inputs, for reference: work
+    # stops at each block's confidence cut, so it is counted in blocks and in the slots
+    # actually drafted (sum of n_draft), never as B x N drafted slots
+    adaptive = None
+    if head is not dense_head:
+        cfg_a = _abi.dspark_config.from_buffer_copy(cfg)
+        cfg_a.skip_truncated = 1
+        ms_a, stage_a, _ = _time_steps(tio, _abi, cfg_a, head, ws, *common, max(3, K // 2),
+                                       args.warmup, world)
+        ms_a = _max_over_ranks(ms_a, world, dev)
+        drafted = int(out.n_draft.sum().item())
+        adaptive = {"skip_truncated": 1, "ms_per_step": ms_a,
+                    "verified_blocks_per_s": wl.B * world / (ms_a / 1e3),
+                    "drafted_slots_per_s": drafted * world / (ms_a / 1e3),
+                    "mean_n_draft": drafted / wl.B,
+                    "stage_us": {k: v * 1e3 for k, v in stage_a.items()}}
+
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = e2e_host(cfg, head, wl, bt, target, dev, stream, flush, K, args.warmup, world)
 
@@ -417,6 +434,7 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": K * launches,
         "other_chain": other,
+        "adaptive": adaptive,
         "clocks": clk,
         "wall_s_timed_region": t_wall,
     }
