@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + written) of one lm_head GEMM launch from an ncu capture of the
 # current kernel, per workload; the summary and the command are in the named file.
 GEMM_TRAFFIC = {
-    "qwen3_8b_b32": (1.295e9 + 0.051e9, "profiles/logits_gemm_qwen3_8b_b32.md"),
+    "qwen3_8b_b32": (1.281e9 + 0.050e9, "profiles/logits_gemm_qwen3_8b_b32.md"),
 }
 # fp32 CUDA-core peak used for the fp32 path: 152 SMs x 128 FP32 lanes x 2 flops (FMA) x
 # 2.07 GHz maximum SM clock
