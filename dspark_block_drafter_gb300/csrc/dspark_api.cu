@@ -23,6 +23,8 @@ static dspark_status cuda_fail(cudaError_t e, const char* where) {
 }
 
 static constexpr size_t kAlign = 256;
+// the longest wait the self-test may ask for: the budget of the pipelines' own waits
+static constexpr long long kMaxSelftestBudget = 2000000000ll;
 
 WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool pruned) {
   WorkspaceLayout w{};
@@ -421,6 +423,22 @@ dspark_status dspark_device_status(void* workspace, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
   if (word & kErrTimeout) return fail(DSPARK_ERR_TIMEOUT, "a device-side wait timed out");
   return fail(DSPARK_ERR_DEVICE, "a kernel saw a token outside [0, V)");
+}
+
+dspark_status dspark_wait_selftest(void* workspace, size_t workspace_bytes,
+                                   int64_t budget_cycles, int32_t pre_abort, void* stream) {
+  if (!workspace || !aligned(workspace, 256))
+    return fail(DSPARK_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+  if (workspace_bytes < 256)
+    return fail(DSPARK_ERR_WORKSPACE, "workspace too small: need 256 bytes");
+  if (budget_cycles < 1 || budget_cycles > kMaxSelftestBudget)
+    return fail(DSPARK_ERR_INVALID_ARG, "budget_cycles must be in [1, 2e9]");
+  if (pre_abort != 0 && pre_abort != 1)
+    return fail(DSPARK_ERR_INVALID_ARG, "pre_abort must be 0 or 1");
+  cudaError_t e = launch_wait_selftest((uint32_t*)workspace, (long long)budget_cycles,
+                                       pre_abort, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test kernel");
+  return DSPARK_OK;
 }
 
 size_t dspark_prepare_head_size(const dspark_config* cfg, const dspark_head* head) {

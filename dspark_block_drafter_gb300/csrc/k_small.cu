@@ -1,9 +1,10 @@
-// Small kernels of the path: the confidence head with the truncation length, and the
-// greedy verify/accept step.
+// Small kernels of the path: the confidence head with the truncation length, the
+// greedy verify/accept step, and the self-test of the bounded device-side wait.
 #include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace dspark {
 
@@ -95,7 +96,32 @@ verify_kernel(int B, int N, const int32_t* __restrict__ draft,
       emitted[(size_t)b * (N + 1) + j] = j < a ? d[j] : (j == a ? bo : -1);
 }
 
+// Self-test of the bounded wait that every pipeline of the library relies on: one thread
+// waits on a fresh mbarrier that nothing ever arrives on, through the same ptx::mbar_wait
+// the GEMM and the chain pipelines use.  When the clock budget runs out (or, with
+// pre_abort, at once through the abort flag) the wait gives up and the kernel raises the
+// timeout bit of the error word, exactly as a pipeline that lost a copy would.
+__global__ void __launch_bounds__(32)
+wait_selftest(uint32_t* __restrict__ err, long long budget, int pre_abort) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = pre_abort;
+    ptx::fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0, budget, &abort_flag))
+    flag_error(err, kErrTimeout);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t* err, long long budget, int pre_abort,
+                                 cudaStream_t stream) {
+  wait_selftest<<<1, 32, 0, stream>>>(err, budget, pre_abort);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_conf(const ProposePlan& p) {
   float* conf = p.conf ? p.conf : p.conf_ws;

@@ -155,5 +155,7 @@ cudaError_t launch_chain_tc(const ProposePlan& p);
 cudaError_t launch_verify(int B, int N, const int32_t* draft, const int32_t* n_draft,
                           const int32_t* target, int32_t* accepted, int32_t* bonus,
                           int32_t* emitted, cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint32_t* err, long long budget, int pre_abort,
+                                 cudaStream_t stream);
 
 }  // namespace dspark

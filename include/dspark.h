@@ -270,6 +270,29 @@ dspark_status dspark_propose_noalloc(const dspark_config* cfg, const dspark_head
    dspark_propose, and clears it.  DSPARK_OK when no kernel flagged anything. */
 dspark_status dspark_device_status(void* workspace, void* stream);
 
+/*
+ * dspark_wait_selftest -- makes one bounded device-side wait run out, on purpose.
+ *
+ * (No counterpart on the pages: a test hook of this library's failure detection.)  Every
+ * wait inside the library's kernels (a pipeline stage waiting for its copy, the MMA
+ * waiting for a free accumulator, a grid barrier) gives up after a clock budget of about
+ * one second, raises the timeout bit of the workspace's error word and lets the kernel
+ * return, so that the CUDA context stays usable.  This call launches one small kernel that
+ * waits, through the same bounded-wait routine, on a barrier that nothing ever completes.
+ *
+ *   workspace        device, >= 256 bytes, 256-byte aligned; only its first word (the
+ *                    error word) is written.  A dspark_propose workspace qualifies.
+ *   budget_cycles    SM clock cycles to wait before giving up, in [1, 2e9].
+ *   pre_abort        1 = the abort flag is already set, so the wait gives up at its first
+ *                    check; 0 = it gives up when the budget runs out.
+ *   stream           the CUDA stream (cudaStream_t), may be NULL.
+ *
+ * Host-detectable errors (above) return before any launch.  Afterwards,
+ * dspark_device_status() on the same workspace reports DSPARK_ERR_TIMEOUT and clears it.
+ */
+dspark_status dspark_wait_selftest(void* workspace, size_t workspace_bytes,
+                                   int64_t budget_cycles, int32_t pre_abort, void* stream);
+
 /* Static description of a status code. */
 const char* dspark_status_string(int32_t status);
 

@@ -133,3 +133,15 @@ def test_skip_truncated_checked_before_launch(lib):
     out = _abi.dspark_outputs(draft=0x100, n_draft=0x200)
     st = ds.dspark_propose(cfg, head, 0x4000, 0x5000, out, 0x10000, need, 0)
     assert st == _abi.DSPARK_ERR_UNSUPPORTED
+
+
+def test_wait_selftest_checked_before_launch(lib):
+    # every refusal comes before a launch, so none of these needs a GPU
+    W = _abi.DSPARK_ERR_WORKSPACE
+    I = _abi.DSPARK_ERR_INVALID_ARG
+    assert ds.dspark_wait_selftest(None, 256, 1000) == W
+    assert ds.dspark_wait_selftest(0x10010, 256, 1000) == W          # not 256-byte aligned
+    assert ds.dspark_wait_selftest(0x10000, 255, 1000) == W
+    assert ds.dspark_wait_selftest(0x10000, 256, 0) == I
+    assert ds.dspark_wait_selftest(0x10000, 256, 2_000_000_001) == I
+    assert ds.dspark_wait_selftest(0x10000, 256, 1000, pre_abort=2) == I
