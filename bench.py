@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import dataclasses
+import datetime
 import json
 import os
 import statistics
@@ -79,8 +80,8 @@ def _algorithmic(wl, V_head):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle samples, every 20 ms, kept for the timed region."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -89,18 +90,26 @@ class ClockSampler:
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
 
-    def start(self):
+    def start(self, ready_timeout_s: float = 5.0):
+        """Starts the sampler and returns once its first sample is written (or after
+        ready_timeout_s), so that it is live before the timed region begins."""
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-i", str(self.index), "-lms", "100"], stdout=self.fh,
+                 "-i", str(self.index), "-lms", "20"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < ready_timeout_s and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -110,28 +119,48 @@ class ClockSampler:
             self.proc.kill()
         self.fh.close()
         with open(self.path) as f:
-            return parse_clocks(f)
+            return parse_clocks(f, window)
 
 
-def parse_clocks(lines):
+BAD_CLOCK_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def _sample_time(stamp: str):
+    try:
+        return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f")
+    except ValueError:
+        return None
+
+
+def parse_clocks(lines, window=None):
     """Summary of nvidia-smi samples (the query columns of ClockSampler.Q, no header):
-    median SM clock, the maximum clock, and every throttle reason seen active."""
+    median SM clock, the maximum clock, and every throttle reason seen active.  With a
+    window (start, end) of local times, only the samples taken inside it count; if none
+    is, every sample does, and "window" says so."""
     rows = []
     for line in lines:
         parts = [x.strip() for x in line.split(",")]
-        if len(parts) >= 9 and parts[1].isdigit():
+        if len(parts) >= 10 and parts[2].isdigit():
             rows.append(parts)
     if not rows:
         return None
-    sm = [int(r[1]) for r in rows]
+    where = "whole run"
+    if window is not None:
+        inside = [r for r in rows
+                  if (t := _sample_time(r[0])) is not None and window[0] <= t <= window[1]]
+        if inside:
+            rows, where = inside, "timed region"
+        else:
+            where = "whole run (no sample fell inside the timed region)"
+    sm = [int(r[2]) for r in rows]
     reasons = set()
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     for r in rows:
-        for n, v in zip(names, r[5:9]):
+        for n, v in zip(names, r[6:10]):
             if v.lower() == "active":
                 reasons.add(n)
-    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]),
-            "samples": len(rows), "reasons": sorted(reasons)}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][3]),
+            "samples": len(rows), "window": where, "reasons": sorted(reasons)}
 
 
 def _dist():
@@ -278,6 +307,7 @@ def _time_steps(tio, _abi, cfg, head, ws, hidden, anchors, out, target, acc, bon
     _barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
+    t_begin = datetime.datetime.now()
     for s_ in range(K):
         flush.zero_()                                   # untimed L2 flush
         ev_step[s_][0].record(stream)
@@ -286,6 +316,7 @@ def _time_steps(tio, _abi, cfg, head, ws, hidden, anchors, out, target, acc, bon
     torch.cuda.synchronize()
     _barrier(world)
     t_wall = time.perf_counter() - t_wall
+    window = (t_begin, datetime.datetime.now())
     assert tio.device_status(ws, stream) == 0
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
 
@@ -303,7 +334,7 @@ def _time_steps(tio, _abi, cfg, head, ws, hidden, anchors, out, target, acc, bon
     stage_ms = {name: statistics.mean(ev_stage[s_][i].elapsed_time(ev_stage[s_][i + 1])
                                       for s_ in range(K))
                 for i, name in enumerate(_abi.STAGE_NAMES)}
-    return statistics.mean(step_ms), stage_ms, t_wall
+    return statistics.mean(step_ms), stage_ms, t_wall, window
 
 
 def run_ours(args):
@@ -358,8 +389,19 @@ def run_ours(args):
     clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     clocks.start()
-    ms, stage_ms, t_wall = _time_steps(tio, _abi, cfg, head, ws, *common, K, args.warmup, world)
-    clk = clocks.stop()
+    ms, stage_ms, t_wall, window = _time_steps(tio, _abi, cfg, head, ws, *common, K,
+                                               args.warmup, world)
+    clk = clocks.stop(window)
+    if clk and set(clk["reasons"]) & set(BAD_CLOCK_REASONS):
+        # a run the GPU throttled for heat or a hardware slowdown is no measurement:
+        # take it once more and report that one
+        first = clk["reasons"]
+        clocks.start()
+        ms, stage_ms, t_wall, window = _time_steps(tio, _abi, cfg, head, ws, *common, K,
+                                                   args.warmup, world)
+        clk = clocks.stop(window)
+        if clk:
+            clk["remeasured_after"] = first
     ms_max, value = job_throughput(ms, wl.B * wl.N, world, dev)
     slots = wl.B * wl.N * world
     launches = _abi.dspark_propose_kernel_count(cfg, head.struct(), out.struct()) + 1
@@ -367,7 +409,7 @@ def run_ours(args):
     # the other chain form on the same inputs, for reference
     other = None
     if head is not dense_head:
-        ms_o, stage_o, _ = _time_steps(tio, _abi, cfg, dense_head, ws_d, *common,
+        ms_o, stage_o, _, _ = _time_steps(tio, _abi, cfg, dense_head, ws_d, *common,
                                        max(3, K // 2), args.warmup, world)
         ms_o = _max_over_ranks(ms_o, world, dev)
         other = {"chain": "dense", "value": slots / (ms_o / 1e3), "ms_per_step": ms_o,
@@ -380,7 +422,7 @@ def run_ours(args):
     if head is not dense_head:
         cfg_a = _abi.dspark_config.from_buffer_copy(cfg)
         cfg_a.skip_truncated = 1
-        ms_a, stage_a, _ = _time_steps(tio, _abi, cfg_a, head, ws, *common, max(3, K // 2),
+        ms_a, stage_a, _, _ = _time_steps(tio, _abi, cfg_a, head, ws, *common, max(3, K // 2),
                                        args.warmup, world)
         ms_a = _max_over_ranks(ms_a, world, dev)
         drafted = int(out.n_draft.sum().item())
@@ -495,7 +537,7 @@ def e2e_host(cfg, head, wl, bt, target_dev, dev, stream, flush, K, W, world):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_8b_b32")

@@ -90,12 +90,29 @@ def test_reference_arm_runs_on_rank0_only():
 
 def test_parse_clocks_reports_median_and_reasons():
     rows = [
-        "0, 1900, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
-        "0, 2000, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active",
-        "0, 1950, 2070, 1350.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/01/02 10:00:00.100, 0, 1900, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/01/02 10:00:00.120, 0, 2000, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/01/02 10:00:00.140, 0, 1950, 2070, 1350.0, 0x4, Not Active, Not Active, Not Active, Active",
         "garbage line",
     ]
     c = bench.parse_clocks(rows)
-    assert c == {"sm_mhz": 1950, "sm_max_mhz": 2070, "samples": 3,
+    assert c == {"sm_mhz": 1950, "sm_max_mhz": 2070, "samples": 3, "window": "whole run",
                  "reasons": ["sw_power_cap"]}
     assert bench.parse_clocks([]) is None
+
+
+def test_parse_clocks_keeps_the_timed_window():
+    import datetime as dt
+    rows = [
+        "2026/01/02 10:00:00.000, 0, 1000, 2070, 100.0, 0x0, Active, Not Active, Not Active, Not Active",
+        "2026/01/02 10:00:00.500, 0, 2010, 2070, 1300.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/01/02 10:00:00.520, 0, 2030, 2070, 1300.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/01/02 10:00:01.500, 0, 1200, 2070, 300.0, 0x0, Not Active, Active, Not Active, Not Active",
+    ]
+    t = dt.datetime(2026, 1, 2, 10, 0, 0)
+    c = bench.parse_clocks(rows, (t + dt.timedelta(seconds=0.4), t + dt.timedelta(seconds=0.6)))
+    # the idle sample before and the slowed one after the window do not count
+    assert c == {"sm_mhz": 2020, "sm_max_mhz": 2070, "samples": 2, "window": "timed region",
+                 "reasons": []}
+    c = bench.parse_clocks(rows, (t + dt.timedelta(seconds=5), t + dt.timedelta(seconds=6)))
+    assert c["samples"] == 4 and c["window"].startswith("whole run")
