@@ -70,3 +70,12 @@ def test_adaptive_needs_the_pruned_chain():
     with pytest.raises(_abi.DSparkError) as e:
         gpu_propose(wl, hd, bt, chain="dense", skip_truncated=True)
     assert e.value.status == _abi.DSPARK_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name", ["qwen3_8b_b32", "qwen38_27b_b8", "gemma4_bonus_b64"])
+def test_adaptive_full_size(name):
+    # the shapes the benchmark times, with work stopped at each block's confidence cut
+    from workloads import WORKLOADS
+    wl = WORKLOADS[name]
+    g, o, rep = run_case(wl, chain="pruned", skip_truncated=True)
+    assert (g["n_draft"] < wl.N).any()
