@@ -31,6 +31,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -88,7 +89,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # raw samples; DSPARK_CLOCKS_DIR keeps them where the caller wants them
+        out_dir = os.environ.get("DSPARK_CLOCKS_DIR", tempfile.gettempdir())
+        self.path = os.path.join(out_dir, f"dspark_clocks_rank{index}.csv")
 
     def start(self, ready_timeout_s: float = 5.0):
         """Starts the sampler and returns once its first sample is written (or after
