@@ -27,6 +27,10 @@
  *     config's dtype for the tensors marked "dtype", int32 / fp32 otherwise.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream) unless stated otherwise.
+ *   - dspark_propose and dspark_verify can be captured into a CUDA graph (stream
+ *     capture) and replayed; a replay reads the buffers the captured call was given, so
+ *     refill them in place between replays.  Make one direct call on the device before
+ *     the first capture: it does the library's one-time per-device set-up.
  *   - Argument errors detectable on the host return before anything is launched and
  *     leave every output untouched.  Problems only the device can see (an anchor
  *     outside [0, V), a bounded wait that gave up) set a sticky error word in the
