@@ -109,6 +109,68 @@ MUTATIONS = {
 }
 
 
+def _chain_variant(ranked_from=None, vals_from=None, markov_at=None, prev_lag=0):
+    """greedy_chain with one planted slip: top-k ranked on the wrong logits, top-k values
+    read from the other logits than their ids, the Markov term only at some slots, or the
+    previous token taken `prev_lag` slots too early."""
+    def chain(z_b, w1, w2_f64, anchor, top_k=1, topk_markov=True):
+        N, V = z_b.shape
+        tok = np.empty(N, np.int64)
+        ids = np.empty((N, top_k), np.int64)
+        vals = np.empty((N, top_k))
+        zc = np.empty_like(z_b)
+        history = [int(anchor)]
+        for i in range(N):
+            prev = history[max(0, len(history) - 1 - prev_lag)]
+            if markov_at is None or markov_at(i):
+                zc[i] = O.corrected_logits(z_b[i], w1, w2_f64, prev)
+            else:
+                zc[i] = z_b[i]
+            tok[i] = O.argmax_lowest(zc[i])
+            use_markov = topk_markov if ranked_from is None else ranked_from(topk_markov)
+            ranked = zc[i] if use_markov else z_b[i]
+            ids[i] = O.topk_sorted(ranked, top_k)
+            src = ranked if vals_from is None else (z_b[i] if use_markov else zc[i])
+            vals[i] = src[ids[i]]
+            history.append(int(tok[i]))
+        return tok, ids, vals, zc
+    return chain
+
+
+def _truncate_last_below(c, m):
+    below = [i for i in range(len(c)) if m > 0 and c[i] < m]
+    return below[-1] if below else len(c)
+
+
+def _verify_counts_matches(draft, n_draft, target):
+    d, t = np.asarray(draft), np.asarray(target)
+    B, N = d.shape
+    a = np.array([int(np.sum(d[b, :n_draft[b]] == t[b, :n_draft[b]])) for b in range(B)])
+    bonus = np.array([t[b, a[b]] for b in range(B)])
+    e = np.full((B, N + 1), -1, np.int64)
+    for b in range(B):
+        e[b, :a[b]] = d[b, :a[b]]
+        e[b, a[b]] = bonus[b]
+    return a, bonus, e
+
+
+MUTATIONS.update({
+    "topk_markov_inverted": ("greedy_chain", _chain_variant(ranked_from=lambda tm: not tm)),
+    "topk_markov_always": ("greedy_chain", _chain_variant(ranked_from=lambda tm: True)),
+    "topk_vals_from_other_logits": ("greedy_chain", _chain_variant(vals_from=True)),
+    "markov_only_first_slot": ("greedy_chain", _chain_variant(markov_at=lambda i: i == 0)),
+    "markov_skips_first_slot": ("greedy_chain", _chain_variant(markov_at=lambda i: i > 0)),
+    "prev_one_slot_stale": ("greedy_chain", _chain_variant(prev_lag=1)),
+    "conf_slot_offset_dropped": ("confidence",
+                                 lambda h, w, b, ifp, N: _orig_conf(h, w, b, 0, N)),
+    "base_slot_offset_dropped": ("base_logits",
+                                 lambda h, W, bias, ifp, N, chunk=8192:
+                                 _orig_base(h, W, bias, 0, N, chunk)),
+    "truncate_at_last_below": ("truncation_length", _truncate_last_below),
+    "verify_counts_matches": ("verify", _verify_counts_matches),
+})
+
+
 @contextlib.contextmanager
 def _planted(name, fn):
     old = getattr(O, name)
