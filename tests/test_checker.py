@@ -157,3 +157,51 @@ def test_adaptive_block_length_passes_and_flags():
         bad = {k: v.copy() for k, v in g.items()}
         bad["draft"][b, cut - 1] = -1               # a slot before the cut left blank
         assert check.check_propose(o, gpu=bad, skip_truncated=True, **kw)["failures"]
+
+
+def test_topk_values_alone_flagged():
+    # ids right, one value off by more than the tolerance
+    o, gpu, kw = _case()
+    gpu["topk_vals"][1, 0, 2] += np.float32(0.05)
+    assert check.check_propose(o, gpu=gpu, **kw)["failures"]
+    o, gpu, kw = _case()
+    gpu["topk_vals"][1, 0, 2] += np.float32(0.005)        # within tolerance
+    assert check.check_propose(o, gpu=gpu, **kw)["failures"] == []
+
+
+def test_invalid_topk_ids_flagged():
+    for bad in ("duplicate", "negative", "too_large"):
+        o, gpu, kw = _case()
+        ids = gpu["topk_ids"][2, 4]
+        if bad == "duplicate":
+            ids[2] = ids[0]
+        elif bad == "negative":
+            ids[1] = -1
+        else:
+            ids[0] = 200
+        rep = check.check_propose(o, gpu=gpu, **kw)
+        assert any("invalid" in f for f in rep["failures"]), bad
+
+
+def test_draft_out_of_range_flagged():
+    o, gpu, kw = _case()
+    gpu["draft"][0, 3] = 200
+    assert any("out of range" in f for f in check.check_propose(o, gpu=gpu, **kw)["failures"])
+
+
+def test_verify_emitted_flagged():
+    rng = np.random.default_rng(5)
+    draft = rng.integers(0, 9, (4, 5))
+    n_draft = np.array([5, 3, 0, 5])
+    target = draft.copy()
+    target = np.concatenate([target, rng.integers(0, 9, (4, 1))], axis=1)
+    target[3, 2] = (target[3, 2] + 1) % 9
+    from oracle import verify
+    a, b, e = verify(draft, n_draft, target)
+    assert check.check_verify(draft, n_draft, target, a, b, e) == []
+    e2 = e.copy()
+    e2[0, 0] = (e2[0, 0] + 1) % 9
+    assert check.check_verify(draft, n_draft, target, a, b, e2)
+    b2 = b.copy()
+    b2[1] = (b2[1] + 1) % 9
+    assert check.check_verify(draft, n_draft, target, a, b2, e)
