@@ -145,3 +145,79 @@ def test_wait_selftest_checked_before_launch(lib):
     assert ds.dspark_wait_selftest(0x10000, 256, 0) == I
     assert ds.dspark_wait_selftest(0x10000, 256, 2_000_000_001) == I
     assert ds.dspark_wait_selftest(0x10000, 256, 1000, pre_abort=2) == I
+
+
+def test_step_host_checked_before_launch(lib):
+    cfg, head = _cfg(), _head()
+    need = ds._abi.dspark_step_host_workspace_size(cfg, head)
+    # the staging area comes on top of the proposal's workspace
+    assert need > ds.dspark_propose_workspace_size(cfg, head)
+    assert ds._abi.dspark_step_host_workspace_size(_cfg(B=0), head) == 0
+    bufs = [0x1000 * (i + 1) for i in range(7)]          # hidden .. bonus (host)
+    for i in range(7):                                   # each required buffer
+        b = list(bufs)
+        b[i] = None
+        st = ds._abi.dspark_step_host(cfg, head, *b, None, None, 0x100000, need, 0)
+        assert st == _abi.DSPARK_ERR_INVALID_ARG, i
+    st = ds._abi.dspark_step_host(cfg, head, *bufs, None, None, 0x100000, need - 1, 0)
+    assert st == _abi.DSPARK_ERR_WORKSPACE
+    st = ds._abi.dspark_step_host(cfg, head, *bufs, None, None, 0x100010, need, 0)
+    assert st == _abi.DSPARK_ERR_WORKSPACE
+
+
+def test_prepare_head_checked_before_launch(lib):
+    bf16 = _cfg(dtype=1)
+    head = _head()
+    need = ds._abi.dspark_prepare_head_size(bf16, head)
+    assert need > 0 and need % 256 == 0
+    # the prepared head holds markov_w2 transposed (bf16, padded rows), column norms etc.
+    assert need >= 2 * 8 * 1000
+    assert ds._abi.dspark_prepare_head_size(_cfg(), head) == 0          # fp32: not used
+    assert ds._abi.dspark_prepare_head(_cfg(), head, 0x100000, need, 0) == \
+        _abi.DSPARK_ERR_UNSUPPORTED
+    assert ds._abi.dspark_prepare_head(bf16, head, None, need, 0) == _abi.DSPARK_ERR_WORKSPACE
+    assert ds._abi.dspark_prepare_head(bf16, head, 0x100010, need, 0) == \
+        _abi.DSPARK_ERR_WORKSPACE
+    assert ds._abi.dspark_prepare_head(bf16, head, 0x100000, need - 1, 0) == \
+        _abi.DSPARK_ERR_WORKSPACE
+    assert ds._abi.dspark_prepare_head(_cfg(dtype=1, B=0), head, 0x100000, need, 0) == \
+        _abi.DSPARK_ERR_INVALID_ARG
+
+
+def test_timed_and_kernel_count_checked(lib):
+    cfg, head = _cfg(), _head()
+    out = _abi.dspark_outputs(draft=0x100, n_draft=0x200)
+    need = ds.dspark_propose_workspace_size(cfg, head)
+    n = _abi.DSPARK_NUM_STAGES + 1
+    st = ds._abi.dspark_propose_timed(cfg, head, 0x4000, 0x5000, out, 0x10000, need, 0,
+                                      [0x10] * (n - 1) + [None])
+    assert st == _abi.DSPARK_ERR_INVALID_ARG                # an event is NULL
+    st = ds._abi.dspark_propose_timed(cfg, head, 0x4000, 0x5000, out, 0x10000, need - 1, 0,
+                                      [0x10] * n)
+    assert st == _abi.DSPARK_ERR_WORKSPACE
+    # launches per pass: confidence, GEMM and two per slot on the fp32 path
+    assert ds._abi.dspark_propose_kernel_count(cfg, head, out) == 2 + 2 * 4
+    # bf16, no prepared head: confidence, GEMM, one chain launch per 32 blocks, top-k
+    bf = _cfg(dtype=1, B=70)
+    topk = _abi.dspark_outputs(draft=0x100, n_draft=0x200, topk_ids=0x300, topk_vals=0x400)
+    assert ds._abi.dspark_propose_kernel_count(bf, head, topk) == 1 + 1 + 3 + 1
+    assert ds._abi.dspark_propose_kernel_count(bf, head, out) == 1 + 1 + 3
+    # a prepared head: the GEMM and the tables with the walk; the confidence kernel first
+    # when the block length is adaptive
+    prep = _head(prepared=0x9000)
+    assert ds._abi.dspark_propose_kernel_count(bf, prep, topk) == 2
+    assert ds._abi.dspark_propose_kernel_count(_cfg(dtype=1, B=70, skip_truncated=1), prep,
+                                               topk) == 3
+    assert ds._abi.dspark_propose_kernel_count(_cfg(B=0), head, out) == -1
+
+
+def test_noalloc_checked_before_launch(lib):
+    out = _abi.dspark_outputs(draft=0x100, n_draft=0x200)
+    # an invalid configuration answers as dspark_propose would
+    st = ds._abi.dspark_propose_noalloc(_cfg(B=0), _head(), 0x4000, 0x5000, out, 0)
+    assert st == _abi.DSPARK_ERR_INVALID_ARG
+    # a call whose scratch would exceed 16 MiB is refused on the host
+    big = _cfg(B=64, L_in=16, V=100000)
+    st = ds._abi.dspark_propose_noalloc(big, _head(V_head=100000), 0x4000, 0x5000, out, 0)
+    assert st == _abi.DSPARK_ERR_WORKSPACE
+    assert "16777216" in ds.dspark_last_error()
