@@ -224,21 +224,27 @@ def _cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(wl, hd, bt, budget_s=20.0, blocks=4):
-    """Time the oracle as it stands on a bounded sample; returns the JSON object."""
+def cpu_baseline(wl, hd, bt, budget_s=20.0, blocks=4, min_work_s=10.0, min_passes=3):
+    """Time the oracle as it stands on a bounded sample; returns the JSON object.
+
+    Passes repeat until at least ``min_work_s`` of oracle work (and ``min_passes``
+    passes) is timed, and stop before a further pass would run past ``budget_s``."""
+    blocks = min(blocks, wl.B)
     times = []
     t_end = time.time() + budget_s
     while True:
         t0 = time.perf_counter()
         oracle_pass(wl, hd, bt, blocks)
         times.append(time.perf_counter() - t0)
-        if time.time() + times[-1] > t_end or len(times) >= 5:
+        if time.time() + times[-1] > t_end:
+            break
+        if len(times) >= min_passes and sum(times) >= min_work_s:
             break
     t = statistics.median(times)
     return {"value": blocks * wl.N / t, "unit": UNIT, "cores": _cores(), "kind": "oracle",
             "sample": f"{blocks} of {wl.B} blocks x {wl.N} slots, full vocabulary "
                       f"(V={wl.V}), propose + verify, float64 NumPy; median of "
-                      f"{len(times)} passes ({t:.2f} s each)"}
+                      f"{len(times)} passes ({t:.2f} s each, {sum(times):.1f} s in all)"}
 
 
 def run_reference(args):
