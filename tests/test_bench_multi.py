@@ -116,3 +116,11 @@ def test_parse_clocks_keeps_the_timed_window():
                  "reasons": []}
     c = bench.parse_clocks(rows, (t + dt.timedelta(seconds=5), t + dt.timedelta(seconds=6)))
     assert c["samples"] == 4 and c["window"].startswith("whole run")
+
+
+def test_cpu_baseline_sample_within_the_batch():
+    from workloads import WORKLOADS, make_batch, make_head
+    wl = WORKLOADS["tiny_fp32"]                        # a batch of 2 blocks
+    c = bench.cpu_baseline(wl, make_head(wl), make_batch(wl), budget_s=2.0, min_work_s=0.3)
+    assert c["sample"].startswith("2 of 2 blocks")
+    assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0
