@@ -117,7 +117,8 @@ typedef struct dspark_head {
 /* Outputs of dspark_propose (device memory).  N = dspark_num_slots(cfg). */
 typedef struct dspark_outputs {
   int32_t* draft;             /* required [B, N]: the greedy chain's tokens; all N slots
-                                 are filled, truncation only sets n_draft */
+                                 are filled and truncation only sets n_draft, except
+                                 with skip_truncated = 1 (-1 from n_draft[b] on) */
   int32_t* n_draft;           /* required [B]: truncated draft length, 0..N */
   int32_t* topk_ids;          /* [B, N, top_k] token ids by value descending, ties to
                                  the lower id; or NULL */
