@@ -105,8 +105,9 @@ def pin_hand_verify():
 
 
 # ------------------------------------------------------------------- brute force
-def _brute_force_propose(hidden, anchors, W, w1, w2, bias, L_in, sfa, k):
-    """The proposal written with explicit loops and a materialised V x V bigram table."""
+def _brute_force_propose(hidden, anchors, W, w1, w2, bias, L_in, sfa, k, topk_markov=True):
+    """The proposal written with explicit loops and a materialised V x V bigram table.
+    With topk_markov False the top-k ranks the base logits instead of the corrected ones."""
     h = O.upcast(hidden)
     W = O.upcast(W)
     w1 = O.upcast(w1)
@@ -121,21 +122,23 @@ def _brute_force_propose(hidden, anchors, W, w1, w2, bias, L_in, sfa, k):
     for b in range(B):
         prev = int(anchors[b])
         for i in range(N):
-            row = []
+            row, base = [], []
             for v in range(V):
                 s = 0.0
                 for c in range(H):
                     s += h[b][ifp + i][c] * W[v][c]
                 if bias is not None:
                     s += float(bias[v])
+                base.append(s)
                 row.append(s + T[prev][v])
             best = 0
             for v in range(1, V):
                 if row[v] > row[best]:
                     best = v
-            order = sorted(range(V), key=lambda v: (-row[v], v))[:k]
+            ranked = row if topk_markov else base
+            order = sorted(range(V), key=lambda v: (-ranked[v], v))[:k]
             draft[b][i] = best
-            topk[b][i] = (order, [row[v] for v in order])
+            topk[b][i] = (order, [ranked[v] for v in order])
             prev = best
     return draft, topk
 
@@ -403,6 +406,89 @@ def pin_bonus_slot_unused():
     assert not np.array_equal(o1["draft"][:, 0], o3["draft"][:, 0])
 
 
+# ------------------------------------------------------------------- random sweep
+def sweep_case(seed):
+    """A random tiny configuration with small-integer weights and hidden states: every
+    logit is exact in float64 and exact ties are common, so the tie rules get exercised.
+    Covers both layouts, both top-k sources, masked rows and the confidence threshold
+    (sometimes exactly equal to a slot's confidence)."""
+    rng = np.random.default_rng(10_000 + seed)
+    sfa = bool(rng.integers(0, 2))
+    B = int(rng.integers(1, 3))
+    L_in = int(rng.integers(1 if sfa else 2, 5))
+    H = int(rng.integers(1, 4))
+    V = int(rng.integers(2, 10))
+    r = int(rng.integers(1, 4))
+
+    def ints(*shape):
+        return rng.integers(-2, 3, size=shape).astype(np.float32)
+
+    hidden, W = ints(B, L_in, H), ints(V, H)
+    w1, w2 = ints(V, r), ints(r, V)
+    bias = None
+    if rng.integers(0, 2):
+        bias = np.zeros(V, np.float32)
+        masked = rng.choice(V, size=int(rng.integers(0, V // 2 + 1)), replace=False)
+        bias[masked] = np.float32(-1e9)
+    n_emit = V if bias is None else int(np.sum(bias > -1e8))
+    k = int(rng.integers(1, n_emit + 1))
+    anchors = rng.integers(0, V, size=B)
+    w_conf = ints(H)
+    b_conf = float(rng.integers(-1, 2))
+    conf_min = [0.0, 0.5, 1.0 / (1.0 + math.exp(-1.0)), 0.9][int(rng.integers(0, 4))]
+    topk_markov = bool(rng.integers(0, 2))
+    return dict(sfa=sfa, B=B, L_in=L_in, V=V, hidden=hidden, W=W, w1=w1, w2=w2, bias=bias,
+                k=k, anchors=anchors, w_conf=w_conf, b_conf=b_conf, conf_min=conf_min,
+                topk_markov=topk_markov)
+
+
+def brute_force_confidence(hidden, w_conf, b_conf, ifp, N, conf_min):
+    """Per-slot sigmoid confidence and the first slot strictly below conf_min, in loops."""
+    B, _, H = hidden.shape
+    conf = [[0.0] * N for _ in range(B)]
+    n_draft = []
+    for b in range(B):
+        for i in range(N):
+            x = sum(float(hidden[b, ifp + i, c]) * float(w_conf[c]) for c in range(H))
+            conf[b][i] = 1.0 / (1.0 + math.exp(-(x + b_conf)))
+        cut = N
+        if conf_min > 0:
+            for i in range(N):
+                if conf[b][i] < conf_min:
+                    cut = i
+                    break
+        n_draft.append(cut)
+    return conf, n_draft
+
+
+def check_sweep_case(seed):
+    c = sweep_case(seed)
+    o = O.propose(c["hidden"], c["anchors"], c["W"], c["w1"], c["w2"], L_in=c["L_in"],
+                  sample_from_anchor=c["sfa"], top_k=c["k"], conf_min=c["conf_min"],
+                  lm_bias=c["bias"], w_conf=c["w_conf"], b_conf=c["b_conf"],
+                  topk_markov=c["topk_markov"])
+    d, tk = _brute_force_propose(c["hidden"], c["anchors"], c["W"], c["w1"], c["w2"],
+                                 c["bias"], c["L_in"], c["sfa"], c["k"], c["topk_markov"])
+    ifp = 0 if c["sfa"] else 1
+    N = c["L_in"] - ifp
+    assert o["draft"].tolist() == d, (seed, o["draft"], d)
+    for b in range(c["B"]):
+        for i in range(N):
+            assert o["topk_ids"][b, i].tolist() == tk[b][i][0], (seed, b, i)
+            assert o["topk_vals"][b, i].tolist() == tk[b][i][1], (seed, b, i)
+            if c["bias"] is not None:
+                assert c["bias"][o["draft"][b, i]] > -1e8, (seed, b, i)
+    conf, n_draft = brute_force_confidence(c["hidden"], c["w_conf"], c["b_conf"], ifp, N,
+                                           c["conf_min"])
+    assert np.allclose(o["conf"], conf, rtol=0, atol=1e-15), seed
+    assert o["n_draft"].tolist() == n_draft, (seed, o["n_draft"], n_draft)
+
+
+def pin_brute_force_sweep():
+    for seed in range(40):
+        check_sweep_case(seed)
+
+
 ALL_PINS = [
     pin_hand_anchor_first, pin_hand_topk_base, pin_hand_plain_argmax,
     pin_hand_bonus_anchor, pin_hand_masked_row, pin_hand_verify,
@@ -410,5 +496,5 @@ ALL_PINS = [
     pin_chain_consistency, pin_single_slot, pin_masked_rows_never_emitted,
     pin_confidence_closed_forms, pin_truncation_positions, pin_verify_brute_force,
     pin_verify_planted_mismatch, pin_bf16_upcast, pin_bonus_slot_unused,
-    pin_adaptive_block_length,
+    pin_adaptive_block_length, pin_brute_force_sweep,
 ]
