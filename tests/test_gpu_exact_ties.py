@@ -1,0 +1,61 @@
+"""Bit-exact parity with ties: small-integer weights and hidden states make every product
+and sum exact in bf16 operands with fp32 accumulation, so the GPU's corrected logits are
+the oracle's exactly.  Drafts, top-k ids and top-k values must then equal the oracle's
+with no tolerance, including the lowest-id rule wherever values tie."""
+import numpy as np
+import pytest
+
+from oracle import propose as oracle_propose
+from workloads import Workload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from gpu_cases import gpu_propose  # noqa: E402
+
+
+def _bf16_bits(a):
+    # small integers have no low mantissa bits, so the bf16 pattern is exact
+    return (np.ascontiguousarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _integer_case(seed, B, L_in, sfa, topk_markov, H=64, V=1024, r=8, k=4):
+    rng = np.random.default_rng(seed)
+
+    def ints(*shape):
+        return rng.integers(-2, 3, size=shape).astype(np.float32)
+
+    wl = Workload("int_ties", B=B, L_in=L_in, H=H, V=V, r=r, top_k=k, sample_from_anchor=sfa,
+                  conf_min=0.0, dtype="bf16", weight_std=1.0, conf_std=1.0,
+                  topk_markov=topk_markov, seed=seed)
+    hd = dict(lm_head=_bf16_bits(ints(V, H)), markov_w1=_bf16_bits(ints(V, r)),
+              markov_w2=_bf16_bits(ints(r, V)), w_conf=None, b_conf=0.0, lm_bias=None,
+              emit_rows=None)
+    bt = dict(hidden=_bf16_bits(ints(B, L_in, H)),
+              anchors=rng.integers(0, V, size=B).astype(np.int32))
+    return wl, hd, bt
+
+
+@pytest.mark.parametrize("chain,B,L_in,sfa,topk_markov", [
+    ("pruned", 32, 8, True, True),      # pair tiles of 256 prediction rows
+    ("dense", 32, 8, True, True),
+    ("pruned", 16, 5, False, True),     # 1+N layout
+    ("dense", 16, 5, False, False),     # top-k over the base logits
+    ("pruned", 8, 4, True, False),
+])
+def test_integer_logits_bit_exact(chain, B, L_in, sfa, topk_markov):
+    wl, hd, bt = _integer_case(4242 + B + L_in, B, L_in, sfa, topk_markov)
+    g, _ = gpu_propose(wl, hd, bt, chain=chain)
+    o = oracle_propose(bt["hidden"], bt["anchors"], hd["lm_head"], hd["markov_w1"],
+                       hd["markov_w2"], L_in=wl.L_in, sample_from_anchor=sfa,
+                       top_k=wl.top_k, conf_min=0.0, topk_markov=topk_markov)
+    # the case must actually contain ties for the rule to be tested
+    zc_rows = o["topk_vals"].reshape(-1, wl.top_k)
+    assert np.any(zc_rows[:, :-1] == zc_rows[:, 1:])
+    assert np.array_equal(g["draft"], o["draft"])
+    assert np.array_equal(g["topk_ids"], o["topk_ids"])
+    assert np.array_equal(g["topk_vals"].astype(np.float64), o["topk_vals"])
+    assert (g["n_draft"] == wl.N).all()
