@@ -59,3 +59,40 @@ def test_integer_logits_bit_exact(chain, B, L_in, sfa, topk_markov):
     assert np.array_equal(g["topk_ids"], o["topk_ids"])
     assert np.array_equal(g["topk_vals"].astype(np.float64), o["topk_vals"])
     assert (g["n_draft"] == wl.N).all()
+
+
+def _ternary_bits(rng, shape, p_nonzero):
+    """bf16 bit patterns of values in {-1, 0, 1}, each nonzero with p_nonzero (split
+    evenly between the signs)."""
+    u = rng.random(shape, dtype=np.float32)
+    bits = np.zeros(shape, np.uint16)
+    bits[u < p_nonzero / 2] = 0x3F80                          # +1.0
+    bits[(u >= p_nonzero / 2) & (u < p_nonzero)] = 0xBF80     # -1.0
+    return bits
+
+
+def test_integer_logits_bit_exact_full_size():
+    # the Qwen3-8B-shaped head at B=32 that the benchmark times, through both chains:
+    # |z| <= H = 4096 and |Markov term| <= r = 256 stay exact in fp32; sparse Markov
+    # weights keep the pruning bound as tight as on the benchmark's inputs
+    B, L_in, H, V, r, k = 32, 16, 4096, 151936, 256, 8
+    rng = np.random.default_rng(777)
+    wl = Workload("int_ties_full", B=B, L_in=L_in, H=H, V=V, r=r, top_k=k,
+                  sample_from_anchor=True, conf_min=0.0, dtype="bf16", weight_std=1.0,
+                  conf_std=1.0, seed=777)
+    hd = dict(lm_head=_ternary_bits(rng, (V, H), 0.5),
+              markov_w1=_ternary_bits(rng, (V, r), 0.05),
+              markov_w2=_ternary_bits(rng, (r, V), 0.05), w_conf=None, b_conf=0.0,
+              lm_bias=None, emit_rows=None)
+    bt = dict(hidden=_ternary_bits(rng, (B, L_in, H), 0.5),
+              anchors=rng.integers(0, V, size=B).astype(np.int32))
+    o = oracle_propose(bt["hidden"], bt["anchors"], hd["lm_head"], hd["markov_w1"],
+                       hd["markov_w2"], L_in=L_in, sample_from_anchor=True, top_k=k,
+                       conf_min=0.0)
+    vals = o["topk_vals"].reshape(-1, k)
+    assert np.any(vals[:, :-1] == vals[:, 1:])
+    for chain in ("pruned", "dense"):
+        g, _ = gpu_propose(wl, hd, bt, chain=chain)
+        assert np.array_equal(g["draft"], o["draft"]), chain
+        assert np.array_equal(g["topk_ids"], o["topk_ids"]), chain
+        assert np.array_equal(g["topk_vals"].astype(np.float64), o["topk_vals"]), chain
