@@ -96,3 +96,42 @@ def test_integer_logits_bit_exact_full_size():
         assert np.array_equal(g["draft"], o["draft"]), chain
         assert np.array_equal(g["topk_ids"], o["topk_ids"]), chain
         assert np.array_equal(g["topk_vals"].astype(np.float64), o["topk_vals"]), chain
+
+
+@pytest.mark.parametrize("name", ["qwen38_27b_b8", "gemma4_bonus_b64"])
+def test_integer_logits_bit_exact_other_full_sizes(name):
+    # the other large shapes: a 5120-wide head over 248320 rows at B=8, and the 1+N layout
+    # over 262144 rows of which 32768 are emittable (both reduced-vocabulary forms)
+    from workloads import WORKLOADS
+    base = WORKLOADS[name]
+    wl = Workload("int_" + name, B=base.B, L_in=base.L_in, H=base.H, V=base.V, r=base.r,
+                  top_k=base.top_k, sample_from_anchor=base.sample_from_anchor,
+                  conf_min=0.0, dtype="bf16", weight_std=1.0, conf_std=1.0,
+                  n_emit=base.n_emit, seed=778)
+    rng = np.random.default_rng(778)
+    hd = dict(lm_head=_ternary_bits(rng, (wl.V, wl.H), 0.5),
+              markov_w1=_ternary_bits(rng, (wl.V, wl.r), 0.05),
+              markov_w2=_ternary_bits(rng, (wl.r, wl.V), 0.05), w_conf=None, b_conf=0.0,
+              lm_bias=None, emit_rows=None)
+    forms = ["full"]
+    if wl.n_emit:
+        emit = np.sort(rng.choice(wl.V, size=wl.n_emit, replace=False)).astype(np.int32)
+        hd["lm_bias"] = np.full(wl.V, -1e9, np.float32)
+        hd["lm_bias"][emit] = 0.0
+        hd["emit_rows"] = emit
+        forms.append("d2t")
+    bt = dict(hidden=_ternary_bits(rng, (wl.B, wl.L_in, wl.H), 0.5),
+              anchors=rng.integers(0, wl.V, size=wl.B).astype(np.int32))
+    o = oracle_propose(bt["hidden"], bt["anchors"], hd["lm_head"], hd["markov_w1"],
+                       hd["markov_w2"], L_in=wl.L_in, sample_from_anchor=wl.sample_from_anchor,
+                       top_k=wl.top_k, conf_min=0.0, lm_bias=hd["lm_bias"])
+    if wl.top_k > 1:
+        vals = o["topk_vals"].reshape(-1, wl.top_k)
+        assert np.any(vals[:, :-1] == vals[:, 1:])
+    for form in forms:
+        for chain in ("pruned", "dense"):
+            g, _ = gpu_propose(wl, hd, bt, form, chain=chain)
+            assert np.array_equal(g["draft"], o["draft"]), (form, chain)
+            assert np.array_equal(g["topk_ids"], o["topk_ids"]), (form, chain)
+            assert np.array_equal(g["topk_vals"].astype(np.float64), o["topk_vals"]), \
+                (form, chain)
