@@ -79,3 +79,12 @@ def test_adaptive_full_size(name):
     wl = WORKLOADS[name]
     g, o, rep = run_case(wl, chain="pruned", skip_truncated=True)
     assert (g["n_draft"] < wl.N).any()
+
+
+def test_adaptive_every_block_cut_at_slot_zero():
+    # every confidence is ~0: no block drafts anything, so the GEMM has no live N-tile
+    # and no table CTA works; the walk still writes -1 / NaN everywhere
+    g, o, rep = run_case(_wl(b_conf=-50.0), chain="pruned", skip_truncated=True)
+    assert (g["n_draft"] == 0).all()
+    assert (g["draft"] == -1).all() and (g["topk_ids"] == -1).all()
+    assert np.isnan(g["topk_vals"]).all()
