@@ -43,7 +43,11 @@ MASK_BIAS_LIMIT = -1e8
 
 
 def upcast(a) -> np.ndarray:
-    """Exact float64 copy of an fp32 array or of a bf16 array given as uint16 bits."""
+    """Exact float64 copy of an fp32 array or of a bf16 array given as uint16 bits.
+
+    Not a step of the method: bf16 is the upper half of an fp32, so widening it (and
+    fp32 to float64) loses nothing, and the oracle computes from the very values the
+    GPU reads."""
     a = np.asarray(a)
     if a.dtype == np.uint16:
         return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
@@ -117,7 +121,10 @@ def corrected_logits(z_row: np.ndarray, w1, w2_f64: np.ndarray, prev) -> np.ndar
 
 
 def argmax_lowest(row: np.ndarray) -> int:
-    """Index of the largest value; among equal maxima the lowest index."""
+    """Index of the largest value; among equal maxima the lowest index.
+
+    [dflash-log], the proposal formula: prev(i > 0) = argmax logits'(i - 1).  The pages
+    do not say how ties break; the reading taken is the lowest token id."""
     m = row.max()
     return int(np.flatnonzero(row == m)[0])
 
@@ -199,7 +206,12 @@ def greedy_chain(z_b: np.ndarray, w1, w2_f64: np.ndarray, anchor: int,
 
 def blank_past_cut(draft, tk_ids, tk_vals, n_draft) -> None:
     """Adaptive block length: the slots of block b from n_draft[b] on are not drafted
-    (draft and top-k ids -1, top-k values NaN), in place."""
+    (draft and top-k ids -1, top-k values NaN), in place.
+
+    [dflash-log], "spec: add confidence-based draft pruning for DSpark": a block is cut
+    at its first slot below the threshold and verify reads nothing past the cut.  The
+    adaptive mode (a reading: the pages leave the wiring open) therefore drafts nothing
+    there, and -1 / NaN mark the undrafted slots."""
     for b in range(draft.shape[0]):
         cut = int(n_draft[b])
         draft[b, cut:] = -1
