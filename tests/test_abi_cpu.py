@@ -221,3 +221,25 @@ def test_noalloc_checked_before_launch(lib):
     st = ds._abi.dspark_propose_noalloc(big, _head(V_head=100000), 0x4000, 0x5000, out, 0)
     assert st == _abi.DSPARK_ERR_WORKSPACE
     assert "16777216" in ds.dspark_last_error()
+
+
+def test_header_is_plain_c():
+    # the boundary is a C ABI: the header must compile as strict C99 with no CUDA or C++
+    # types, and a C caller must be able to name every entry point (source through stdin,
+    # object to /dev/null: nothing is written)
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    names = _declared_functions()
+    src = ['#include "dspark.h"', "typedef void (*any_fn)(void);", "int main(void) {",
+           "  dspark_config c = {0}; dspark_head h = {0}; dspark_outputs o = {0};",
+           "  any_fn f;", "  (void)c; (void)h; (void)o;"]
+    src += [f"  f = (any_fn)&{n}; (void)f;" for n in names]
+    src += ["  return DSPARK_OK + DSPARK_NUM_STAGES * 0;", "}"]
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), "-x", "c", "-c", "-",
+                        "-o", os.devnull], input="\n".join(src) + "\n",
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
