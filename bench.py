@@ -444,6 +444,10 @@ def run_ours(args):
     # end to end through the host-buffer entry point (copies inside the timed region)
     e2e = e2e_host(cfg, head, wl, bt, target, dev, stream, flush, K, args.warmup, world)
 
+    # dspark_verify alone, back to back on this GPU (an extra; never the headline)
+    verify_only = _verify_only(tio, out, target, acc, bonus, emitted, stream, K,
+                               args.warmup, wl.B)
+
     peaks = _peaks()
     alg = _algorithmic(wl, head.V_head)
     gemm_ms = stage_ms["logits"]
@@ -486,6 +490,7 @@ def run_ours(args):
         "gpu_launches": K * launches,
         "other_chain": other,
         "adaptive": adaptive,
+        "verify_only": verify_only,
         "clocks": clk,
         "wall_s_timed_region": t_wall,
     }
@@ -497,6 +502,28 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def _verify_only(tio, out, target, acc, bonus, emitted, stream, K, W, B):
+    """Device time of dspark_verify alone (K calls back to back after W warm-up calls, on
+    the proposal's draft): per call and as verified blocks/s of this GPU.  Any failure
+    leaves the extra out (None) instead of ending the benchmark."""
+    import torch
+    try:
+        for _ in range(W):
+            tio.verify(out.draft, out.n_draft, target, acc, bonus, emitted, stream)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            tio.verify(out.draft, out.n_draft, target, acc, bonus, emitted, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / K
+        return {"us_per_call": us, "blocks_per_s": B / (us * 1e-6), "calls": K}
+    except Exception as exc:  # an extra: report why it is missing, keep the line
+        return {"unavailable": f"{type(exc).__name__}: {exc}"}
 
 
 def e2e_host(cfg, head, wl, bt, target_dev, dev, stream, flush, K, W, world):

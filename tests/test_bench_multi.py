@@ -124,3 +124,34 @@ def test_cpu_baseline_sample_within_the_batch():
     c = bench.cpu_baseline(wl, make_head(wl), make_batch(wl), budget_s=2.0, min_work_s=0.3)
     assert c["sample"].startswith("2 of 2 blocks")
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0
+
+
+def test_verify_only_timing_arithmetic(monkeypatch):
+    import types
+
+    import torch
+
+    class Event:                       # 2 ms between the two records
+        def __init__(self, enable_timing=True):
+            pass
+
+        def record(self, stream=None):
+            pass
+
+        def elapsed_time(self, other):
+            return 2.0
+
+    monkeypatch.setattr(torch.cuda, "Event", Event)
+    monkeypatch.setattr(torch.cuda, "synchronize", lambda *a, **k: None)
+    calls = []
+    tio = types.SimpleNamespace(verify=lambda *a: calls.append(a))
+    out = types.SimpleNamespace(draft="d", n_draft="n")
+    r = bench._verify_only(tio, out, "t", "a", "b", None, None, K=10, W=3, B=32)
+    assert len(calls) == 13 and calls[0][:2] == ("d", "n")
+    assert r == {"us_per_call": 200.0, "blocks_per_s": 32 / 200e-6, "calls": 10}
+
+    def broken(*a):
+        raise RuntimeError("no device")
+    r = bench._verify_only(types.SimpleNamespace(verify=broken), out, "t", "a", "b", None,
+                           None, K=10, W=3, B=32)
+    assert r == {"unavailable": "RuntimeError: no device"}
