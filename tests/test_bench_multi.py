@@ -155,3 +155,21 @@ def test_verify_only_timing_arithmetic(monkeypatch):
     r = bench._verify_only(types.SimpleNamespace(verify=broken), out, "t", "a", "b", None,
                            None, K=10, W=3, B=32)
     assert r == {"unavailable": "RuntimeError: no device"}
+
+
+@pytest.mark.parametrize("name,v_head,mbytes,gflops", [
+    ("qwen3_8b_b1", 151936, 1322.6, 21.2),
+    ("qwen3_8b_b32", 151936, 1327.0, 677.1),
+    ("qwen38_27b_b8", 248320, 2671.3, 341.8),
+    ("gemma4_bonus_b64", 32768, 196.3, 74.1),    # the 32768 emittable rows only
+])
+def test_algorithmic_work_per_pass(name, v_head, mbytes, gflops):
+    # the roofline's numerator: bytes and flops the method must touch per pass, against
+    # figures worked out separately from the same definition (lm_head rows needed, the
+    # markov_w2 columns needed, gathered markov_w1 rows, hidden, w_conf, outputs and
+    # verify I/O; 2·M·H·V_e + 2·M·r·V_e + 2·M·H flops)
+    from workloads import WORKLOADS
+    a = bench._algorithmic(WORKLOADS[name], v_head)
+    assert a["bytes"] / 1e6 == pytest.approx(mbytes, rel=5e-3)
+    assert a["flops"] / 1e9 == pytest.approx(gflops, rel=5e-3)
+    assert a["gemm_flops"] == 2.0 * WORKLOADS[name].M * WORKLOADS[name].H * v_head
