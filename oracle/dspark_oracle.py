@@ -25,7 +25,12 @@ Readings taken where the pages are silent (each is also listed in the design not
     conf_min <= 0 disables it; confidence is per slot, not a running product;
   * in the 1+N layout, the first prediction slot's previous token is the anchor;
   * top-k candidates of every slot take the Markov term of the chain's own previous
-    token (the greedy path), as the chain's argmax does.
+    token (the greedy path), as the chain's argmax does;
+  * the candidate tree that tree verify walks is the whole top-k lattice: every
+    candidate of slot i is a child of every candidate of slot i - 1, down to the
+    truncated draft length;
+  * a separate confidence input (conf_hidden), when given, replaces the hidden states
+    in the confidence head only, slot for slot.
 """
 from __future__ import annotations
 
@@ -34,7 +39,7 @@ import numpy as np
 __all__ = [
     "upcast", "block_layout", "base_logits", "markov_bias", "corrected_logits",
     "confidence", "truncation_length", "topk_sorted", "argmax_lowest",
-    "greedy_chain", "propose", "verify", "MASK_BIAS_LIMIT",
+    "greedy_chain", "propose", "verify", "tree_verify", "MASK_BIAS_LIMIT",
 ]
 
 # A bias at or below this value marks a row the reduced-vocabulary draft cannot emit
@@ -59,8 +64,9 @@ def upcast(a) -> np.ndarray:
 def block_layout(L_in: int, sample_from_anchor: bool) -> tuple[int, int]:
     """(N, i_first_pred): prediction slots per block and the first predicting slot.
 
-    [dflash-log], "The proposal is the only change": the block is anchor-first, slot 0
-    already predicts the first draft, so every one of the L_in slots predicts.
+    [dflash-log], the paragraph saying that DSpark changes only the proposal: the block
+    is anchor-first, slot 0 already predicts the first draft, so every one of the L_in
+    slots predicts.
     [spec-pr], "Format differences": with sample_from_anchor false the block is the
     1+N infilling layout, slot 0 holds the bonus token and is not a prediction slot,
     so a block of 1+n_max slots yields n_max drafts; the read loop starts at
@@ -151,8 +157,9 @@ def confidence(hidden, w_conf, b_conf: float, i_first_pred: int, N: int) -> np.n
 
     [dflash-log], "spec: add confidence-based draft pruning for DSpark": the
     confidence head predicts each drafted position's acceptance.  Its form, a linear
-    projection of the slot's hidden state followed by a logistic, is the reading the
-    head's name (conf_proj) and its use as a survival probability support.
+    projection of the slot's hidden state followed by a logistic, is the reading that
+    the head's name (conf_proj) and its use as the chance that a slot survives
+    verification support.
     """
     h = upcast(hidden)[:, i_first_pred:i_first_pred + N, :]
     x = h @ upcast(w_conf) + float(b_conf)
@@ -162,8 +169,9 @@ def confidence(hidden, w_conf, b_conf: float, i_first_pred: int, N: int) -> np.n
 def truncation_length(conf_row: np.ndarray, conf_min: float) -> int:
     """Index of the first slot whose confidence is below conf_min, else N.
 
-    [dflash-log], "spec: add confidence-based draft pruning for DSpark": the block is
-    truncated at the first position below the threshold; 0 (the default) disables it.
+    [dflash-log], "spec: add confidence-based draft pruning for DSpark": the block ends
+    at its first slot whose confidence falls under the threshold; a threshold of 0 (the
+    default) turns the pruning off.
     "dflash: draft full n_max blocks ...": every block is drafted in full and
     truncated afterwards, so truncation only sets the length.
     """
@@ -223,7 +231,7 @@ def propose(hidden, anchors, lm_head, markov_w1, markov_w2, *, L_in: int,
             sample_from_anchor: bool, top_k: int, conf_min: float,
             lm_bias=None, w_conf=None, b_conf: float = 0.0,
             topk_markov: bool = True, return_logits: bool = False,
-            skip_truncated: bool = False) -> dict:
+            skip_truncated: bool = False, conf_hidden=None) -> dict:
     """The whole proposal of a batch: base logits, chain, top-k, confidence, truncation.
 
     Returns a dict with draft [B, N], topk_ids / topk_vals [B, N, k], conf [B, N]
@@ -235,6 +243,11 @@ def propose(hidden, anchors, lm_head, markov_w1, markov_w2, *, L_in: int,
     pruning) and verify reads nothing past that cut, so the slots after it need not be
     drafted at all: their draft and top-k ids read -1 and their top-k values NaN.  The
     slots before the cut, the confidences and n_draft are those of the full proposal.
+
+    ``conf_hidden`` [B, L_in, H] (optional): [luce-pr], summary, names a calibrated
+    confidence export taken before the final norm, i.e. a hidden state of its own for
+    the confidence head.  When given, the confidence head reads it in place of
+    ``hidden`` (same slots); the logits and the chain still read ``hidden``.
     """
     N, ifp = block_layout(L_in, sample_from_anchor)
     z = base_logits(hidden, lm_head, lm_bias, ifp, N)
@@ -252,7 +265,8 @@ def propose(hidden, anchors, lm_head, markov_w1, markov_w2, *, L_in: int,
         if return_logits:
             zc_all[b] = zc
     if w_conf is not None:
-        conf = confidence(hidden, w_conf, b_conf, ifp, N)
+        conf = confidence(hidden if conf_hidden is None else conf_hidden, w_conf, b_conf,
+                          ifp, N)
         n_draft = np.array([truncation_length(conf[b], conf_min) for b in range(B)],
                            np.int64)
     else:
@@ -291,3 +305,49 @@ def verify(draft, n_draft, target):
         emitted[b, :a] = draft[b, :a]
         emitted[b, a] = bonus[b]
     return accepted, bonus, emitted
+
+
+def tree_verify(topk_ids, n_draft, target):
+    """Verify of the top-k candidate lattice (the DDTree consumer), greedy target.
+
+    [luce-pr], description: the DDTree's candidates are the per-slot top-k, and they
+    get the Markov bias too; its summary leaves the tree step itself unchanged.
+    [ort-pr], the DFlash 2 and DSpark builder commits: a block drafter hands the runtime
+    a lattice of dspark_top_k candidates per slot, which the runtime walks greedily, and
+    DSpark reuses DFlash 2's verification path.  Reading (the pages define no tree
+    construction): the tree is
+    the whole lattice -- every candidate of slot i is a child of every candidate of slot
+    i - 1 -- down to the truncated length n_draft[b].  The greedy target accepts the
+    child equal to its own argmax after the accepted prefix; that prefix is always the
+    target's own tokens, so its argmax at depth i is target[b, i].
+
+    topk_ids [B, N, k], n_draft [B], target [B, N + 1].  Returns (accepted [B], bonus
+    [B], emitted [B, N + 1], path [B, N]): accepted = the depth reached, bonus =
+    target[b, accepted], emitted = the accepted tokens then the bonus then -1, path =
+    the rank of the candidate taken at each accepted depth and -1 after.
+    """
+    ids = np.asarray(topk_ids, np.int64)
+    target = np.asarray(target, np.int64)
+    B, N, k = ids.shape
+    accepted = np.zeros(B, np.int64)
+    bonus = np.zeros(B, np.int64)
+    emitted = np.full((B, N + 1), -1, np.int64)
+    path = np.full((B, N), -1, np.int64)
+    for b in range(B):
+        limit = min(max(int(n_draft[b]), 0), N)
+        depth = 0
+        while depth < limit:
+            rank = -1
+            for q in range(k):
+                if ids[b, depth, q] == target[b, depth]:
+                    rank = q
+                    break
+            if rank < 0:
+                break
+            emitted[b, depth] = ids[b, depth, rank]
+            path[b, depth] = rank
+            depth += 1
+        accepted[b] = depth
+        bonus[b] = target[b, depth]
+        emitted[b, depth] = bonus[b]
+    return accepted, bonus, emitted, path

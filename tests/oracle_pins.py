@@ -406,6 +406,109 @@ def pin_bonus_slot_unused():
     assert not np.array_equal(o1["draft"][:, 0], o3["draft"][:, 0])
 
 
+# ------------------------------------------------------------------- tree verify
+def _random_lattice(rng, B, N, k, V):
+    """Top-k ids of distinct tokens per slot, as the proposal produces them."""
+    return np.array([[rng.choice(V, k, replace=False) for _ in range(N)]
+                     for _ in range(B)], np.int64)
+
+
+def _tree_brute_force(ids_b, nd, t):
+    """Every node of the candidate tree, written out: a node is the tuple of candidate
+    ranks taken at depths 0..d-1 (d <= nd).  The greedy target reaches a node when the
+    node's tokens equal its own tokens t[0..d-1]; it accepts the deepest such node."""
+    N, k = ids_b.shape
+    best, best_ranks = 0, ()
+    for d in range(nd + 1):
+        for ranks in itertools.product(range(k), repeat=d):
+            tokens = [int(ids_b[i, ranks[i]]) for i in range(d)]
+            if tokens == [int(x) for x in t[:d]] and d >= best:
+                best, best_ranks = d, ranks
+    return best, best_ranks
+
+
+def pin_tree_verify_brute_force():
+    rng = np.random.default_rng(21)
+    V, N = 4, 3
+    for k in (1, 2, 3):
+        for _ in range(3):
+            ids = _random_lattice(rng, 1, N, k, V)
+            for t in itertools.product(range(V), repeat=N + 1):
+                for nd in range(N + 1):
+                    a, bo, em, path = O.tree_verify(ids, [nd], [t])
+                    want, ranks = _tree_brute_force(ids[0], nd, t)
+                    assert int(a[0]) == want, (ids, t, nd)
+                    assert int(bo[0]) == t[want]
+                    # greedy lossless: the target's own tokens, then -1
+                    assert em[0, :want + 1].tolist() == list(t[:want + 1])
+                    assert all(x == -1 for x in em[0, want + 1:])
+                    assert path[0, :want].tolist() == list(ranks)
+                    assert all(x == -1 for x in path[0, want:])
+
+
+def pin_tree_verify_top1_is_verify():
+    """With one candidate per slot the lattice is the greedy draft itself."""
+    rng = np.random.default_rng(22)
+    B, N, V = 5, 6, 5
+    for _ in range(50):
+        ids = rng.integers(0, V, (B, N, 1))
+        t = rng.integers(0, V, (B, N + 1))
+        t[:, :3] = np.where(rng.random((B, 3)) < 0.6, ids[:, :3, 0], t[:, :3])
+        nd = rng.integers(0, N + 1, B)
+        a, bo, em, _ = O.tree_verify(ids, nd, t)
+        a2, bo2, em2 = O.verify(ids[:, :, 0], nd, t)
+        assert np.array_equal(a, a2) and np.array_equal(bo, bo2) and np.array_equal(em, em2)
+
+
+def pin_tree_verify_planted_miss():
+    """The target's token at depth j is in no candidate of that depth: accepted
+    min(j, n_draft), whichever ranks matched before it."""
+    rng = np.random.default_rng(23)
+    N, k, V = 8, 4, 100
+    for nd in (0, 3, 8):
+        for j in range(N):
+            ids = _random_lattice(rng, 1, N, k, V)
+            ranks = rng.integers(0, k, N)
+            t = np.array([ids[0, i, ranks[i]] for i in range(N)] + [7])
+            t[j] = next(x for x in range(V) if x not in ids[0, j])
+            a, bo, _, path = O.tree_verify(ids, [nd], [t])
+            assert int(a[0]) == min(j, nd)
+            assert int(bo[0]) == t[min(j, nd)]
+            assert path[0, :min(j, nd)].tolist() == ranks[:min(j, nd)].tolist()
+
+
+# ------------------------------------------------------------------- conf input
+def pin_separate_confidence_input():
+    """A separate confidence input changes the confidences (closed form with a one-hot
+    w_conf) and nothing else; given the hidden states themselves it changes nothing."""
+    rng = np.random.default_rng(24)
+    B, L, H, V, r = 3, 5, 8, 50, 4
+    hidden = rng.standard_normal((B, L, H)).astype(np.float32)
+    ch = rng.standard_normal((B, L, H)).astype(np.float32)
+    W = rng.standard_normal((V, H)).astype(np.float32)
+    w1 = rng.standard_normal((V, r)).astype(np.float32)
+    w2 = rng.standard_normal((r, V)).astype(np.float32)
+    wc = np.zeros(H, np.float32)
+    wc[2] = 1.0
+    anchors = rng.integers(0, V, B)
+    for sfa in (True, False):
+        kw = dict(L_in=L, sample_from_anchor=sfa, top_k=3, conf_min=0.5, w_conf=wc,
+                  b_conf=0.25)
+        base = O.propose(hidden, anchors, W, w1, w2, **kw)
+        same = O.propose(hidden, anchors, W, w1, w2, conf_hidden=hidden, **kw)
+        other = O.propose(hidden, anchors, W, w1, w2, conf_hidden=ch, **kw)
+        for key in ("draft", "topk_ids", "topk_vals", "conf", "n_draft"):
+            assert np.array_equal(base[key], same[key]), key
+        for key in ("draft", "topk_ids", "topk_vals"):
+            assert np.array_equal(base[key], other[key]), key
+        ifp = 0 if sfa else 1
+        N = base["N"]
+        want = 1.0 / (1.0 + np.exp(-(ch[:, ifp:ifp + N, 2].astype(np.float64) + 0.25)))
+        assert np.allclose(other["conf"], want, rtol=0, atol=1e-15)
+        cut = [next((i for i in range(N) if want[b, i] < 0.5), N) for b in range(B)]
+        assert other["n_draft"].tolist() == cut
+
+
 # ------------------------------------------------------------------- random sweep
 def sweep_case(seed):
     """A random tiny configuration with small-integer weights and hidden states: every
@@ -496,5 +599,7 @@ ALL_PINS = [
     pin_chain_consistency, pin_single_slot, pin_masked_rows_never_emitted,
     pin_confidence_closed_forms, pin_truncation_positions, pin_verify_brute_force,
     pin_verify_planted_mismatch, pin_bf16_upcast, pin_bonus_slot_unused,
-    pin_adaptive_block_length, pin_brute_force_sweep,
+    pin_adaptive_block_length, pin_brute_force_sweep, pin_tree_verify_brute_force,
+    pin_tree_verify_top1_is_verify, pin_tree_verify_planted_miss,
+    pin_separate_confidence_input,
 ]

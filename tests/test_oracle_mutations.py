@@ -171,6 +171,55 @@ MUTATIONS.update({
 })
 
 
+_orig_tree = O.tree_verify
+_orig_propose = O.propose
+
+
+def _tree_top1_only(ids, nd, t):
+    return _orig_tree(np.asarray(ids)[:, :, :1], nd, t)
+
+
+def _tree_ignores_ndraft(ids, nd, t):
+    return _orig_tree(ids, np.full(len(nd), np.asarray(ids).shape[1]), t)
+
+
+def _tree_bonus_next(ids, nd, t):
+    a, b, e, p = _orig_tree(ids, nd, t)
+    t = np.asarray(t)
+    b2 = np.array([t[i, min(a[i] + 1, t.shape[1] - 1)] for i in range(len(a))])
+    e = e.copy()
+    for i in range(len(a)):
+        e[i, a[i]] = b2[i]
+    return a, b2, e, p
+
+
+def _tree_next_depth(ids, nd, t):
+    """candidates of depth i compared with the target's token of depth i + 1"""
+    t = np.asarray(t)
+    return _orig_tree(ids, nd, np.concatenate([t[:, 1:], t[:, -1:]], axis=1))
+
+
+def _tree_rank_reported_last(ids, nd, t):
+    a, b, e, p = _orig_tree(ids, nd, t)
+    k = np.asarray(ids).shape[2]
+    return a, b, e, np.where(p >= 0, k - 1 - p, p)
+
+
+MUTATIONS.update({
+    "tree_top1_only": ("tree_verify", _tree_top1_only),
+    "tree_ignores_ndraft": ("tree_verify", _tree_ignores_ndraft),
+    "tree_bonus_off_by_one": ("tree_verify", _tree_bonus_next),
+    "tree_depth_slip": ("tree_verify", _tree_next_depth),
+    "tree_path_rank_flipped": ("tree_verify", _tree_rank_reported_last),
+    "conf_hidden_ignored": ("propose",
+                            lambda *a, conf_hidden=None, **kw: _orig_propose(*a, **kw)),
+    "conf_hidden_feeds_logits": ("propose",
+                                 lambda h, *a, conf_hidden=None, **kw:
+                                 _orig_propose(h if conf_hidden is None else conf_hidden,
+                                               *a, conf_hidden=conf_hidden, **kw)),
+})
+
+
 @contextlib.contextmanager
 def _planted(name, fn):
     old = getattr(O, name)
