@@ -81,6 +81,7 @@ SIGNATURES = {
                                        ctypes.POINTER(dspark_outputs), c_ptr]),
     "dspark_verify": (c_i32, [c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "dspark_device_status": (c_i32, [c_ptr, c_ptr]),
+    "dspark_noalloc_device_status": (c_i32, [c_ptr]),
     "dspark_wait_selftest": (c_i32, [c_ptr, ctypes.c_size_t, ctypes.c_int64, c_i32, c_ptr]),
     "dspark_status_string": (ctypes.c_char_p, [c_i32]),
     "dspark_last_error": (ctypes.c_char_p, []),
@@ -184,6 +185,10 @@ def dspark_verify(B: int, N: int, draft: int, n_draft: int, target: int, accepte
 
 def dspark_device_status(workspace: int, stream: int = 0) -> int:
     return lib().dspark_device_status(workspace, stream)
+
+
+def dspark_noalloc_device_status(stream: int = 0) -> int:
+    return lib().dspark_noalloc_device_status(stream)
 
 
 def dspark_wait_selftest(workspace: int, workspace_bytes: int, budget_cycles: int,

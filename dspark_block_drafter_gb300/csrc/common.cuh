@@ -12,6 +12,7 @@ namespace dspark {
 enum : uint32_t {
   kErrBadToken = 1u,   // an anchor / previous token outside [0, V)
   kErrTimeout = 2u,    // a bounded wait gave up
+  kErrPrepared = 4u,   // the prepared head buffer was made for other weights or sizes
 };
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

@@ -199,6 +199,13 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
     p.cnorm = (const float*)(pr + pl.cnorm);
     p.cnmax = (const float*)(pr + pl.cnmax);
     p.w1max = (const unsigned*)(pr + pl.w1max);
+    p.prep = (const PreparedHeader*)(pr + pl.header);
+    p.prep_want.magic = kPreparedMagic;
+    p.prep_want.V = cfg->V;
+    p.prep_want.Vh = head->V_head;
+    p.prep_want.r = cfg->r;
+    p.prep_want.w1 = (unsigned long long)(uintptr_t)head->markov_w1;
+    p.prep_want.w2 = (unsigned long long)(uintptr_t)head->markov_w2;
     const PrunedLists ll = plan_pruned_lists(cfg->B, N, cfg->top_k);
     char* lists = ws + wl.cand;
     p.cand_v = (int32_t*)(lists + ll.cand_v);
@@ -422,6 +429,10 @@ dspark_status dspark_device_status(void* workspace, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
   if (word & kErrTimeout) return fail(DSPARK_ERR_TIMEOUT, "a device-side wait timed out");
+  if (word & kErrPrepared)
+    return fail(DSPARK_ERR_DEVICE,
+                "head->prepared was prepared for other weights or sizes (run "
+                "dspark_prepare_head for this head)");
   return fail(DSPARK_ERR_DEVICE, "a kernel saw a token outside [0, V)");
 }
 
@@ -487,14 +498,78 @@ const char* dspark_last_error(void) { return g_last_error.c_str(); }
 // Scratch for dspark_propose_noalloc: a fixed array in device memory that exists on every
 // GPU that loads this library, from the load until the process exits.  Host code must not
 // pass `g_noalloc_scratch` itself to a kernel: on the host that name is only a stand-in,
-// so the device address is looked up once per device with cudaGetSymbolAddress.
+// so its device address is looked up with cudaGetSymbolAddress while the device is
+// current.  The address belongs to the CUDA context that is current (a cudaDeviceReset or
+// a caller's own driver-API context gives another one), so it is looked up again on
+// every call that is not being captured into a graph, and remembered per context for
+// calls that are.
 static constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+  void* ctx;
+  void* ptr;
+};
+ScratchEntry g_noalloc_seen[kMaxContexts] = {};
+int g_noalloc_next = 0;
+
+// The calling thread's current CUDA context (driver API, reached through the runtime's
+// entry-point query so that the library needs no link against libcuda).
+dspark_status current_context(void** ctx) {
+  using GetCurrent = int (*)(void**);
+  static GetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (GetCurrent)p;
+  });
+  if (!fn) return fail(DSPARK_ERR_CUDA, "cuCtxGetCurrent is not available");
+  *ctx = nullptr;
+  if (fn(ctx) != 0 || !*ctx) return fail(DSPARK_ERR_CUDA, "no current CUDA context");
+  return DSPARK_OK;
+}
+
+// The device address of the built-in scratch in the current context.
+dspark_status noalloc_scratch(void* stream, void** scratch) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing((cudaStream_t)stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  void* ptr = nullptr;
+  if (cap == cudaStreamCaptureStatusNone) {
+    // (with the device current; this also brings up its context on a first call)
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
+  }
+  void* ctx = nullptr;
+  dspark_status st = current_context(&ctx);
+  if (st != DSPARK_OK) return st;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  int slot = -1;
+  for (int j = 0; j < kMaxContexts; ++j)
+    if (g_noalloc_seen[j].ctx == ctx) slot = j;
+  if (cap != cudaStreamCaptureStatusNone) {
+    if (slot < 0 || !g_noalloc_seen[slot].ptr)
+      return fail(DSPARK_ERR_INVALID_ARG,
+                  "dspark_propose_noalloc: make one call on this device outside stream "
+                  "capture first (it looks up the built-in scratch)");
+    *scratch = g_noalloc_seen[slot].ptr;
+    return DSPARK_OK;
+  }
+  if (slot < 0) {
+    slot = g_noalloc_next;
+    g_noalloc_next = (g_noalloc_next + 1) % kMaxContexts;
+  }
+  g_noalloc_seen[slot] = {ctx, ptr};
+  *scratch = ptr;
+  return DSPARK_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -513,26 +588,20 @@ dspark_status dspark_propose_noalloc(const dspark_config* cfg, const dspark_head
                     " bytes of scratch; the built-in scratch of dspark_propose_noalloc holds " +
                     std::to_string(kNoAllocScratchBytes) +
                     " bytes (use dspark_propose with a caller workspace)");
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices)
-    return fail(DSPARK_ERR_UNSUPPORTED, "device ordinal beyond the supported range");
-  void* scratch;
-  {
-    // first call on this device (which is current): resolve the array's device address
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-      void* ptr = nullptr;
-      e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
-      g_noalloc_ptr[dev] = ptr;
-    }
-    scratch = g_noalloc_ptr[dev];
-  }
-  // the control words that must start at zero are cleared by dspark_propose itself
+  void* scratch = nullptr;
+  dspark_status st = noalloc_scratch(stream, &scratch);
+  if (st != DSPARK_OK) return st;
+  // the control words that must start at zero (the error word among them) are cleared by
+  // dspark_propose itself
   return propose_impl(cfg, head, hidden, anchors, out, scratch, kNoAllocScratchBytes, stream,
                       nullptr);
+}
+
+dspark_status dspark_noalloc_device_status(void* stream) {
+  void* scratch = nullptr;
+  dspark_status st = noalloc_scratch(stream, &scratch);
+  if (st != DSPARK_OK) return st;
+  return dspark_device_status(scratch, stream);
 }
 
 }  // extern "C"

@@ -124,6 +124,10 @@ prepare_w1max(const __nv_bfloat16* __restrict__ w1, int V, int r, unsigned* __re
   if (lane == 0) atomicMax(out, __float_as_uint(best));
 }
 
+// The header goes in last, so that a buffer whose preparation did not finish reads as
+// unprepared.
+__global__ void prepare_header(PreparedHeader* dst, const PreparedHeader h) { *dst = h; }
+
 struct Cand {
   float x;     // corrected logit (NaN until evaluated)
   float z;     // base logit
@@ -347,6 +351,8 @@ struct TableArgs {
   int* walk_done;            // [B], zero at the start of the pass: table CTAs done per block
   const int32_t* nd_in;      // [B] cuts computed before the chain (adaptive block length:
                              // slots from the cut on are skipped), or NULL
+  const PreparedHeader* prep;    // the prepared buffer's header
+  PreparedHeader prep_want;      // what it must say for this head
   int B, N, V, Vh, T, r, k, kk, zrank, want_topk, L_in, ifp, H;
 };
 
@@ -977,6 +983,12 @@ pruned_table(const TableArgs a, const SelectArgs sel) {
   const int tid = threadIdx.x;
   pdl_signal();
   pdl_wait();                                        // z and zmax of the lm_head GEMM
+  // a prepared buffer made for other weights or sizes: nothing in it is read, nothing
+  // is drafted, and the error word says why
+  if (!prepared_matches(a.prep, a.prep_want)) {
+    if (tid == 0 && b == 0 && i == 0) flag_error(a.err, kErrPrepared);
+    return;
+  }
   // with the adaptive block length, a slot from the block's cut on is not drafted
   if (!a.nd_in || i < a.nd_in[b]) table_work(a, dsm, b, i);
   // ---- the last of the block's N CTAs to get here walks the block (the others' lists
@@ -1000,6 +1012,8 @@ PreparedLayout plan_prepared(int Vh, int r) {
   l.Vhp = align_up((size_t)Vh, kTile);
   l.tiles = l.Vhp / kTile;
   size_t off = 0;
+  l.header = off;
+  off = align_up(off + sizeof(PreparedHeader), 256);
   l.w2t = off;
   off = align_up(off + l.Vhp * r * sizeof(__nv_bfloat16), 256);
   l.cnorm = off;
@@ -1049,6 +1063,14 @@ cudaError_t launch_prepare_head(const void* w1, const void* w2, int V, int r, in
   const int grid = std::min(4096, (V + rows_per_cta - 1) / rows_per_cta);
   prepare_w1max<<<grid, 256, 0, stream>>>((const __nv_bfloat16*)w1, V, r,
                                           (unsigned*)(base + l.w1max));
+  PreparedHeader h{};
+  h.magic = kPreparedMagic;
+  h.V = V;
+  h.Vh = Vh;
+  h.r = r;
+  h.w1 = (unsigned long long)(uintptr_t)w1;
+  h.w2 = (unsigned long long)(uintptr_t)w2;
+  prepare_header<<<1, 1, 0, stream>>>((PreparedHeader*)(base + l.header), h);
   return cudaGetLastError();
 }
 
@@ -1057,7 +1079,7 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   const bool want_topk = p.topk_ids || p.topk_vals;
   const int kk = want_topk ? p.k : 1;
   const int zrank = (want_topk && !p.topk_markov) ? 1 : 0;
-  if (!p.z_octet || p.N > kMaxSlots || p.r % 8 != 0 || !p.walk_done)
+  if (!p.z_octet || p.N > kMaxSlots || p.r % 8 != 0 || !p.walk_done || !p.prep)
     return cudaErrorInvalidValue;
   TableArgs t{};
   t.z = p.z;
@@ -1088,6 +1110,8 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   t.err = p.ctrl;
   t.walk_done = p.walk_done;
   t.nd_in = p.skip_truncated ? p.n_draft : nullptr;
+  t.prep = p.prep;
+  t.prep_want = p.prep_want;
   t.B = p.B;
   t.N = p.N;
   t.V = p.V;

@@ -74,6 +74,8 @@ struct GemmArgs {
   uint8_t* zwritten;       // [N][B][zm_tiles]
   const float* cnmax;      // [zm_tiles] largest markov_w2 column norm of each tile
   const unsigned* w1max;   // largest markov_w1 row norm (float bits)
+  const PreparedHeader* prep;  // header of the prepared buffer cnmax and w1max lie in
+  PreparedHeader prep_want;    // what it must say (otherwise every tile is stored)
   int zbound_k;
   const int32_t* n_draft;  // [B] cuts computed before the GEMM (adaptive block length), or
                            // NULL: every row is drafted
@@ -372,7 +374,9 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     const int p = warp * 32 + lane;
     const int il = p / g.BB, bl = p - il * g.BB;     // slot and block within this CTA's half
     const size_t oct_step = g.ldb * 8;               // floats between consecutive row octets
-    const int K = g.zbound_k;
+    // (a prepared buffer made for another head: its bounds are not read, every tile is
+    // stored, and the chain reports the mismatch)
+    const int K = (g.zbound_k > 0 && prepared_matches(g.prep, g.prep_want)) ? g.zbound_k : 0;
     const int NB = K <= 8 ? K * kBucketX : K;        // maxima kept per row
     const float umax = K > 0 ? __uint_as_float(*g.w1max) * (1.f + kPrunedRelMargin) : 0.f;
     // a key of the same order as the float, 0 below every float
@@ -770,6 +774,8 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   g.zwritten = p.zwritten;
   g.cnmax = p.cnmax;
   g.w1max = p.w1max;
+  g.prep = p.prep;
+  g.prep_want = p.prep_want;
   g.zbound_k = p.zbound_k;
   g.n_draft = p.skip_truncated ? p.n_draft : nullptr;
   g.Vhp = p.Vhp;

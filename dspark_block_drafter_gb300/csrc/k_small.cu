@@ -12,8 +12,9 @@ namespace {
 
 // conf[b, i] = sigmoid(h[b, ifp + i] . w_conf + b_conf) and n_draft[b] = the first slot
 // with conf < conf_min, else N (llama.cpp commit 6fed9f6, "spec: add confidence-based
-// draft pruning for DSpark": truncate at the first position below the threshold, 0
-// disables).  One CTA per block; warps take slots round-robin.
+// draft pruning for DSpark": a block ends at its first slot whose confidence falls under
+// the threshold, and a threshold of 0 turns this off).  One CTA per block; warps take
+// slots round-robin.
 template <typename T>
 __global__ void __launch_bounds__(512)
 conf_truncate(const T* __restrict__ hidden, const T* __restrict__ w_conf, float b_conf,
@@ -64,9 +65,9 @@ conf_truncate(const T* __restrict__ hidden, const T* __restrict__ w_conf, float 
   }
 }
 
-// Greedy verify/accept, unchanged from DFlash (llama.cpp commit 6fed9f6: "verify
-// unchanged, same as DFlash"; greedy stays lossless).  One warp per block: a ballot over
-// the slot comparisons finds the first mismatch.
+// Greedy verify/accept, which DSpark takes over from DFlash as it is (llama.cpp commit
+// 6fed9f6, the verify paragraph of the squash log; greedy decoding stays lossless).  One
+// warp per block: a ballot over the slot comparisons finds the first mismatch.
 __global__ void __launch_bounds__(256)
 verify_kernel(int B, int N, const int32_t* __restrict__ draft,
               const int32_t* __restrict__ n_draft, const int32_t* __restrict__ target,

@@ -10,6 +10,23 @@
 
 namespace dspark {
 
+// First bytes of a prepared head buffer: what it was prepared for.  The kernels that
+// read a prepared buffer compare it with the head of the call before they read anything
+// else in it, and flag kErrPrepared (reading nothing more) when they differ.
+struct PreparedHeader {
+  uint32_t magic;          // kPreparedMagic once dspark_prepare_head has run
+  int32_t V, Vh, r;
+  unsigned long long w1, w2;   // device addresses of markov_w1 / markov_w2
+};
+constexpr uint32_t kPreparedMagic = 0x4B525044u;
+
+__device__ __forceinline__ bool prepared_matches(const PreparedHeader* h,
+                                                 const PreparedHeader& want) {
+  const PreparedHeader got = *h;
+  return got.magic == want.magic && got.V == want.V && got.Vh == want.Vh &&
+         got.r == want.r && got.w1 == want.w1 && got.w2 == want.w2;
+}
+
 // Everything a proposal launch needs, resolved by the ABI layer.
 struct ProposePlan {
   // sizes
@@ -43,6 +60,8 @@ struct ProposePlan {
   const float* cnorm;   // prepared head: column norms of markov_w2 [Vhp]
   const float* cnmax;   // prepared head: per-tile maxima of cnorm [Vhp / 128]
   const unsigned* w1max;  // prepared head: max row norm of markov_w1 (float bits)
+  const PreparedHeader* prep;  // prepared head: its header, or NULL
+  PreparedHeader prep_want;    // the header this call's head would have
   int32_t* cand_v;      // pruned chain: candidate head rows of each slot [N][B][cap]
   float* cand_z;        //               their base logits
   int32_t* cand_n;      //               candidate counts [N][B]
@@ -93,12 +112,13 @@ struct WorkspaceLayout {
 };
 WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool pruned);
 
-// Layout of a prepared head (dspark_prepare_head): markov_w2 transposed to [Vhp][r]
+// Layout of a prepared head (dspark_prepare_head): a PreparedHeader (256 bytes reserved),
+// markov_w2 transposed to [Vhp][r]
 // bf16, the fp32 Euclidean norm of every markov_w2 column [Vhp] (0 past V_head), the
 // maximum of those norms over each 128-row tile [Vhp / 128], and the largest norm of a
 // markov_w1 row (one float).
 struct PreparedLayout {
-  size_t w2t, cnorm, cnmax, w1max, total;
+  size_t header, w2t, cnorm, cnmax, w1max, total;
   size_t Vhp, tiles;
 };
 PreparedLayout plan_prepared(int Vh, int r);

@@ -33,8 +33,10 @@
  *     the first capture: it does the library's one-time per-device set-up.
  *   - Argument errors detectable on the host return before anything is launched and
  *     leave every output untouched.  Problems only the device can see (an anchor
- *     outside [0, V), a bounded wait that gave up) set a sticky error word in the
- *     workspace; read it with dspark_device_status().
+ *     outside [0, V), a bounded wait that gave up, a prepared buffer made for another
+ *     head) set bits of an error word in the workspace.  Each dspark_propose call clears
+ *     that word when it starts, so it describes the latest call on that workspace; read
+ *     it with dspark_device_status().
  *   - dspark_last_error() returns a message for the calling thread's last failure.
  */
 #ifndef DSPARK_H_
@@ -175,8 +177,11 @@ dspark_status dspark_verify(int32_t B, int32_t N, const int32_t* draft,
                             void* stream);
 
 /* Bytes of the buffer dspark_prepare_head() fills for this head (bf16 only; 0 on invalid
-   input or fp32).  Layout: markov_w2 transposed [round_up(V_head, 128)][r] bf16, the fp32
-   Euclidean norm of every markov_w2 column, and their maximum over each 128-row tile. */
+   input or fp32).  Layout: a 256-byte header recording what the buffer was prepared for
+   (V, V_head, r and the markov_w1 / markov_w2 addresses), markov_w2 transposed
+   [round_up(V_head, 128)][r] bf16, the fp32 Euclidean norm of every markov_w2 column,
+   their maximum over each 128-row tile, and the largest Euclidean norm of a markov_w1
+   row. */
 size_t dspark_prepare_head_size(const dspark_config* cfg, const dspark_head* head);
 
 /*
@@ -185,7 +190,16 @@ size_t dspark_prepare_head_size(const dspark_config* cfg, const dspark_head* hea
  *
  * prepared  device buffer of dspark_prepare_head_size() bytes, 256-byte aligned, owned by
  *           the caller; pass it as head->prepared to later dspark_propose calls.  It must
- *           be re-prepared if markov_w2 changes.  head->prepared itself is ignored here.
+ *           be prepared again whenever markov_w1 or markov_w2 changes, in place or by
+ *           address: the pruned chain's bounds come from both (the column norms of
+ *           markov_w2 and the largest row norm of markov_w1), and stale bounds can drop
+ *           the true argmax or top-k rows without any error.  head->prepared itself is
+ *           ignored here.
+ *
+ * A dspark_propose call whose V, V_head, r, markov_w1 or markov_w2 address differ from
+ * those the buffer was prepared for reads nothing past the buffer's header: it drafts
+ * nothing and dspark_device_status() then reports DSPARK_ERR_DEVICE with that reason.
+ * (Contents changed in place at the same addresses cannot be detected; re-prepare.)
  */
 dspark_status dspark_prepare_head(const dspark_config* cfg, const dspark_head* head,
                                   void* prepared, size_t prepared_bytes, void* stream);
@@ -258,22 +272,34 @@ dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head
  *   - Calls whose dspark_propose_workspace_size() exceeds 16 MiB return
  *     DSPARK_ERR_WORKSPACE before launching anything (small batches and vocabularies
  *     only; larger ones need dspark_propose and a caller workspace).
- *   - The first call on a device looks up the scratch's device address (with that device
- *     current) and keeps it; make that first call before any stream capture.
+ *   - The scratch's device address belongs to the CUDA context current at the call.  A
+ *     call that is not being captured looks it up (with the device current) and keeps it
+ *     for that context; a call made while `stream` is capturing uses the address kept
+ *     for the current context and is refused if there is none.  So make one call on each
+ *     device (and again after a cudaDeviceReset) before any stream capture.
  *   - Every call on a device shares the one scratch array, which keeps the contents the
  *     last call left (each call clears what has to start at zero).  Calls that overlap on
  *     the GPU -- on different streams, or from different host threads without ordering --
  *     race on it and give wrong results: order them on one stream.
- *   - Device-side error words land in that shared scratch and are not readable through
- *     dspark_device_status().
+ *   - Problems only the device can see (an anchor outside [0, V), a bounded wait that
+ *     gave up) are recorded in the scratch's error word; read them with
+ *     dspark_noalloc_device_status() before the next call on the device clears them.
  */
 dspark_status dspark_propose_noalloc(const dspark_config* cfg, const dspark_head* head,
                                      const void* hidden, const int32_t* anchors,
                                      const dspark_outputs* out, void* stream);
 
-/* Synchronises `stream`, reads the sticky device error word of a workspace used by
-   dspark_propose, and clears it.  DSPARK_OK when no kernel flagged anything. */
+/* Synchronises `stream`, reads the device error word of a workspace used by
+   dspark_propose (it describes the latest call on that workspace), and clears it.
+   DSPARK_OK when no kernel flagged anything; DSPARK_ERR_DEVICE or DSPARK_ERR_TIMEOUT
+   otherwise, with the reason in dspark_last_error(). */
 dspark_status dspark_device_status(void* workspace, void* stream);
+
+/* dspark_device_status() for the built-in scratch of dspark_propose_noalloc() on the
+   current device: synchronises `stream`, reads the error word of the latest no-alloc call
+   on this device and clears it.  (No counterpart on the pages, like the entry point it
+   serves.)  Call it on the stream of that call, outside stream capture. */
+dspark_status dspark_noalloc_device_status(void* stream);
 
 /*
  * dspark_wait_selftest -- makes one bounded device-side wait run out, on purpose.

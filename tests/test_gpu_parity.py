@@ -282,3 +282,45 @@ def test_pm_skip_with_every_row_fallback():
 def test_odd_slot_counts_pruned(B, L_in, sfa):
     run_case(_small(B=B, L_in=L_in, sample_from_anchor=sfa, H=128, V=2048, r=16, top_k=3),
              chain="pruned")
+
+
+# ------------------------------------------------------------------ a prepared buffer used
+# with another head: nothing past its header is read, the error word says why
+@pytest.mark.parametrize("change", ["markov_w2 address", "rank", "head rows"])
+def test_prepared_buffer_for_another_head(change):
+    import dspark_block_drafter_gb300 as ds
+    from dspark_block_drafter_gb300 import torch_io as tio
+    wl = _small(r=32, V=1024, B=32, L_in=8, H=256, weight_std=0.1)
+    hd, bt = make_head(wl), make_batch(wl)
+    cfg = tio.make_config(wl.B, wl.L_in, wl.H, wl.V, wl.r, wl.top_k, True, wl.conf_min, "bf16")
+    head = tio.head_to_device(hd).prepare(cfg)
+    hidden, anchors = tio.to_device(bt["hidden"]), tio.to_device(bt["anchors"])
+    if change == "markov_w2 address":            # same sizes, other weights
+        other = head.markov_w2.clone()
+        use_cfg, use = cfg, tio.Head(head.lm_head, head.markov_w1, other, None, None,
+                                     head.w_conf, head.b_conf, head.prepared)
+    elif change == "rank":                       # prepared for r = 32, used with r = 16
+        wl2 = _small(r=16, V=1024, B=32, L_in=8, H=256, weight_std=0.1)
+        hd2 = make_head(wl2)
+        use_cfg = tio.make_config(wl.B, wl.L_in, wl.H, wl.V, 16, wl.top_k, True,
+                                  wl.conf_min, "bf16")
+        h2 = tio.head_to_device(hd2)
+        use = tio.Head(h2.lm_head, h2.markov_w1, h2.markov_w2, None, None, h2.w_conf,
+                       h2.b_conf, head.prepared)
+    else:                                        # the compact form of fewer head rows
+        rows = np.sort(np.random.default_rng(3).choice(wl.V, 512, replace=False))
+        hd["emit_rows"] = rows
+        hd["lm_bias"] = np.zeros(wl.V, np.float32)
+        h2 = tio.head_to_device(hd, "d2t")
+        use_cfg, use = cfg, tio.Head(h2.lm_head, h2.markov_w1, h2.markov_w2, h2.lm_bias,
+                                     h2.d2t, h2.w_conf, h2.b_conf, head.prepared)
+    out = tio.Outputs.allocate(wl.B, wl.N, wl.top_k, use.V_head)
+    ws = tio.workspace_for(use_cfg, use)
+    tio.propose(use_cfg, use, hidden, anchors, out, ws)
+    assert tio.device_status(ws) == ds._abi.DSPARK_ERR_DEVICE
+    assert "prepared" in ds._abi.dspark_last_error()
+    assert tio.device_status(ws) == 0
+    # the same workspace, with a buffer prepared for this head, is clean again
+    use.prepare(use_cfg)
+    tio.propose(use_cfg, use, hidden, anchors, out, ws)
+    assert tio.device_status(ws) == 0

@@ -6,6 +6,9 @@ that must not touch the allocator) pass no workspace; the library uses its built
 check, on two calls in a row (the scratch keeps what the previous call left), that it
 returns what dspark_propose with a caller workspace returns.
 
+The scratch's error word is read with dspark_noalloc_device_status: a bad anchor is
+reported there, and the next clean call reads clean.
+
 This file is named so that pytest collects it last.
 """
 import numpy as np
@@ -97,3 +100,25 @@ def test_no_alloc_rejects_calls_beyond_its_scratch():
     st = _abi.dspark_propose_noalloc(cfg, head, 0x40000, 0x50000, out, 0)
     assert st == _abi.DSPARK_ERR_WORKSPACE
     assert "16777216" in _abi.dspark_last_error()
+
+
+@pytest.mark.parametrize("case", ["bf16-dense", "bf16-pruned-1+N"])
+def test_no_alloc_device_errors_are_readable(case):
+    wl, prepared = CASES[case]
+    cfg, head, hidden, anchors = _setup(wl, prepared)
+    stream = torch.cuda.current_stream().cuda_stream
+    bad = anchors.clone()
+    bad[1] = wl.V + 3                            # a token outside [0, V)
+    out = tio.Outputs.allocate(wl.B, wl.N, wl.top_k, head.V_head)
+    _abi.check(_abi.dspark_propose_noalloc(cfg, head.struct(), hidden.data_ptr(),
+                                           bad.data_ptr(), out.struct(), stream))
+    assert _abi.dspark_noalloc_device_status(stream) == _abi.DSPARK_ERR_DEVICE
+    assert "outside" in _abi.dspark_last_error()
+    assert _abi.dspark_noalloc_device_status(stream) == _abi.DSPARK_OK   # read clears it
+    # a bad call, then a good one: the good call starts from a clear word
+    _abi.check(_abi.dspark_propose_noalloc(cfg, head.struct(), hidden.data_ptr(),
+                                           bad.data_ptr(), out.struct(), stream))
+    ref = _with_workspace(wl, cfg, head, hidden, anchors)
+    got = _no_alloc(wl, cfg, head, hidden, anchors)
+    assert _abi.dspark_noalloc_device_status(stream) == _abi.DSPARK_OK
+    _same(ref, got, TOL[wl.dtype])
