@@ -13,5 +13,5 @@ loudly if the library has not been built.
 from ._abi import (DSPARK_BF16, DSPARK_F32, DSPARK_OK, DSparkError, check,  # noqa: F401
                    dspark_config, dspark_device_status, dspark_head, dspark_last_error,
                    dspark_num_slots, dspark_outputs, dspark_propose,
-                   dspark_propose_workspace_size, dspark_status_string, dspark_verify,
-                   dspark_wait_selftest, lib)
+                   dspark_propose_workspace_size, dspark_status_string, dspark_tree_verify,
+                   dspark_verify, dspark_wait_selftest, lib)

@@ -58,10 +58,10 @@ SIGNATURES = {
     "dspark_propose_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(dspark_config),
                                                         ctypes.POINTER(dspark_head)]),
     "dspark_propose": (c_i32, [ctypes.POINTER(dspark_config), ctypes.POINTER(dspark_head),
-                               c_ptr, c_ptr, ctypes.POINTER(dspark_outputs), c_ptr,
+                               c_ptr, c_ptr, c_ptr, ctypes.POINTER(dspark_outputs), c_ptr,
                                ctypes.c_size_t, c_ptr]),
     "dspark_propose_timed": (c_i32, [ctypes.POINTER(dspark_config),
-                                     ctypes.POINTER(dspark_head), c_ptr, c_ptr,
+                                     ctypes.POINTER(dspark_head), c_ptr, c_ptr, c_ptr,
                                      ctypes.POINTER(dspark_outputs), c_ptr, ctypes.c_size_t,
                                      c_ptr, ctypes.POINTER(c_ptr)]),
     "dspark_propose_kernel_count": (c_i32, [ctypes.POINTER(dspark_config),
@@ -71,15 +71,17 @@ SIGNATURES = {
                                                           ctypes.POINTER(dspark_head)]),
     "dspark_step_host": (c_i32, [ctypes.POINTER(dspark_config), ctypes.POINTER(dspark_head),
                                  c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
-                                 c_ptr, c_ptr, ctypes.c_size_t, c_ptr]),
+                                 c_ptr, c_ptr, c_ptr, ctypes.c_size_t, c_ptr]),
     "dspark_prepare_head_size": (ctypes.c_size_t, [ctypes.POINTER(dspark_config),
                                                    ctypes.POINTER(dspark_head)]),
     "dspark_prepare_head": (c_i32, [ctypes.POINTER(dspark_config), ctypes.POINTER(dspark_head),
                                     c_ptr, ctypes.c_size_t, c_ptr]),
     "dspark_propose_noalloc": (c_i32, [ctypes.POINTER(dspark_config),
-                                       ctypes.POINTER(dspark_head), c_ptr, c_ptr,
+                                       ctypes.POINTER(dspark_head), c_ptr, c_ptr, c_ptr,
                                        ctypes.POINTER(dspark_outputs), c_ptr]),
     "dspark_verify": (c_i32, [c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
+    "dspark_tree_verify": (c_i32, [c_i32, c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
+                                   c_ptr, c_ptr, c_ptr]),
     "dspark_device_status": (c_i32, [c_ptr, c_ptr]),
     "dspark_noalloc_device_status": (c_i32, [c_ptr]),
     "dspark_wait_selftest": (c_i32, [c_ptr, ctypes.c_size_t, ctypes.c_int64, c_i32, c_ptr]),
@@ -122,9 +124,11 @@ def dspark_propose_workspace_size(cfg: dspark_config, head: dspark_head) -> int:
 
 def dspark_propose(cfg: dspark_config, head: dspark_head, hidden: int, anchors: int,
                    out: dspark_outputs, workspace: int, workspace_bytes: int,
-                   stream: int = 0) -> int:
+                   stream: int = 0, conf_hidden: int | None = None) -> int:
+    """``conf_hidden`` goes to the C argument of that name (after ``anchors``)."""
     return lib().dspark_propose(ctypes.byref(cfg), ctypes.byref(head), hidden, anchors,
-                                ctypes.byref(out), workspace, workspace_bytes, stream)
+                                conf_hidden, ctypes.byref(out), workspace, workspace_bytes,
+                                stream)
 
 
 def dspark_prepare_head_size(cfg: dspark_config, head: dspark_head) -> int:
@@ -143,12 +147,12 @@ STAGE_NAMES = ("conf", "logits", "chain", "topk")
 
 def dspark_propose_timed(cfg: dspark_config, head: dspark_head, hidden: int, anchors: int,
                          out: dspark_outputs, workspace: int, workspace_bytes: int,
-                         stream: int, events) -> int:
+                         stream: int, events, conf_hidden: int | None = None) -> int:
     """``events``: DSPARK_NUM_STAGES + 1 cudaEvent_t handles (ints)."""
     arr = (c_ptr * (DSPARK_NUM_STAGES + 1))(*events)
     return lib().dspark_propose_timed(ctypes.byref(cfg), ctypes.byref(head), hidden, anchors,
-                                      ctypes.byref(out), workspace, workspace_bytes, stream,
-                                      arr)
+                                      conf_hidden, ctypes.byref(out), workspace,
+                                      workspace_bytes, stream, arr)
 
 
 def dspark_propose_kernel_count(cfg: dspark_config, head: dspark_head,
@@ -164,23 +168,34 @@ def dspark_step_host_workspace_size(cfg: dspark_config, head: dspark_head) -> in
 def dspark_step_host(cfg: dspark_config, head: dspark_head, hidden_h: int, anchors_h: int,
                      target_h: int, draft_h: int, n_draft_h: int, accepted_h: int,
                      bonus_h: int, topk_ids_h: int | None, topk_vals_h: int | None,
-                     workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+                     workspace: int, workspace_bytes: int, stream: int = 0,
+                     conf_hidden_h: int | None = None) -> int:
+    """``conf_hidden_h`` goes to the C argument of that name (after ``anchors_h``)."""
     return lib().dspark_step_host(ctypes.byref(cfg), ctypes.byref(head), hidden_h, anchors_h,
-                                  target_h, draft_h, n_draft_h, accepted_h, bonus_h,
-                                  topk_ids_h, topk_vals_h, workspace, workspace_bytes, stream)
+                                  conf_hidden_h, target_h, draft_h, n_draft_h, accepted_h,
+                                  bonus_h, topk_ids_h, topk_vals_h, workspace, workspace_bytes,
+                                  stream)
 
 
 def dspark_propose_noalloc(cfg: dspark_config, head: dspark_head, hidden: int, anchors: int,
-                           out: dspark_outputs, stream: int = 0) -> int:
+                           out: dspark_outputs, stream: int = 0,
+                           conf_hidden: int | None = None) -> int:
     """dspark_propose with the library's built-in 16 MiB scratch (no workspace)."""
     return lib().dspark_propose_noalloc(ctypes.byref(cfg), ctypes.byref(head), hidden, anchors,
-                                        ctypes.byref(out), stream)
+                                        conf_hidden, ctypes.byref(out), stream)
 
 
 def dspark_verify(B: int, N: int, draft: int, n_draft: int, target: int, accepted: int,
                   bonus: int, emitted: int | None, stream: int = 0) -> int:
     return lib().dspark_verify(B, N, draft, n_draft, target, accepted, bonus, emitted,
                                stream)
+
+
+def dspark_tree_verify(B: int, N: int, top_k: int, topk_ids: int, n_draft: int, target: int,
+                       accepted: int, bonus: int, emitted: int | None, path: int | None,
+                       stream: int = 0) -> int:
+    return lib().dspark_tree_verify(B, N, top_k, topk_ids, n_draft, target, accepted, bonus,
+                                    emitted, path, stream)
 
 
 def dspark_device_status(workspace: int, stream: int = 0) -> int:

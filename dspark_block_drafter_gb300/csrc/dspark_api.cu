@@ -144,7 +144,8 @@ size_t dspark_propose_workspace_size(const dspark_config* cfg, const dspark_head
 
 static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* head,
                                   const void* hidden, const int32_t* anchors,
-                                  const dspark_outputs* out, void* workspace,
+                                  const void* conf_hidden, const dspark_outputs* out,
+                                  void* workspace,
                                   size_t workspace_bytes, void* stream,
                                   void* const* events) {
   int N, ifp;
@@ -155,6 +156,8 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
     return fail(DSPARK_ERR_INVALID_ARG, "outputs draft and n_draft are required");
   if (cfg->dtype == DSPARK_BF16 && !aligned(hidden, 16))
     return fail(DSPARK_ERR_INVALID_ARG, "bf16 hidden must be 16-byte aligned");
+  if (cfg->dtype == DSPARK_BF16 && conf_hidden && !aligned(conf_hidden, 16))
+    return fail(DSPARK_ERR_INVALID_ARG, "bf16 conf_hidden must be 16-byte aligned");
   const bool pruned = use_pruned(cfg, head) && !out->logits;
   if (cfg->skip_truncated && !pruned)
     return fail(DSPARK_ERR_UNSUPPORTED,
@@ -173,6 +176,7 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   p.Vh = head->V_head; p.r = cfg->r; p.k = cfg->top_k; p.topk_markov = cfg->topk_markov;
   p.dtype = cfg->dtype; p.conf_min = cfg->conf_min; p.b_conf = head->b_conf;
   p.hidden = hidden; p.anchors = anchors; p.lm_head = head->lm_head;
+  p.conf_hidden = conf_hidden ? conf_hidden : hidden;
   p.lm_bias = head->lm_bias; p.d2t = head->d2t; p.w1 = head->markov_w1;
   p.w2 = head->markov_w2; p.w_conf = head->w_conf;
   p.draft = out->draft; p.n_draft = out->n_draft; p.topk_ids = out->topk_ids;
@@ -255,22 +259,22 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
 
 dspark_status dspark_propose(const dspark_config* cfg, const dspark_head* head,
                              const void* hidden, const int32_t* anchors,
-                             const dspark_outputs* out, void* workspace,
-                             size_t workspace_bytes, void* stream) {
-  return propose_impl(cfg, head, hidden, anchors, out, workspace, workspace_bytes, stream,
-                      nullptr);
+                             const void* conf_hidden, const dspark_outputs* out,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  return propose_impl(cfg, head, hidden, anchors, conf_hidden, out, workspace,
+                      workspace_bytes, stream, nullptr);
 }
 
 dspark_status dspark_propose_timed(const dspark_config* cfg, const dspark_head* head,
                                    const void* hidden, const int32_t* anchors,
-                                   const dspark_outputs* out, void* workspace,
-                                   size_t workspace_bytes, void* stream,
+                                   const void* conf_hidden, const dspark_outputs* out,
+                                   void* workspace, size_t workspace_bytes, void* stream,
                                    void* const* events) {
   if (!events) return fail(DSPARK_ERR_INVALID_ARG, "events is NULL");
   for (int s = 0; s <= DSPARK_NUM_STAGES; ++s)
     if (!events[s]) return fail(DSPARK_ERR_INVALID_ARG, "an event is NULL");
-  return propose_impl(cfg, head, hidden, anchors, out, workspace, workspace_bytes, stream,
-                      events);
+  return propose_impl(cfg, head, hidden, anchors, conf_hidden, out, workspace,
+                      workspace_bytes, stream, events);
 }
 
 int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head* head,
@@ -287,14 +291,15 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
 
 // staging for dspark_step_host, placed after dspark_propose's workspace
 struct StageLayout {
-  size_t hidden, anchors, target, draft, n_draft, accepted, bonus, tk_ids, tk_vals, total;
+  size_t hidden, conf_hidden, anchors, target, draft, n_draft, accepted, bonus, tk_ids, tk_vals, total;
 };
-static StageLayout plan_stage(const dspark_config* c, int N, size_t base) {
+static StageLayout plan_stage(const dspark_config* c, int N, size_t base, bool conf_input) {
   StageLayout s{};
   size_t es = c->dtype == DSPARK_BF16 ? 2 : 4;
   size_t off = base;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, kAlign); return o; };
   s.hidden = take(es * (size_t)c->B * c->L_in * c->H);
+  s.conf_hidden = take(conf_input ? es * (size_t)c->B * c->L_in * c->H : 0);
   s.anchors = take(4 * (size_t)c->B);
   s.target = take(4 * (size_t)c->B * (N + 1));
   s.draft = take(4 * (size_t)c->B * N);
@@ -310,15 +315,18 @@ static StageLayout plan_stage(const dspark_config* c, int N, size_t base) {
 size_t dspark_step_host_workspace_size(const dspark_config* cfg, const dspark_head* head) {
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return 0;
+  // (room for a separate confidence input is always planned, so one size fits both)
   return plan_stage(cfg, N,
                     plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype,
                                    use_pruned(cfg, head))
-                        .total)
+                        .total,
+                    true)
       .total;
 }
 
 dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head,
                                const void* hidden_h, const int32_t* anchors_h,
+                               const void* conf_hidden_h,
                                const int32_t* target_h, int32_t* draft_h,
                                int32_t* n_draft_h, int32_t* accepted_h, int32_t* bonus_h,
                                int32_t* topk_ids_h, float* topk_vals_h,
@@ -330,7 +338,7 @@ dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head
     return fail(DSPARK_ERR_INVALID_ARG, "a required host buffer is NULL");
   size_t base =
       plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype, use_pruned(cfg, head)).total;
-  StageLayout s = plan_stage(cfg, N, base);
+  StageLayout s = plan_stage(cfg, N, base, true);
   if (!workspace || !aligned(workspace, 256))
     return fail(DSPARK_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
   if (workspace_bytes < s.total)
@@ -361,6 +369,9 @@ dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head
   };
   if ((e = h2d(s.hidden, hidden_h, es * B * cfg->L_in * cfg->H)) != cudaSuccess)
     return cuda_fail(e, "host-to-device copy");
+  if (conf_hidden_h &&
+      (e = h2d(s.conf_hidden, conf_hidden_h, es * B * cfg->L_in * cfg->H)) != cudaSuccess)
+    return cuda_fail(e, "host-to-device copy");
   const int32_t* anchors_d = (const int32_t*)device_view(anchors_h);
   const int32_t* target_d = (const int32_t*)device_view(target_h);
   if (!anchors_d) {
@@ -386,7 +397,9 @@ dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head
   o.topk_vals = !topk_vals_h ? nullptr : in_place ? (float*)out_d[5] : (float*)(ws + s.tk_vals);
   int32_t* accepted_d = in_place ? (int32_t*)out_d[2] : (int32_t*)(ws + s.accepted);
   int32_t* bonus_d = in_place ? (int32_t*)out_d[3] : (int32_t*)(ws + s.bonus);
-  st = propose_impl(cfg, head, ws + s.hidden, anchors_d, &o, workspace, base, stream, nullptr);
+  st = propose_impl(cfg, head, ws + s.hidden, anchors_d,
+                    conf_hidden_h ? (const void*)(ws + s.conf_hidden) : nullptr, &o, workspace,
+                    base, stream, nullptr);
   if (st != DSPARK_OK) return st;
   st = dspark_verify(cfg->B, N, o.draft, o.n_draft, target_d, accepted_d, bonus_d, nullptr,
                      stream);
@@ -414,6 +427,21 @@ dspark_status dspark_verify(int32_t B, int32_t N, const int32_t* draft,
   cudaError_t e = launch_verify(B, N, draft, n_draft, target, accepted, bonus, emitted,
                                 (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "verify kernel");
+  return DSPARK_OK;
+}
+
+dspark_status dspark_tree_verify(int32_t B, int32_t N, int32_t top_k,
+                                 const int32_t* topk_ids, const int32_t* n_draft,
+                                 const int32_t* target, int32_t* accepted, int32_t* bonus,
+                                 int32_t* emitted, int32_t* path, void* stream) {
+  if (B < 1 || N < 1) return fail(DSPARK_ERR_INVALID_ARG, "B and N must be >= 1");
+  if (top_k < 1 || top_k > 32) return fail(DSPARK_ERR_INVALID_ARG, "top_k must be in [1, 32]");
+  if (!topk_ids || !n_draft || !target || !accepted || !bonus)
+    return fail(DSPARK_ERR_INVALID_ARG,
+                "topk_ids, n_draft, target, accepted and bonus are required");
+  cudaError_t e = launch_tree_verify(B, N, top_k, topk_ids, n_draft, target, accepted, bonus,
+                                     emitted, path, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tree verify kernel");
   return DSPARK_OK;
 }
 
@@ -576,7 +604,8 @@ extern "C" {
 
 dspark_status dspark_propose_noalloc(const dspark_config* cfg, const dspark_head* head,
                                      const void* hidden, const int32_t* anchors,
-                                     const dspark_outputs* out, void* stream) {
+                                     const void* conf_hidden, const dspark_outputs* out,
+                                     void* stream) {
   const size_t need = dspark_propose_workspace_size(cfg, head);
   if (need == 0) {
     int N, ifp;
@@ -593,8 +622,8 @@ dspark_status dspark_propose_noalloc(const dspark_config* cfg, const dspark_head
   if (st != DSPARK_OK) return st;
   // the control words that must start at zero (the error word among them) are cleared by
   // dspark_propose itself
-  return propose_impl(cfg, head, hidden, anchors, out, scratch, kNoAllocScratchBytes, stream,
-                      nullptr);
+  return propose_impl(cfg, head, hidden, anchors, conf_hidden, out, scratch,
+                      kNoAllocScratchBytes, stream, nullptr);
 }
 
 dspark_status dspark_noalloc_device_status(void* stream) {

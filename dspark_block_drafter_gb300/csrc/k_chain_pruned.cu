@@ -1094,7 +1094,7 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
   t.w2t = p.w2t;
   t.anchors = p.anchors;
   t.d2t = p.d2t;
-  t.hidden = (const __nv_bfloat16*)p.hidden;
+  t.hidden = (const __nv_bfloat16*)p.conf_hidden;
   // (with the adaptive block length the confidences are already computed)
   t.w_conf = p.skip_truncated ? nullptr : (const __nv_bfloat16*)p.w_conf;
   t.b_conf = p.b_conf;

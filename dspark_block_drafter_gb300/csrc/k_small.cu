@@ -97,6 +97,54 @@ verify_kernel(int B, int N, const int32_t* __restrict__ draft,
       emitted[(size_t)b * (N + 1) + j] = j < a ? d[j] : (j == a ? bo : -1);
 }
 
+// Verify of the top-k candidate lattice (the DDTree consumer; lucebox PR #626, description:
+// the tree's candidates are the per-slot top-k with the Markov bias; onnxruntime-genai
+// PR #2490, the DFlash 2 / DSpark builder commits: the runtime walks the drafter's
+// candidate lattice greedily).  Every candidate of slot i is a child of every candidate
+// of slot i - 1, so the greedy target, whose argmax after an accepted prefix is its own
+// token target[b, i], goes one level deeper exactly when that token is among slot i's
+// candidates.  One warp per block: lane i scans the k candidates of depth i, a ballot
+// finds the first depth without the target's token.
+__global__ void __launch_bounds__(256)
+tree_verify_kernel(int B, int N, int k, const int32_t* __restrict__ topk_ids,
+                   const int32_t* __restrict__ n_draft, const int32_t* __restrict__ target,
+                   int32_t* __restrict__ accepted, int32_t* __restrict__ bonus,
+                   int32_t* __restrict__ emitted, int32_t* __restrict__ path) {
+  const int b = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  pdl_wait();                                        // the lattice of the proposal
+  if (b >= B) return;
+  const int nd = min(max(n_draft[b], 0), N);
+  const int32_t* t = target + (size_t)b * (N + 1);
+  // rank of the target's token among depth j's candidates, or -1
+  auto rank_at = [&](int j) {
+    const int32_t* c = topk_ids + ((size_t)b * N + j) * k;
+    const int32_t want = t[j];
+    for (int q = 0; q < k; ++q)
+      if (c[q] == want) return q;
+    return -1;
+  };
+  int a = nd;
+  for (int j0 = 0; j0 < nd; j0 += 32) {
+    const int j = j0 + lane;
+    const bool miss = j < nd && rank_at(j) < 0;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, miss);
+    if (m) { a = j0 + __ffs(m) - 1; break; }
+  }
+  const int bo = t[a];
+  if (lane == 0) {
+    accepted[b] = a;
+    bonus[b] = bo;
+  }
+  // the accepted tokens are the target's own, then the bonus token
+  if (emitted)
+    for (int j = lane; j <= N; j += 32)
+      emitted[(size_t)b * (N + 1) + j] = j <= a ? t[j] : -1;
+  if (path)
+    for (int j = lane; j < N; j += 32)
+      path[(size_t)b * N + j] = j < a ? rank_at(j) : -1;
+}
+
 // Self-test of the bounded wait that every pipeline of the library relies on: one thread
 // waits on a fresh mbarrier that nothing ever arrives on, through the same ptx::mbar_wait
 // the GEMM and the chain pipelines use.  When the clock budget runs out (or, with
@@ -130,11 +178,11 @@ cudaError_t launch_conf(const ProposePlan& p) {
   const int threads = 32 * std::min(16, std::max(1, p.N));   // one warp per slot
   if (p.dtype == 0)
     conf_truncate<float><<<p.B, threads, smem, p.stream>>>(
-        (const float*)p.hidden, (const float*)p.w_conf, p.b_conf, p.L_in, p.N, p.ifp, p.H,
+        (const float*)p.conf_hidden, (const float*)p.w_conf, p.b_conf, p.L_in, p.N, p.ifp, p.H,
         p.conf_min, conf, p.n_draft);
   else
     conf_truncate<__nv_bfloat16><<<p.B, threads, smem, p.stream>>>(
-        (const __nv_bfloat16*)p.hidden, (const __nv_bfloat16*)p.w_conf, p.b_conf, p.L_in,
+        (const __nv_bfloat16*)p.conf_hidden, (const __nv_bfloat16*)p.w_conf, p.b_conf, p.L_in,
         p.N, p.ifp, p.H, p.conf_min, conf, p.n_draft);
   return cudaGetLastError();
 }
@@ -146,6 +194,16 @@ cudaError_t launch_verify(int B, int N, const int32_t* draft, const int32_t* n_d
   return launch_dependent(verify_kernel, dim3((B + warps_per_cta - 1) / warps_per_cta),
                           dim3(32 * warps_per_cta), 0, stream, B, N, draft, n_draft, target,
                           accepted, bonus, emitted);
+}
+
+cudaError_t launch_tree_verify(int B, int N, int k, const int32_t* topk_ids,
+                               const int32_t* n_draft, const int32_t* target,
+                               int32_t* accepted, int32_t* bonus, int32_t* emitted,
+                               int32_t* path, cudaStream_t stream) {
+  const int warps_per_cta = 8;
+  return launch_dependent(tree_verify_kernel, dim3((B + warps_per_cta - 1) / warps_per_cta),
+                          dim3(32 * warps_per_cta), 0, stream, B, N, k, topk_ids, n_draft,
+                          target, accepted, bonus, emitted, path);
 }
 
 }  // namespace dspark

@@ -34,6 +34,7 @@ struct ProposePlan {
   float conf_min, b_conf;
   // inputs
   const void* hidden;
+  const void* conf_hidden;   // what the confidence head reads: hidden, or a separate input
   const int32_t* anchors;
   const void* lm_head;
   const float* lm_bias;
@@ -175,6 +176,10 @@ cudaError_t launch_chain_tc(const ProposePlan& p);
 cudaError_t launch_verify(int B, int N, const int32_t* draft, const int32_t* n_draft,
                           const int32_t* target, int32_t* accepted, int32_t* bonus,
                           int32_t* emitted, cudaStream_t stream);
+cudaError_t launch_tree_verify(int B, int N, int k, const int32_t* topk_ids,
+                               const int32_t* n_draft, const int32_t* target,
+                               int32_t* accepted, int32_t* bonus, int32_t* emitted,
+                               int32_t* path, cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint32_t* err, long long budget, int pre_abort,
                                  cudaStream_t stream);
 

@@ -138,11 +138,12 @@ def workspace_for(cfg, head: Head, device="cuda") -> torch.Tensor:
 
 
 def propose(cfg, head: Head, hidden: torch.Tensor, anchors: torch.Tensor, out: Outputs,
-            workspace: torch.Tensor, stream=None) -> None:
+            workspace: torch.Tensor, stream=None, conf_hidden: Optional[torch.Tensor] = None
+            ) -> None:
     """dspark_propose on torch tensors; raises DSparkError on a non-OK status."""
     _abi.check(_abi.dspark_propose(cfg, head.struct(), hidden.data_ptr(), anchors.data_ptr(),
                                    out.struct(), workspace.data_ptr(), workspace.numel(),
-                                   _stream(stream)))
+                                   _stream(stream), _ptr(conf_hidden)))
 
 
 def verify(draft, n_draft, target, accepted, bonus, emitted=None, stream=None) -> None:
@@ -151,6 +152,16 @@ def verify(draft, n_draft, target, accepted, bonus, emitted=None, stream=None) -
     _abi.check(_abi.dspark_verify(B, N, draft.data_ptr(), n_draft.data_ptr(),
                                   target.data_ptr(), accepted.data_ptr(), bonus.data_ptr(),
                                   _ptr(emitted), _stream(stream)))
+
+
+def tree_verify(topk_ids, n_draft, target, accepted, bonus, emitted=None, path=None,
+                stream=None) -> None:
+    """dspark_tree_verify on torch tensors; raises DSparkError on a non-OK status."""
+    B, N, k = topk_ids.shape
+    _abi.check(_abi.dspark_tree_verify(B, N, k, topk_ids.data_ptr(), n_draft.data_ptr(),
+                                       target.data_ptr(), accepted.data_ptr(),
+                                       bonus.data_ptr(), _ptr(emitted), _ptr(path),
+                                       _stream(stream)))
 
 
 def device_status(workspace: torch.Tensor, stream=None) -> int:

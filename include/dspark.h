@@ -145,6 +145,11 @@ size_t dspark_propose_workspace_size(const dspark_config* cfg, const dspark_head
  * hidden  device [B, L_in, H] dtype: the drafter's final hidden states
  * anchors device [B] int32: token 0 of every block (the dedicated anchor input of the
  *         llama.cpp squash log; in the 1+N layout the bonus token), each in [0, V)
+ * conf_hidden device [B, L_in, H] dtype, or NULL: a separate input of the confidence
+ *         head (lucebox PR #626, summary: a calibrated confidence export taken before
+ *         the final norm).  When given, the confidence head reads it in place of
+ *         `hidden`, slot for slot; the logits and the chain still read `hidden`.  NULL:
+ *         the confidence head reads `hidden`.
  * out     the outputs above
  *
  * Steps, all on the device: (a) emittable-row handling from lm_bias / d2t;
@@ -155,7 +160,7 @@ size_t dspark_propose_workspace_size(const dspark_config* cfg, const dspark_head
  */
 dspark_status dspark_propose(const dspark_config* cfg, const dspark_head* head,
                              const void* hidden, const int32_t* anchors,
-                             const dspark_outputs* out,
+                             const void* conf_hidden, const dspark_outputs* out,
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
@@ -175,6 +180,36 @@ dspark_status dspark_verify(int32_t B, int32_t N, const int32_t* draft,
                             const int32_t* n_draft, const int32_t* target,
                             int32_t* accepted, int32_t* bonus, int32_t* emitted,
                             void* stream);
+
+/*
+ * dspark_tree_verify -- greedy verify of the top-k candidate lattice (the tree consumer
+ * of the per-slot candidates; lucebox PR #626, description: the DDTree's candidate
+ * top-k gets the Markov bias; onnxruntime-genai PR #2490, DFlash 2 / DSpark builder
+ * commits: the runtime walks the drafter's candidate lattice greedily).
+ *
+ * The tree is the whole lattice: every candidate of slot i is a child of every candidate
+ * of slot i - 1, down to depth n_draft[b] (the pages define no other construction).  A
+ * greedy target accepts the child equal to its argmax after the accepted prefix; as that
+ * prefix is always the target's own tokens, the argmax at depth i is target[b, i].
+ *
+ * topk_ids device [B, N, top_k] int32: the candidates of dspark_propose (topk_ids)
+ * n_draft  device [B] int32 (clamped to [0, N])
+ * target   device [B, N + 1] int32: the target model's argmax tokens along its own
+ *          greedy continuation
+ * accepted device [B] int32: a = the largest j <= n_draft[b] such that target[b, i] is
+ *          among topk_ids[b, i, :] for every i < j
+ * bonus    device [B] int32: target[b, a]
+ * emitted  device [B, N + 1] int32 or NULL: target[b, 0..a], then -1 (greedy lossless)
+ * path     device [B, N] int32 or NULL: for i < a the rank q with
+ *          topk_ids[b, i, q] == target[b, i] (the first such q), -1 from a on
+ *
+ * With top_k = 1 it equals dspark_verify on the greedy draft.  Host-detectable errors
+ * (sizes, NULL required pointers) return before any launch.
+ */
+dspark_status dspark_tree_verify(int32_t B, int32_t N, int32_t top_k,
+                                 const int32_t* topk_ids, const int32_t* n_draft,
+                                 const int32_t* target, int32_t* accepted, int32_t* bonus,
+                                 int32_t* emitted, int32_t* path, void* stream);
 
 /* Bytes of the buffer dspark_prepare_head() fills for this head (bf16 only; 0 on invalid
    input or fp32).  Layout: a 256-byte header recording what the buffer was prepared for
@@ -219,8 +254,8 @@ enum {
    one's.  The work done is identical to dspark_propose's. */
 dspark_status dspark_propose_timed(const dspark_config* cfg, const dspark_head* head,
                                    const void* hidden, const int32_t* anchors,
-                                   const dspark_outputs* out, void* workspace,
-                                   size_t workspace_bytes, void* stream,
+                                   const void* conf_hidden, const dspark_outputs* out,
+                                   void* workspace, size_t workspace_bytes, void* stream,
                                    void* const* events);
 
 /* Number of kernels one dspark_propose call launches for this config, head and set of
@@ -238,6 +273,8 @@ size_t dspark_step_host_workspace_size(const dspark_config* cfg, const dspark_he
  * and target in, runs dspark_propose and dspark_verify, copies the results out.
  *
  * hidden_h  host [B, L_in, H] dtype      anchors_h host [B] int32
+ * conf_hidden_h host [B, L_in, H] dtype, or NULL: the confidence head's separate input
+ *           (see dspark_propose); copied in like hidden_h
  * target_h  host [B, N + 1] int32 (the target's argmax tokens for the verify step)
  * draft_h   host [B, N] int32            n_draft_h host [B] int32
  * accepted_h, bonus_h host [B] int32
@@ -253,6 +290,7 @@ size_t dspark_step_host_workspace_size(const dspark_config* cfg, const dspark_he
  */
 dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head,
                                const void* hidden_h, const int32_t* anchors_h,
+                               const void* conf_hidden_h,
                                const int32_t* target_h, int32_t* draft_h,
                                int32_t* n_draft_h, int32_t* accepted_h, int32_t* bonus_h,
                                int32_t* topk_ids_h, float* topk_vals_h,
@@ -287,7 +325,8 @@ dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head
  */
 dspark_status dspark_propose_noalloc(const dspark_config* cfg, const dspark_head* head,
                                      const void* hidden, const int32_t* anchors,
-                                     const dspark_outputs* out, void* stream);
+                                     const void* conf_hidden, const dspark_outputs* out,
+                                     void* stream);
 
 /* Synchronises `stream`, reads the device error word of a workspace used by
    dspark_propose (it describes the latest call on that workspace), and clears it.

@@ -11,7 +11,7 @@ TOL = {"f32": 1e-5, "bf16": 2e-2}
 
 
 def gpu_propose(wl, hd, bt, form="full", want_logits=False, want_topk=True, stream=None,
-                chain="dense", skip_truncated=False):
+                chain="dense", skip_truncated=False, conf_hidden=None):
     """Run dspark_propose on the GPU; returns (numpy outputs, workspace tensor).
 
     chain "dense" evaluates every head row; "pruned" prepares the head first so that the
@@ -30,21 +30,22 @@ def gpu_propose(wl, hd, bt, form="full", want_logits=False, want_topk=True, stre
     out = tio.Outputs.allocate(wl.B, wl.N, wl.top_k, head.V_head, topk=want_topk,
                                conf=hd.get("w_conf") is not None, logits=want_logits)
     ws = tio.workspace_for(cfg, head)
-    tio.propose(cfg, head, hidden, anchors, out, ws, stream)
+    ch = None if conf_hidden is None else tio.to_device(conf_hidden)
+    tio.propose(cfg, head, hidden, anchors, out, ws, stream, conf_hidden=ch)
     torch.cuda.synchronize()
     st = tio.device_status(ws)
     assert st == 0, f"device status {st}"
     return out.numpy(), ws
 
 
-def oracle_run(wl, hd, bt, want_logits=False, skip_truncated=False):
+def oracle_run(wl, hd, bt, want_logits=False, skip_truncated=False, conf_hidden=None):
     return oracle_propose(bt["hidden"], bt["anchors"], hd["lm_head"], hd["markov_w1"],
                           hd["markov_w2"], L_in=wl.L_in,
                           sample_from_anchor=wl.sample_from_anchor, top_k=wl.top_k,
                           conf_min=wl.conf_min, lm_bias=hd.get("lm_bias"),
                           w_conf=hd.get("w_conf"), b_conf=hd.get("b_conf", 0.0),
                           topk_markov=wl.topk_markov, return_logits=want_logits,
-                          skip_truncated=skip_truncated)
+                          skip_truncated=skip_truncated, conf_hidden=conf_hidden)
 
 
 def compare(wl, hd, bt, o, g, form="full", skip_truncated=False):
@@ -58,12 +59,12 @@ def compare(wl, hd, bt, o, g, form="full", skip_truncated=False):
 
 
 def run_case(wl, form="full", want_logits=True, hd=None, bt=None, chain="dense",
-             skip_truncated=False):
+             skip_truncated=False, conf_hidden=None):
     hd = make_head(wl) if hd is None else hd
     bt = make_batch(wl) if bt is None else bt
     g, _ = gpu_propose(wl, hd, bt, form, want_logits and chain == "dense", chain=chain,
-                       skip_truncated=skip_truncated)
-    o = oracle_run(wl, hd, bt, skip_truncated=skip_truncated)
+                       skip_truncated=skip_truncated, conf_hidden=conf_hidden)
+    o = oracle_run(wl, hd, bt, skip_truncated=skip_truncated, conf_hidden=conf_hidden)
     rep = compare(wl, hd, bt, o, g, form, skip_truncated=skip_truncated)
     assert rep["failures"] == [], rep
     return g, o, rep

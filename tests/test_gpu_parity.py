@@ -324,3 +324,38 @@ def test_prepared_buffer_for_another_head(change):
     use.prepare(use_cfg)
     tio.propose(use_cfg, use, hidden, anchors, out, ws)
     assert tio.device_status(ws) == 0
+
+
+# ------------------------------------------------------------------ a separate confidence
+# input: the confidence head reads it, the logits and the chain do not
+@pytest.mark.parametrize("chain,sfa,dtype", [("dense", True, "bf16"), ("pruned", False, "bf16"),
+                                             ("pruned", True, "bf16"), ("dense", True, "f32")])
+def test_separate_confidence_input(chain, sfa, dtype):
+    from workloads import make_conf_hidden
+    wl = _small(sample_from_anchor=sfa, dtype=dtype, r=32, conf_std=0.3, L_in=7)
+    hd, bt = make_head(wl), make_batch(wl)
+    ch = make_conf_hidden(wl)
+    g, o, rep = run_case(wl, chain=chain, hd=hd, bt=bt, conf_hidden=ch)
+    plain, _ = gpu_propose(wl, hd, bt, chain=chain)
+    for key in ("draft", "topk_ids"):
+        assert np.array_equal(g[key], plain[key]), key
+    assert not np.allclose(g["conf"], plain["conf"])
+    # the hidden states themselves as the separate input change nothing
+    same, _ = gpu_propose(wl, hd, bt, chain=chain, conf_hidden=bt["hidden"])
+    for key in ("draft", "topk_ids", "topk_vals", "conf", "n_draft"):
+        assert np.array_equal(same[key], plain[key]), key
+
+
+def test_separate_confidence_input_full_size():
+    from workloads import make_conf_hidden
+    wl = WORKLOADS["qwen3_8b_b32"]
+    hd, bt = make_head(wl), make_batch(wl)
+    run_case(wl, chain="pruned", hd=hd, bt=bt, conf_hidden=make_conf_hidden(wl))
+
+
+def test_separate_confidence_input_adaptive():
+    from workloads import make_conf_hidden
+    wl = _small(r=32, conf_std=0.3, L_in=9, B=5)
+    hd, bt = make_head(wl), make_batch(wl)
+    run_case(wl, chain="pruned", hd=hd, bt=bt, conf_hidden=make_conf_hidden(wl),
+             skip_truncated=True)

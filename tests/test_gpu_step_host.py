@@ -4,7 +4,7 @@ kernels) and with pageable ones (copied through workspace staging)."""
 import numpy as np
 import pytest
 
-from workloads import Workload, make_batch, make_head, make_target
+from workloads import Workload, make_batch, make_conf_hidden, make_head, make_target
 
 pytestmark = pytest.mark.gpu
 
@@ -27,12 +27,14 @@ def _wl(**kw):
 @pytest.mark.parametrize("pinned", [True, False])
 @pytest.mark.parametrize("chain", ["dense", "pruned"])
 @pytest.mark.parametrize("with_topk", [True, False])
-def test_step_host_matches_device_path(pinned, chain, with_topk):
+@pytest.mark.parametrize("conf_input", [False, True])
+def test_step_host_matches_device_path(pinned, chain, with_topk, conf_input):
     from dspark_block_drafter_gb300 import _abi
     from dspark_block_drafter_gb300 import torch_io as tio
     wl = _wl()
     hd, bt = make_head(wl), make_batch(wl)
-    g, _ = gpu_propose(wl, hd, bt, chain=chain)
+    ch = make_conf_hidden(wl) if conf_input else None
+    g, _ = gpu_propose(wl, hd, bt, chain=chain, conf_hidden=ch)
     target = make_target(wl, g["draft"]).astype(np.int32)
 
     cfg = tio.make_config(wl.B, wl.L_in, wl.H, wl.V, wl.r, wl.top_k, wl.sample_from_anchor,
@@ -46,6 +48,7 @@ def test_step_host_matches_device_path(pinned, chain, with_topk):
         return t.pin_memory() if pinned else t
 
     hidden_h = host(tio.to_device(bt["hidden"], "cpu").contiguous())
+    ch_h = host(tio.to_device(ch, "cpu").contiguous()) if conf_input else None
     anchors_h = host(torch.from_numpy(np.ascontiguousarray(bt["anchors"], dtype=np.int32)))
     target_h = host(torch.from_numpy(np.ascontiguousarray(target)))
     i32 = dict(dtype=torch.int32)
@@ -61,7 +64,8 @@ def test_step_host_matches_device_path(pinned, chain, with_topk):
         cfg, head.struct(), hidden_h.data_ptr(), anchors_h.data_ptr(), target_h.data_ptr(),
         draft_h.data_ptr(), nd_h.data_ptr(), acc_h.data_ptr(), bon_h.data_ptr(),
         tki_h.data_ptr() if with_topk else 0, tkv_h.data_ptr() if with_topk else 0,
-        ws.data_ptr(), n, stream.cuda_stream))
+        ws.data_ptr(), n, stream.cuda_stream,
+        conf_hidden_h=None if ch_h is None else ch_h.data_ptr()))
     torch.cuda.synchronize()
     assert tio.device_status(ws) == 0
 

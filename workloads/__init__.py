@@ -26,11 +26,12 @@ import numpy as np
 
 __all__ = [
     "Workload", "WORKLOADS", "make_head", "make_batch", "make_target",
-    "to_bf16_bits", "slots_of",
+    "make_conf_hidden", "make_lattice_target", "to_bf16_bits", "slots_of",
 ]
 
 # sub-stream ids, one per tensor
-_S_LM_HEAD, _S_W1, _S_W2, _S_WCONF, _S_HIDDEN, _S_ANCHORS, _S_EMIT, _S_TARGET = range(1, 9)
+(_S_LM_HEAD, _S_W1, _S_W2, _S_WCONF, _S_HIDDEN, _S_ANCHORS, _S_EMIT, _S_TARGET,
+ _S_CONF_HIDDEN, _S_LATTICE) = range(1, 11)
 _ROW_CHUNK = 4096
 
 
@@ -202,4 +203,38 @@ def make_target(wl: Workload, draft: np.ndarray, batch_index: int = 0) -> np.nda
         target[b, :a] = draft[b, :a]
         if a < N:
             target[b, a] = (draft[b, a] + shift[b]) % wl.V
+    return target.astype(np.int32)
+
+
+def make_conf_hidden(wl: Workload, batch_index: int = 0) -> np.ndarray:
+    """A separate input of the confidence head, [B, L_in, H], N(0, 1) like the hidden
+    states but drawn from a sub-stream of its own."""
+    return _normal_rows(wl.seed + 1000 * batch_index, _S_CONF_HIDDEN, wl.B * wl.L_in, wl.H,
+                        1.0, wl.dtype, 8).reshape(wl.B, wl.L_in, wl.H)
+
+
+def make_lattice_target(wl: Workload, topk_ids: np.ndarray, batch_index: int = 0,
+                        p: Optional[float] = None) -> np.ndarray:
+    """Target argmax tokens [B, N+1] for verifying a candidate lattice topk_ids [B, N, k].
+
+    Along a seeded prefix (geometric length with mismatch probability p, default the
+    workload's accept_p or 0.5) the target's token at each slot is one of that slot's
+    candidates, at a uniformly drawn rank; at the end of the prefix it is a token that is
+    none of the slot's candidates; every later slot and the bonus slot are uniform.
+    """
+    ids = np.asarray(topk_ids, np.int64)
+    B, N, k = ids.shape
+    g = _rng(wl.seed + 1000 * batch_index, _S_LATTICE)
+    target = g.integers(0, wl.V, size=(B, N + 1))
+    p = p if p is not None else (wl.accept_p if wl.accept_p is not None else 0.5)
+    agree = g.geometric(p, size=B) - 1
+    ranks = g.integers(0, k, size=(B, N))
+    for b in range(B):
+        a = int(min(agree[b], N))
+        target[b, :a] = ids[b, np.arange(a), ranks[b, :a]]
+        if a < N:
+            x = int(g.integers(0, wl.V))
+            while x in set(ids[b, a].tolist()):
+                x = (x + 1) % wl.V
+            target[b, a] = x
     return target.astype(np.int32)
