@@ -1,4 +1,5 @@
 // The C ABI: argument validation, workspace carve-up and kernel dispatch.
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -38,13 +39,16 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
     return o;
   };
   w.ctrl = take(256);
-  w.bar = take(sizeof(unsigned) * (size_t)((B + 31) / 32));
+  w.bar = take(sizeof(unsigned) * (size_t)((B + 15) / 16));   // one per dense-chain launch
   w.keys = take(sizeof(unsigned long long) * (size_t)N * B);
   // the maxima of the lower bounds with which the GEMM leaves tiles of z out start from
   // zero (below every key) in every pass
   if (pruned) {
     w.zbound = take(sizeof(uint32_t) * (size_t)N * B * 2 * k);   // up to two maxima per rank
     w.walk_done = take(sizeof(int32_t) * (size_t)B);
+  } else if (dtype != DSPARK_F32) {   // the dense chain's candidate counts and bound maxima
+    w.dense_cnt = take(sizeof(int32_t) * (size_t)N * B);
+    w.dense_bucket = take(sizeof(uint32_t) * (size_t)N * B * kDenseBuckets);
   }
   w.zero_end = off;
   w.z = take(sizeof(float) * (size_t)N * w.Vhp * w.ldb);
@@ -56,9 +60,9 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
   if (dtype == DSPARK_F32) {          // the CUDA-core chain keeps one corrected row per block
     w.zc = take(sizeof(float) * (size_t)B * w.ldz);
     w.prev = take(sizeof(int32_t) * (size_t)B);
-  } else {                            // the tensor-core chain keeps per-CTA top-k partials
-    w.part_val = take(sizeof(float) * (size_t)N * B * kChainMaxCtas * k);
-    w.part_id = take(sizeof(int32_t) * (size_t)N * B * kChainMaxCtas * k);
+  } else if (!pruned) {               // the dense chain's candidate rows
+    w.dense_val = take(sizeof(float) * (size_t)N * B * kDenseCap);
+    w.dense_id = take(sizeof(int32_t) * (size_t)N * B * kDenseCap);
   }
   w.conf = take(sizeof(float) * (size_t)B * N);
   w.total = off;
@@ -191,8 +195,10 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   p.ldb = wl.ldb;
   p.zc = (float*)(ws + wl.zc);
   p.prev = (int32_t*)(ws + wl.prev);
-  p.part_val = (float*)(ws + wl.part_val);
-  p.part_id = (int32_t*)(ws + wl.part_id);
+  p.cand_val = (float*)(ws + wl.dense_val);
+  p.cand_id = (int32_t*)(ws + wl.dense_id);
+  p.cand_cnt = (int32_t*)(ws + wl.dense_cnt);
+  p.bucket = (uint32_t*)(ws + wl.dense_bucket);
   p.conf_ws = (float*)(ws + wl.conf);
   p.stream = (cudaStream_t)stream;
   if (pruned) {
@@ -250,7 +256,7 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   if (e != cudaSuccess) return cuda_fail(e, "base logits");
   if ((e = mark(DSPARK_STAGE_CHAIN)) != cudaSuccess) return cuda_fail(e, "event record");
   e = p.dtype == DSPARK_F32 ? launch_chain_simt(p)
-                            : (pruned ? launch_chain_pruned(p) : launch_chain_tc(p));
+                            : (pruned ? launch_chain_pruned(p) : launch_chain_dense(p));
   if (e != cudaSuccess) return cuda_fail(e, "chain");
   if ((e = mark(DSPARK_STAGE_TOPK)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = mark(DSPARK_NUM_STAGES)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -285,8 +291,17 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
   if (use_pruned(cfg, head) && !out->logits)            // GEMM; tables with the walk;
     return cfg->skip_truncated ? 3 : 2;                 // confidence first when adaptive
   const bool topk = out->topk_ids || out->topk_vals;
-  return 1 /* confidence */ + 1 /* GEMM */ + (cfg->B + 31) / 32 /* chain, 32 blocks each */ +
-         (topk ? 1 : 0);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    sms = 152;
+  }
+  const int group = dense_chain_group(head->V_head, sms);
+  const bool merge = topk && (cfg->top_k > 1 || !cfg->topk_markov);
+  return 1 /* confidence */ + 1 /* GEMM */ +
+         (cfg->B + group - 1) / std::max(group, 1) /* chain, one launch per group */ +
+         (merge ? 1 : 0);
 }
 
 // staging for dspark_step_host, placed after dspark_propose's workspace

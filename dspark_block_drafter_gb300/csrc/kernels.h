@@ -51,11 +51,13 @@ struct ProposePlan {
   float* logits;
   // workspace pieces
   uint32_t* ctrl;       // [0] = error word
-  unsigned int* bar;    // grid-barrier counters of the chain, one per launch (<= 32 blocks
-                        // apart)
+  unsigned int* bar;    // grid-barrier counters of the dense chain, one per 16 blocks
   unsigned long long* keys;  // [N][B] order keys of each slot's winner
-  float* part_val;      // [N][B][kChainMaxCtas][k] per-CTA top-k partials
-  int32_t* part_id;
+  float* cand_val;      // dense chain: [N][B][kDenseCap] rows that reach the slot's
+  int32_t* cand_id;     //   top-k bound, and their ranked values
+  int32_t* cand_cnt;    //   [N][B] how many (zeroed per pass)
+  uint32_t* bucket;     //   [N][B][kDenseBuckets] maxima of the CTAs' best values (order
+                        //   keys, zeroed per pass)
   float* zmax;          // per-tile maxima of z [N][B][Vhp / 128], or NULL (dense chain)
   const __nv_bfloat16* w2t;   // prepared head: markov_w2 transposed [Vhp][r], or NULL
   const float* cnorm;   // prepared head: column norms of markov_w2 [Vhp]
@@ -103,12 +105,15 @@ __host__ __device__ __forceinline__ size_t z_octet_index(size_t i, size_t v, siz
 
 // Upper bound on the chain kernel's grid (one CTA per SM).
 constexpr int kChainMaxCtas = 256;
+// Dense chain: candidate rows kept per (slot, block), and maxima that bound the top k.
+constexpr int kDenseCap = 256;
+constexpr int kDenseBuckets = 32;
 
 // Workspace carve-up shared by the size query and the launch.  [ctrl, zero_end) is
 // cleared at the start of every call.
 struct WorkspaceLayout {
-  size_t ctrl, bar, keys, zbound, walk_done, zero_end, z, zmax, zwritten, cand, zc, prev, conf, part_val,
-      part_id, total;
+  size_t ctrl, bar, keys, zbound, walk_done, dense_cnt, dense_bucket, zero_end, z, zmax,
+      zwritten, cand, zc, prev, conf, dense_val, dense_id, total;
   size_t Vhp, ldb, ldz;
 };
 WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool pruned);
@@ -172,7 +177,10 @@ cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, s
 cudaError_t launch_base_logits_tc(const ProposePlan& p);
 cudaError_t launch_base_logits_simt(const ProposePlan& p);
 cudaError_t launch_chain_simt(const ProposePlan& p);
-cudaError_t launch_chain_tc(const ProposePlan& p);
+cudaError_t launch_chain_dense(const ProposePlan& p);
+// Blocks per launch of the dense chain for a head of Vh rows on `sms` SMs (32 or 16), or
+// 0 when its per-CTA share of the Markov terms does not fit TMEM.
+int dense_chain_group(int Vh, int sms);
 cudaError_t launch_verify(int B, int N, const int32_t* draft, const int32_t* n_draft,
                           const int32_t* target, int32_t* accepted, int32_t* bonus,
                           int32_t* emitted, cudaStream_t stream);
