@@ -46,8 +46,7 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
   if (pruned) {
     w.zbound = take(sizeof(uint32_t) * (size_t)N * B * 2 * k);   // up to two maxima per rank
     w.walk_done = take(sizeof(int32_t) * (size_t)B);
-  } else if (dtype != DSPARK_F32) {   // the dense chain's candidate counts and bound maxima
-    w.dense_cnt = take(sizeof(int32_t) * (size_t)N * B);
+  } else if (dtype != DSPARK_F32) {   // the dense chain's bound maxima
     w.dense_bucket = take(sizeof(uint32_t) * (size_t)N * B * kDenseBuckets);
   }
   w.zero_end = off;
@@ -60,9 +59,11 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
   if (dtype == DSPARK_F32) {          // the CUDA-core chain keeps one corrected row per block
     w.zc = take(sizeof(float) * (size_t)B * w.ldz);
     w.prev = take(sizeof(int32_t) * (size_t)B);
-  } else if (!pruned) {               // the dense chain's candidate rows
-    w.dense_val = take(sizeof(float) * (size_t)N * B * kDenseCap);
-    w.dense_id = take(sizeof(int32_t) * (size_t)N * B * kDenseCap);
+  } else if (!pruned) {               // the dense chain's candidate rows, per CTA
+    const size_t per = (size_t)N * B * kChainMaxCtas;
+    w.dense_cnt = take(sizeof(int32_t) * per);
+    w.dense_val = take(sizeof(float) * per * kDenseLocal);
+    w.dense_id = take(sizeof(int32_t) * per * kDenseLocal);
   }
   w.conf = take(sizeof(float) * (size_t)B * N);
   w.total = off;

@@ -65,9 +65,9 @@ struct DenseArgs {
   int32_t* topk_ids;      // written here only for k = 1 over corrected logits (the argmax)
   float* topk_vals;
   float* logits;
-  float* cand_val;        // [N][B][kDenseCap] rows at or above the top-k bound
+  float* cand_val;        // [N][B][G][kDenseLocal] rows at or above the top-k bound
   int32_t* cand_id;
-  int32_t* cand_cnt;      // [N][B]
+  int32_t* cand_cnt;      // [N][B][G] how many this CTA found
   uint32_t* bucket;       // [N][B][kDenseBuckets] maxima of the CTAs' best values
   unsigned long long* keys;
   unsigned int* bar;
@@ -138,7 +138,8 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
   float* s_zb = (float*)(s_bi + kEpiWarps * 32);                       // [8][32]
   float* s_thv = s_zb + kEpiWarps * 32;                                // [32]
   int32_t* s_prev = (int32_t*)(s_thv + 32);                            // [32]
-  uint64_t* full = (uint64_t*)(((uintptr_t)(s_prev + 32) + 7) & ~(uintptr_t)7);
+  int* s_cnt = s_prev + 32;                                            // [32]
+  uint64_t* full = (uint64_t*)(((uintptr_t)(s_cnt + 32) + 7) & ~(uintptr_t)7);
   uint64_t* empty = full + a.stages;
   uint64_t* zfull = empty + a.stages;
   uint64_t* zempty = zfull + kZStages;
@@ -195,28 +196,38 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
   if (warp == kW2Warp || warp == kW2Warp + 1) {
     // ---------------------------------------------------------- markov_w2 producers
     // Producer j loads the stages of even (j = 0) or odd (j = 1) iteration numbers.
-    if (lane == 0) {
+    // A stage is 2 x (ks / 128) boxes of 128 K-rows x 64 columns (16 KB), one per lane:
+    // several issuing threads keep more boxes in flight than one.
+    {
       const uint32_t j = (uint32_t)(warp - kW2Warp);
       const uint32_t per_slot = (uint32_t)(nt * a.kstages);
       const uint32_t total = per_slot * (uint32_t)a.N;
+      const int nbox = 2 * (a.ks / 128);
       uint32_t it = j, issued_last = 0;
       bool ok = true, any = false;
       for (; ok && it < total; it += 2) {
         const uint32_t s = it % a.stages, ph = (it / a.stages) & 1;
-        if (!ptx::mbar_wait_sleep(&empty[s], ph ^ 1, kWaitBudget, abort_flag)) {
+        // (every lane waits: a warp whose lanes sit diverged in a wait slows the warp
+        // collectives of the whole SM)
+        const bool w_ok =
+            __all_sync(0xFFFFFFFFu, ptx::mbar_wait_sleep(&empty[s], ph ^ 1, kWaitBudget, abort_flag));
+        if (w_ok && lane == 0) ptx::mbar_arrive_expect_tx(&full[s], a.stage);
+        __syncwarp();
+        if (!w_ok) {
           ok = false;
           break;
         }
         const uint32_t w = it % per_slot;
         const int t = t_begin + (int)(w / a.kstages), kst = (int)(w % a.kstages);
-        uint8_t* dst = s_w2 + (size_t)s * a.stage;
-        ptx::mbar_arrive_expect_tx(&full[s], a.stage);
-        ptx::tma_load_2d(dst, &tm_w2, &full[s], t * kTileV, kst * a.ks);
-        ptx::tma_load_2d(dst + a.box, &tm_w2, &full[s], t * kTileV + 64, kst * a.ks);
+        if (lane < nbox) {
+          const int half = lane & 1, kq = lane >> 1;        // column half, 128-row block
+          uint8_t* dst = s_w2 + (size_t)s * a.stage + half * a.box + kq * 16384;
+          ptx::tma_load_2d(dst, &tm_w2, &full[s], t * kTileV + half * 64, kst * a.ks + kq * 128);
+        }
         issued_last = it;
         any = true;
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         give_up();
         // the copies of this producer still in flight (among the last `stages` issued)
         // land before the CTA winds down
@@ -231,22 +242,27 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
     }
   } else if (warp == kZWarp) {
     // ---------------------------------------------------------- base-logit producer
-    if (lane == 0) {
+    // (all lanes run the loop in step; lane 0 issues)
+    {
       const uint32_t total = (uint32_t)(nt * a.N);
       uint32_t it = 0;
       bool ok = true;
       for (; ok && it < total; ++it) {
         const uint32_t s = it % kZStages, ph = (it / kZStages) & 1;
-        if (!ptx::mbar_wait_sleep(&zempty[s], ph ^ 1, kWaitBudget, abort_flag)) {
+        if (!__all_sync(0xFFFFFFFFu,
+                        ptx::mbar_wait_sleep(&zempty[s], ph ^ 1, kWaitBudget, abort_flag))) {
           ok = false;
           break;
         }
         const int slot = (int)(it / nt), t = t_begin + (int)(it % nt);
-        ptx::mbar_arrive_expect_tx(&zfull[s], kZStage);
-        ptx::tma_load_2d(s_z + (size_t)s * kZStage, &tm_z, &zfull[s], a.b0,
-                         (int)((size_t)slot * a.Vhp) + t * kTileV);
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&zfull[s], kZStage);
+          ptx::tma_load_2d(s_z + (size_t)s * kZStage, &tm_z, &zfull[s], a.b0,
+                           (int)((size_t)slot * a.Vhp) + t * kTileV);
+        }
+        __syncwarp();
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         give_up();
         const uint32_t first = it > (uint32_t)kZStages ? it - kZStages : 0;
         for (uint32_t q = first; q < it; ++q)
@@ -255,20 +271,22 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // (all lanes run the loop in step and wait together; lane 0 issues)
+    {
       const uint32_t idesc = ptx::idesc_bf16_f32(kTileV, a.n_mma, /*A MN-major*/ 1, 0);
       const uint32_t u0 = ptx::smem_u32(s_u);
       uint32_t it = 0;
       bool ok = true;
       for (int step = 0; ok && step < a.N; ++step) {
-        if (!ptx::mbar_wait_sleep(u_ready, step & 1, kWaitBudget, abort_flag)) {
+        if (!__all_sync(0xFFFFFFFFu,
+                        ptx::mbar_wait_sleep(u_ready, step & 1, kWaitBudget, abort_flag))) {
           ok = false;
           break;
         }
         const int buf = a.dbuf ? (step & 1) : 0;
         const int use = a.dbuf ? (step >> 1) : step;
-        if (use > 0 &&
-            !ptx::mbar_wait_sleep(&tmem_free[buf], (use - 1) & 1, kWaitBudget, abort_flag)) {
+        if (use > 0 && !__all_sync(0xFFFFFFFFu, ptx::mbar_wait_sleep(&tmem_free[buf], (use - 1) & 1,
+                                                                      kWaitBudget, abort_flag))) {
           ok = false;
           break;
         }
@@ -277,26 +295,33 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
           const uint32_t d = tmem + col_of(step, lt);
           for (int kst = 0; kst < a.kstages; ++kst, ++it) {
             const uint32_t s = it % a.stages, ph = (it / a.stages) & 1;
-            if (!ptx::mbar_wait_sleep(&full[s], ph, kWaitBudget, abort_flag)) {
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait_sleep(&full[s], ph, kWaitBudget, abort_flag))) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            const uint32_t w0 = ptx::smem_u32(s_w2 + (size_t)s * a.stage);
-            for (int kk = 0; kk < a.ks / 16; ++kk) {
-              const uint32_t kb = (uint32_t)(kst * (a.ks / 64) + kk / 4);
-              ptx::mma_f16(d, ptx::desc_mnmajor_sw128(w0 + kk * 2048, a.box, 1024),
-                           ptx::desc_kmajor_sw128(u0 + kb * a.u_kb_bytes + (kk % 4) * 32),
-                           idesc, (kst | kk) != 0);
+            if (lane == 0) {
+              const uint32_t w0 = ptx::smem_u32(s_w2 + (size_t)s * a.stage);
+              for (int kk = 0; kk < a.ks / 16; ++kk) {
+                const uint32_t kb = (uint32_t)(kst * (a.ks / 64) + kk / 4);
+                ptx::mma_f16(d, ptx::desc_mnmajor_sw128(w0 + kk * 2048, a.box, 1024),
+                             ptx::desc_kmajor_sw128(u0 + kb * a.u_kb_bytes + (kk % 4) * 32),
+                             idesc, (kst | kk) != 0);
+              }
+              ptx::mma_commit(&empty[s]);
             }
-            ptx::mma_commit(&empty[s]);
+            __syncwarp();
           }
-          if (ok) ptx::mma_commit(&acc_full[(a.dbuf ? (step & 1) : 0) * a.tmax + lt]);
+          if (ok && lane == 0) ptx::mma_commit(&acc_full[(a.dbuf ? (step & 1) : 0) * a.tmax + lt]);
+          __syncwarp();
         }
       }
-      if (!ok) give_up();
-      ptx::mma_commit(drain);
-      ptx::mbar_wait_sleep(drain, 0, kWaitBudget, nullptr);
+      if (!ok && lane == 0) give_up();
+      if (lane == 0) {
+        ptx::mma_commit(drain);
+        ptx::mbar_wait_sleep(drain, 0, kWaitBudget, nullptr);
+      }
+      __syncwarp();
     }
   } else {
     // ---------------------------------------------------------------- epilogue
@@ -374,72 +399,212 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
       epi_sync();
     };
 
+    // Bound of each block's top k for slot `step`: the k-th largest of its nb bucket
+    // maxima (an empty bucket reads as -inf).  One warp per block, lane j ranks bucket j
+    // (ties by index); a warp's four blocks load their buckets together.
+    constexpr int kPer = 32 / kEpiWarps;
+    auto load_bound = [&](int step, uint32_t (&kb)[kPer]) {
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int c = warp + q * kEpiWarps;
+        const size_t sb = (size_t)step * a.B + a.b0 + c;
+        kb[q] = (c < a.Bg && lane < a.nb) ? __ldcg(&a.bucket[sb * kDenseBuckets + lane]) : 0u;
+      }
+    };
+    auto rank_bound = [&](const uint32_t (&kb)[kPer]) {
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int c = warp + q * kEpiWarps;
+        if (c >= a.Bg) break;                           // (uniform over the warp)
+        int rank = 0;
+        for (int h = 0; h < a.nb; ++h) {
+          const uint32_t y = __shfl_sync(0xFFFFFFFFu, kb[q], h);
+          rank += (y > kb[q]) | ((y == kb[q]) & (h < lane));
+        }
+        if (lane < a.nb && rank == a.k - 1)
+          s_thv[c] = kb[q] == 0u ? -INFINITY : order_key32_value((int)(kb[q] ^ 0x80000000u));
+      }
+    };
+    // The rows of tile lt of slot `step` at or above their block's bound (in s_thv) go
+    // to this CTA's list of the block: a few over the whole grid.
+    auto scan_tile = [&](int step, int lt) {
+      const int v = (t_begin + lt) * kTileV + row;
+      const uint32_t taddr = tmem + lane_base + col_of(step, lt);
+      for (int c0 = 0; c0 < a.Bg; c0 += 8) {
+        uint32_t r[8];
+        __syncwarp();                                     // (after the divergent appends)
+        ptx::tmem_ld_32x32b_x8(taddr + c0, r);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float x = __uint_as_float(r[j]);
+          if (v < a.Vh && c0 + j < a.Bg && x >= s_thv[c0 + j]) {
+            // a place in this CTA's list (shared-memory counter), then plain stores:
+            // nothing waits on the memory system while markov_w2 streams
+            const int e = atomicAdd(&s_cnt[c0 + j], 1);
+            if (e < kDenseLocal) {
+              const size_t o =
+                  (((size_t)step * a.B + a.b0 + c0 + j) * G + blockIdx.x) * kDenseLocal + e;
+              a.cand_val[o] = x;
+              a.cand_id[o] = v;
+            }
+          }
+        }
+      }
+      __syncwarp();
+    };
+    // After a slot's scan: this CTA's count of each block's candidates (more than
+    // kDenseLocal: its list overflowed), and the counters restart.  (After an epi_sync.)
+    auto publish_counts = [&](int step) {
+      if (tid < a.Bg) {
+        a.cand_cnt[((size_t)step * a.B + a.b0 + tid) * G + blockIdx.x] = s_cnt[tid];
+        s_cnt[tid] = 0;
+      }
+    };
+    // With two TMEM buffers, slot s's scan runs inside slot s + 1's first pass, tile by
+    // tile, before each tile's wait for its MMA; with one it runs after the barrier.
+    const bool fuse = TOPK && a.dbuf;
+
     bool ok = true;
+    if (tid < 32) s_cnt[tid] = 0;
     load_prev(0);
     gather_u();
     for (int step = 0; ok && step < a.N; ++step) {
       const int buf = a.dbuf ? (step & 1) : 0;
       const int use = a.dbuf ? (step >> 1) : step;
-      // -------- 3. pass 1: z' = z + m, back into TMEM; running maxima per block
-      float mv[32];                 // best corrected value of each block in this thread
-      int mi[32];                   // its head row
-      float zm[ZRANK ? 32 : 1];     // best base value (top-k over base logits)
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        mv[c] = -INFINITY;
-        mi[c] = 0x7FFFFFFF;
-        if (ZRANK) zm[c] = -INFINITY;
+      // -------- 3. pass 1: z' = z + m, back into TMEM.  Each chunk of 16 blocks is
+      //            reduced across the warp at once (redux on order keys: the largest value,
+      //            then the lowest row holding it), and lane j keeps the warp's running
+      //            best of block c0 + j in shared memory.  A compact loop: this code runs
+      //            once per tile, so the instruction cache stays warm.
+      if (lane < 32) {
+        s_bv[warp * 32 + lane] = -INFINITY;
+        s_bi[warp * 32 + lane] = 0x7FFFFFFF;
+        if (ZRANK) s_zb[warp * 32 + lane] = -INFINITY;
       }
+      __syncwarp();
       for (int lt = par; lt < nt; lt += 2) {
         const int v = (t_begin + lt) * kTileV + row;
         const bool v_ok = v < a.Vh;
+        const bool scan_prev = fuse && step > 0;
+        const bool two = a.n_mma > 16;
+        uint32_t rp[32];                                  // the previous slot's z' (fused scan)
+        if (scan_prev) {
+          const uint32_t pa = tmem + lane_base + col_of(step - 1, lt);
+          __syncwarp();
+          ptx::tmem_ld_32x32b_x16(pa, *reinterpret_cast<uint32_t(*)[16]>(&rp[0]));
+          if (two) ptx::tmem_ld_32x32b_x16(pa + 16, *reinterpret_cast<uint32_t(*)[16]>(&rp[16]));
+        }
         const uint32_t zit = (uint32_t)(step * nt + lt);
         const uint32_t zs = zit % kZStages, zph = (zit / kZStages) & 1;
         bool w_ok = ptx::mbar_wait_sleep(&zfull[zs], zph, kWaitBudget, abort_flag);
         w_ok = w_ok && ptx::mbar_wait_sleep(&acc_full[buf * a.tmax + lt], use & 1, kWaitBudget,
                                             abort_flag);
         ok = __all_sync(0xFFFFFFFFu, w_ok);
-        if (!ok) break;
+        if (!ok) {
+          ptx::tmem_ld_wait();
+          break;
+        }
         ptx::tc_fence_after();
         const uint8_t* zrow = s_z + (size_t)zs * kZStage + (size_t)row * 128;
         const uint32_t taddr = tmem + lane_base + col_of(step, lt);
+        uint32_t r[32];                                   // this slot's Markov terms
+        ptx::tmem_ld_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+        if (two) ptx::tmem_ld_32x32b_x16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+        float zv[32];
 #pragma unroll
-        for (int c0 = 0; c0 < 32; c0 += 16) {             // (unrolled: c0 indexes registers)
-          if (c0 >= a.n_mma) break;
-          uint32_t r[16];
-          __syncwarp();                                   // (tcgen05 loads are .aligned)
-          ptx::tmem_ld_32x32b_x16(taddr + c0, r);
-          float zv[16];
+        for (int q = 0; q < 8; ++q) {                     // 16-byte chunk q of the row, swizzled
+          if (q >= 4 && !two) break;
+          const float4 f = *reinterpret_cast<const float4*>(zrow + ((q ^ (row & 7)) << 4));
+          zv[4 * q] = f.x;
+          zv[4 * q + 1] = f.y;
+          zv[4 * q + 2] = f.z;
+          zv[4 * q + 3] = f.w;
+        }
+        ptx::tmem_ld_wait();
+        // the previous slot's candidates of this tile: rows at or above their block's
+        // bound.  The bounds are read first and the hits found without a branch, so that
+        // nothing serialises the loop; hits themselves are rare.
+        if (scan_prev) {
+          uint32_t hit = 0;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {                 // 16-byte chunk c0/4 + q, swizzled
-            const float4 f = *reinterpret_cast<const float4*>(
-                zrow + (((c0 / 4 + q) ^ (row & 7)) << 4));
-            zv[4 * q] = f.x;
-            zv[4 * q + 1] = f.y;
-            zv[4 * q + 2] = f.z;
-            zv[4 * q + 3] = f.w;
+          for (int q = 0; q < 8; ++q) {
+            const float4 t4 = *reinterpret_cast<const float4*>(s_thv + 4 * q);
+            hit |= (__uint_as_float(rp[4 * q]) >= t4.x ? 1u : 0u) << (4 * q);
+            hit |= (__uint_as_float(rp[4 * q + 1]) >= t4.y ? 1u : 0u) << (4 * q + 1);
+            hit |= (__uint_as_float(rp[4 * q + 2]) >= t4.z ? 1u : 0u) << (4 * q + 2);
+            hit |= (__uint_as_float(rp[4 * q + 3]) >= t4.w ? 1u : 0u) << (4 * q + 3);
           }
-          ptx::tmem_ld_wait();
-          uint32_t back[16];
+          hit &= v_ok ? (a.Bg >= 32 ? 0xFFFFFFFFu : ((1u << a.Bg) - 1u)) : 0u;
+          while (hit) {
+            const int j = __ffs(hit) - 1;
+            hit &= hit - 1;
+            uint32_t xb = rp[0];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float x = v_ok ? zv[j] + __uint_as_float(r[j]) : -INFINITY;
-            const float zr = v_ok ? zv[j] : -INFINITY;
-            back[j] = __float_as_uint(ZRANK ? zr : x);
-            const int c = c0 + j;
-            if (x > mv[c]) {                             // rows rise: the lowest id wins ties
-              mv[c] = x;
-              mi[c] = v;
+            for (int q = 1; q < 32; ++q) xb = j == q ? rp[q] : xb;
+            const int e = atomicAdd(&s_cnt[j], 1);
+            if (e < kDenseLocal) {
+              const size_t o =
+                  (((size_t)(step - 1) * a.B + a.b0 + j) * G + blockIdx.x) * kDenseLocal + e;
+              a.cand_val[o] = __uint_as_float(xb);
+              a.cand_id[o] = v;
             }
-            if (ZRANK) zm[c] = fmaxf(zm[c], zr);
-            if (a.logits && v_ok && c < a.Bg)
-              a.logits[((size_t)(a.b0 + c) * a.N + step) * a.Vh + v] = x;
           }
-          __syncwarp();
-          if (TOPK) ptx::tmem_st_32x32b_x16(taddr + c0, back);
         }
         __syncwarp();
-        if (TOPK) ptx::tmem_st_wait();
+        // z' = z + m (or -inf past the head), back into r for the top-k scan; then each
+        // block's best over the warp's 32 rows: all keys first, then the reductions back
+        // to back (they are independent), lane j keeping block j's result
+        const int ncol = two ? 32 : 16;
+        int kx[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j >= ncol) break;
+          const float x = v_ok ? zv[j] + __uint_as_float(r[j]) : -INFINITY;
+          kx[j] = order_key32(canon(x));
+          r[j] = __float_as_uint(ZRANK ? (v_ok ? zv[j] : -INFINITY) : x);
+          if (a.logits && v_ok && j < a.Bg)               // (tests only)
+            a.logits[((size_t)(a.b0 + j) * a.N + step) * a.Vh + v] = x;
+        }
+        int mk = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j >= ncol) break;
+          const int m = __reduce_max_sync(0xFFFFFFFFu, kx[j]);
+          kx[j] = kx[j] == m ? v : 0x7FFFFFFF;            // (now the candidate row)
+          if (lane == j) mk = m;
+        }
+        int mid = 0x7FFFFFFF;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j >= ncol) break;
+          const int id = (int)__reduce_min_sync(0xFFFFFFFFu, (unsigned)kx[j]);
+          if (lane == j) mid = id;
+        }
+        float mzv = -INFINITY;
+        if (ZRANK) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j >= ncol) break;
+            const int mz = __reduce_max_sync(0xFFFFFFFFu, order_key32(v_ok ? zv[j] : -INFINITY));
+            if (lane == j) mzv = order_key32_value(mz);
+          }
+        }
+        if (lane < ncol) {                                 // rows rise with the tiles: on
+          const int c = warp * 32 + lane;                 // equal values the earlier,
+          const float bv = order_key32_value(mk);         // lower row stays
+          if (better(bv, mid, s_bv[c], s_bi[c])) {
+            s_bv[c] = bv;
+            s_bi[c] = mid;
+          }
+          if (ZRANK) s_zb[c] = fmaxf(s_zb[c], mzv);
+        }
+        __syncwarp();
+        if (TOPK) {
+          ptx::tmem_st_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+          if (two) ptx::tmem_st_32x32b_x16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+          ptx::tmem_st_wait();
+        }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&zempty[zs]);
       }
@@ -450,36 +615,14 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
         ok = false;
         break;
       }
-      // -------- 4. argmax: a shuffle network leaves block `lane`'s best of the warp in
-      //            lane `lane`; then the warps, then the grid
-#pragma unroll
-      for (int h = 16; h >= 1; h >>= 1) {
-        const bool upper = (lane & h) != 0;
-#pragma unroll
-        for (int j = 0; j < h; ++j) {
-          const float send_v = upper ? mv[j] : mv[j + h];
-          const int send_i = upper ? mi[j] : mi[j + h];
-          float keep_v = upper ? mv[j + h] : mv[j];
-          int keep_i = upper ? mi[j + h] : mi[j];
-          const float ov = __shfl_xor_sync(0xFFFFFFFFu, send_v, h);
-          const int oi = __shfl_xor_sync(0xFFFFFFFFu, send_i, h);
-          if (better(ov, oi, keep_v, keep_i)) {
-            keep_v = ov;
-            keep_i = oi;
-          }
-          mv[j] = keep_v;
-          mi[j] = keep_i;
-          if (ZRANK) {                                   // the base values' maxima alike
-            const float sz = upper ? zm[j] : zm[j + h];
-            const float kz = upper ? zm[j + h] : zm[j];
-            zm[j] = fmaxf(kz, __shfl_xor_sync(0xFFFFFFFFu, sz, h));
-          }
-        }
-      }
-      s_bv[warp * 32 + lane] = mv[0];
-      s_bi[warp * 32 + lane] = mi[0];
-      if (ZRANK) s_zb[warp * 32 + lane] = zm[0];
+      // -------- 4. argmax: the warps' bests (in shared memory), then the grid
+      ptx::tc_fence_before();
       epi_sync();
+      // (fused: every warp has scanned the previous slot's TMEM columns; they are free)
+      if (fuse && step > 0) {
+        if (tid == 0) ptx::mbar_arrive(&tmem_free[(step - 1) & 1]);
+        publish_counts(step - 1);
+      }
       if (tid < a.Bg) {
         float bv = s_bv[tid];
         int bi = s_bi[tid];
@@ -502,13 +645,14 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
         // arrive on the grid barrier; the release orders this thread's atomics first
         red_release_add(a.bar, 1u);
       }
-      // -------- 5. the grid barrier: every CTA has published this slot's winners
-      if (tid == 0) {
+      // -------- 5. the grid barrier: every CTA has published this slot's winners.
+      //            (Warp 0 polls with all its lanes, in step.)
+      if (warp == 0) {
         const unsigned target = (unsigned)(step + 1) * (unsigned)G * (unsigned)a.Bg;
         const long long t0 = clock64();
-        while (ld_acquire(a.bar) < target) {
-          if (clock64() - t0 > kWaitBudget) {
-            give_up();
+        while (__all_sync(0xFFFFFFFFu, ld_acquire(a.bar) < target)) {
+          if (__any_sync(0xFFFFFFFFu, clock64() - t0 > kWaitBudget)) {
+            if (lane == 0) give_up();
             break;
           }
           __nanosleep(32);
@@ -518,59 +662,30 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
         ok = false;
         break;
       }
-      // -------- 6. the next slot's previous tokens and u: its MMAs start
+      // -------- 6. the next slot's previous tokens and u: its MMAs start.  (This slot's
+      //            bucket maxima are loaded first, while the memory system is quiet.)
+      uint32_t kb[kPer];
+      if (TOPK) load_bound(step, kb);
       load_prev(step + 1);
       if (step + 1 < a.N) gather_u();
-      // -------- 7. this slot's top-k candidates, while the next slot's MMAs run
+      // -------- 7. this slot's top-k scan: fused into the next slot's first pass, or
+      //            here when TMEM holds one slot
       if (TOPK) {
-        // bound of each block: the k-th largest of its nb bucket maxima (an empty bucket
-        // reads as -inf); one warp per block, lane j ranks bucket j (ties by index)
-        for (int c = warp; c < a.Bg; c += kEpiWarps) {
-          const size_t sb = (size_t)step * a.B + a.b0 + c;
-          const uint32_t kb = lane < a.nb ? __ldcg(&a.bucket[sb * kDenseBuckets + lane]) : 0u;
-          int rank = 0;
-          for (int h = 0; h < a.nb; ++h) {
-            const uint32_t y = __shfl_sync(0xFFFFFFFFu, kb, h);
-            rank += (y > kb) | ((y == kb) & (h < lane));
-          }
-          if (lane < a.nb && rank == a.k - 1)
-            s_thv[c] = kb == 0u ? -INFINITY : order_key32_value((int)(kb ^ 0x80000000u));
-        }
+        rank_bound(kb);
         epi_sync();
-        // rows at or above the bound go to the block's list (a few over the whole grid)
-        for (int lt = par; lt < nt; lt += 2) {
-          const int v = (t_begin + lt) * kTileV + row;
-          const uint32_t taddr = tmem + lane_base + col_of(step, lt);
-#pragma unroll
-          for (int c0 = 0; c0 < 32; c0 += 16) {
-            if (c0 >= a.n_mma) break;
-            uint32_t r[16];
-            __syncwarp();                                 // (after the divergent appends)
-            ptx::tmem_ld_32x32b_x16(taddr + c0, r);
-            float th[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) th[j] = s_thv[c0 + j];
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float x = __uint_as_float(r[j]);
-              if (v < a.Vh && c0 + j < a.Bg && x >= th[j]) {
-                const size_t sb = (size_t)step * a.B + a.b0 + c0 + j;
-                const int e = atomicAdd(&a.cand_cnt[sb], 1);
-                if (e < kDenseCap) {
-                  a.cand_val[sb * kDenseCap + e] = x;
-                  a.cand_id[sb * kDenseCap + e] = v;
-                }
-              }
-            }
-          }
+        if (!fuse || step + 1 == a.N) {
+          for (int lt = par; lt < nt; lt += 2) scan_tile(step, lt);
+          epi_sync();
+          publish_counts(step);
         }
       }
-      // this slot's TMEM columns are free for the MMA of a later slot
-      __syncwarp();
-      ptx::tc_fence_before();
-      epi_sync();
-      if (tid == 0) ptx::mbar_arrive(&tmem_free[buf]);
+      if (!fuse) {
+        // this slot's TMEM columns are free for the MMA of a later slot
+        __syncwarp();
+        ptx::tc_fence_before();
+        epi_sync();
+        if (tid == 0) ptx::mbar_arrive(&tmem_free[buf]);
+      }
     }
   }
   __syncwarp();
@@ -587,9 +702,9 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
 // the top k.  Sorted by (value descending, id ascending); a list that overflowed is
 // replaced by an exact evaluation of every head row of that slot and block.
 struct FinalArgs {
-  const float* cand_val;
+  const float* cand_val;            // [N][B][G][kDenseLocal]
   const int32_t* cand_id;
-  const int32_t* cand_cnt;
+  const int32_t* cand_cnt;          // [N][B][G]
   const unsigned long long* keys;   // [N][B] winners (previous tokens of the recompute)
   const int32_t* anchors;
   const int32_t* d2t;
@@ -600,7 +715,7 @@ struct FinalArgs {
   float* vals;
   uint32_t* err;
   size_t Vhp, ldb;
-  int B, N, V, Vh, r, k, zrank;
+  int B, N, V, Vh, r, k, zrank, G;
 };
 
 constexpr int kFinalThreads = 256;
@@ -610,25 +725,41 @@ topk_final(const FinalArgs a) {
   const int i = blockIdx.x / a.B, b = blockIdx.x % a.B;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const size_t sb = (size_t)i * a.B + b;
-  const int n = a.cand_cnt[sb];
   __shared__ float s_v[kDenseCap];
   __shared__ int s_i[kDenseCap];
   __shared__ float s_wv[kFinalThreads / 32];
   __shared__ int s_wi[kFinalThreads / 32];
   __shared__ float s_u[512];
+  __shared__ int s_n, s_over;
   auto out = [&](int q, float v, int id) {
     const size_t o = ((size_t)b * a.N + i) * a.k + q;
     const int hrow = (id >= 0 && id < a.Vh) ? id : 0;
     if (a.ids) a.ids[o] = a.d2t ? a.d2t[hrow] : hrow;
     if (a.vals) a.vals[o] = v;
   };
-  if (n <= kDenseCap) {
-    for (int e = tid; e < n; e += kFinalThreads) {
-      s_v[e] = a.cand_val[sb * kDenseCap + e];
-      s_i[e] = a.cand_id[sb * kDenseCap + e];
+  if (tid == 0) {
+    s_n = 0;
+    s_over = 0;
+  }
+  __syncthreads();
+  // the CTAs' lists of this slot and block, gathered into one (thread t: CTA t)
+  for (int t = tid; t < a.G; t += kFinalThreads) {
+    const int n = a.cand_cnt[sb * a.G + t];
+    if (n > kDenseLocal) s_over = 1;
+    for (int e = 0; e < min(n, kDenseLocal); ++e) {
+      const int pos = atomicAdd(&s_n, 1);
+      if (pos < kDenseCap) {
+        s_v[pos] = a.cand_val[(sb * a.G + t) * kDenseLocal + e];
+        s_i[pos] = a.cand_id[(sb * a.G + t) * kDenseLocal + e];
+      } else {
+        s_over = 1;
+      }
     }
-    __syncthreads();
+  }
+  __syncthreads();
+  if (!s_over) {
     if (warp != 0) return;
+    const int n = s_n;
     // k rounds of a warp-wide best strictly after the previous pick
     float pv = 0.f;
     int pid = 0;
@@ -791,7 +922,7 @@ cudaError_t launch_chain_dense(const ProposePlan& p) {
   {
     cuuint64_t dims[2] = {(cuuint64_t)p.Vh, (cuuint64_t)p.r};
     cuuint64_t strides[1] = {(cuuint64_t)p.Vh * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)ks};
+    cuuint32_t box[2] = {64, 128};
     cuuint32_t es[2] = {1, 1};
     if (encode(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)p.w2, dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -851,8 +982,8 @@ cudaError_t launch_chain_dense(const ProposePlan& p) {
     a.tmem_cols = cols;
     a.u_kb_bytes = (uint32_t)a.n_mma * 128;
     a.nb = std::min(kDenseBuckets, std::max(2, 2 * p.k));
-    // s_bv, s_bi, s_zb, s_thv, s_prev; then the barriers and four words
-    const size_t misc = (size_t)3 * kEpiWarps * 32 * 4 + 2 * 32 * 4 + 8 +
+    // s_bv, s_bi, s_zb, s_thv, s_prev, s_cnt; then the barriers and four words
+    const size_t misc = (size_t)3 * kEpiWarps * 32 * 4 + 3 * 32 * 4 + 8 +
                         8 * ((size_t)2 * 4 + 2 * kZStages + 2 * tmax + 4) + 16;
     const size_t fixed = 1024 + (size_t)kZStages * kZStage +
                          (size_t)a.kb_count * a.u_kb_bytes + misc;
@@ -891,6 +1022,7 @@ cudaError_t launch_chain_dense(const ProposePlan& p) {
     f.r = p.r;
     f.k = p.k;
     f.zrank = zrank ? 1 : 0;
+    f.G = grid;
     if (p.r > 512) return cudaErrorInvalidValue;
     topk_final<<<p.B * p.N, kFinalThreads, 0, p.stream>>>(f);
     return cudaGetLastError();

@@ -53,9 +53,9 @@ struct ProposePlan {
   uint32_t* ctrl;       // [0] = error word
   unsigned int* bar;    // grid-barrier counters of the dense chain, one per 16 blocks
   unsigned long long* keys;  // [N][B] order keys of each slot's winner
-  float* cand_val;      // dense chain: [N][B][kDenseCap] rows that reach the slot's
-  int32_t* cand_id;     //   top-k bound, and their ranked values
-  int32_t* cand_cnt;    //   [N][B] how many (zeroed per pass)
+  float* cand_val;      // dense chain: [N][B][kChainMaxCtas][kDenseLocal] rows of each
+  int32_t* cand_id;     //   CTA that reach the slot's top-k bound, their ranked values
+  int32_t* cand_cnt;    //   [N][B][kChainMaxCtas] how many each CTA found
   uint32_t* bucket;     //   [N][B][kDenseBuckets] maxima of the CTAs' best values (order
                         //   keys, zeroed per pass)
   float* zmax;          // per-tile maxima of z [N][B][Vhp / 128], or NULL (dense chain)
@@ -105,7 +105,9 @@ __host__ __device__ __forceinline__ size_t z_octet_index(size_t i, size_t v, siz
 
 // Upper bound on the chain kernel's grid (one CTA per SM).
 constexpr int kChainMaxCtas = 256;
-// Dense chain: candidate rows kept per (slot, block), and maxima that bound the top k.
+// Dense chain: candidate rows kept per (slot, block, CTA) and per (slot, block), and the
+// number of maxima that bound the top k.
+constexpr int kDenseLocal = 4;
 constexpr int kDenseCap = 256;
 constexpr int kDenseBuckets = 32;
 
