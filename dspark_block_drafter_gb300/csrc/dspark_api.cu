@@ -31,7 +31,7 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
   WorkspaceLayout w{};
   w.ldz = align_up((size_t)Vh, 64);
   w.Vhp = align_up((size_t)Vh, 128);
-  w.ldb = align_up((size_t)B, 4);
+  w.ldb = align_up((size_t)B, 8);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;

@@ -14,14 +14,17 @@
 //      B operand (K-major, 128-byte swizzled; N = blocks padded to 16 or 32);
 //   2. two producer warps stream markov_w2 in [K-rows x 128 columns] stages by TMA
 //      (MN-major A operand; the same tiles every slot, so they run ahead across slots),
-//      and a third streams the slot's base logits z, [128 rows x 32 blocks] per tile;
+//      and a third streams the slot's base logits z, [128 rows x 32 blocks] per tile,
+//      with an evict-first L2 policy (z is read once; markov_w2 stays in L2);
 //   3. the MMA thread issues m[v, b] = sum_k w2[k, v] u[b, k] for every tile (tcgen05,
 //      M = 128 head rows) into the slot's TMEM columns;
-//   4. pass 1 (the critical path): thread = head row, 16 blocks at a time; z' = z + m
-//      goes back into TMEM, and each thread keeps a running maximum per block.  A
-//      shuffle network gives each lane one block's best of the warp, shared memory the
-//      CTA's, a 64-bit atomicMax the grid's; each block's thread then arrives on the grid
-//      barrier with a release;
+//   4. pass 1 (the critical path): every epilogue warp takes every tile, thread = one
+//      head row of its TMEM lane quadrant x half of the blocks; z' = z + m goes back into
+//      TMEM, and each thread keeps a running best per block (value and tile).  After the
+//      last tile a shuffle network gives each lane one block's best of the warp, shared
+//      memory the CTA's, a 64-bit atomicMax the grid's; each block's thread then arrives
+//      on the grid barrier with a release and pulls the markov_w1 row of its CTA's best
+//      into L2 (the next slot gathers one of those rows);
 //   5. once the barrier completes, the epilogue gathers the next slot's u (so its MMAs
 //      start) and then, while they run, finds this slot's top-k candidates: every CTA
 //      also posted its best value of each block into one of 2k bucket maxima (the CTA
@@ -49,7 +52,7 @@ namespace {
 
 constexpr int kTileV = 128;
 constexpr uint32_t kZStage = kTileV * 32 * 4;           // base logits of a tile: 16 KB
-constexpr int kEpiWarps = 8;                            // 4 TMEM quadrants x 2 tile parities
+constexpr int kEpiWarps = 8;                            // 4 TMEM quadrants x 2 block halves
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kMmaWarp = 8, kZWarp = 9, kW2Warp = 10;   // two markov_w2 producers: 10, 11
 constexpr int kThreads = 32 * 12;
@@ -160,7 +163,7 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
     }
     for (int s = 0; s < kZStages; ++s) {
       ptx::mbar_init(&zfull[s], 1);
-      ptx::mbar_init(&zempty[s], 4);              // the four warps of one tile parity
+      ptx::mbar_init(&zempty[s], kEpiWarps);      // every epilogue warp reads every tile
     }
     for (int q = 0; q < 2 * a.tmax; ++q) ptx::mbar_init(&acc_full[q], 1);
     ptx::mbar_init(&tmem_free[0], 1);
@@ -245,6 +248,7 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
     // (all lanes run the loop in step; lane 0 issues)
     {
       const uint32_t total = (uint32_t)(nt * a.N);
+      const uint64_t z_policy = ptx::l2_policy_evict_first();
       uint32_t it = 0;
       bool ok = true;
       for (; ok && it < total; ++it) {
@@ -256,9 +260,11 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
         }
         const int slot = (int)(it / nt), t = t_begin + (int)(it % nt);
         if (lane == 0) {
+          // (each tile of z is read once: its lines go first, so that markov_w2, read
+          // again every slot, keeps its place in L2)
           ptx::mbar_arrive_expect_tx(&zfull[s], kZStage);
-          ptx::tma_load_2d(s_z + (size_t)s * kZStage, &tm_z, &zfull[s], a.b0,
-                           (int)((size_t)slot * a.Vhp) + t * kTileV);
+          ptx::tma_load_2d_hint(s_z + (size_t)s * kZStage, &tm_z, &zfull[s], a.b0,
+                                (int)((size_t)slot * a.Vhp) + t * kTileV, z_policy);
         }
         __syncwarp();
       }
@@ -326,9 +332,11 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
   } else {
     // ---------------------------------------------------------------- epilogue
     const int tid = threadIdx.x;                    // 0..255
-    const int quad = warp % 4, par = warp / 4;      // TMEM lane quadrant, tile parity
+    const int quad = warp % 4;                      // TMEM lane quadrant
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const int row = quad * 32 + lane;               // row of the tile this thread owns
+    // the blocks (TMEM columns) of this warp: one half of the MMA's N, 16 or 8 of them
+    const int ncw = a.n_mma / 2, c0w = (warp / 4) * ncw;
 
     // u = markov_w1[prev] for the group's blocks into the swizzled K-major B operand
     // (zero past r and past the group's blocks); prev from s_prev
@@ -412,16 +420,25 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
       }
     };
     auto rank_bound = [&](const uint32_t (&kb)[kPer]) {
+      // (the warp's blocks ranked together and nb even: 2 x kPer independent shuffles
+      // in flight per step)
+      int rank[kPer];
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) rank[q] = 0;
+      for (int h = 0; h < a.nb; h += 2) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+#pragma unroll
+          for (int q = 0; q < kPer; ++q) {
+            const uint32_t y = __shfl_sync(0xFFFFFFFFu, kb[q], h + e);
+            rank[q] += (y > kb[q]) | ((y == kb[q]) & (h + e < lane));
+          }
+        }
+      }
 #pragma unroll
       for (int q = 0; q < kPer; ++q) {
         const int c = warp + q * kEpiWarps;
-        if (c >= a.Bg) break;                           // (uniform over the warp)
-        int rank = 0;
-        for (int h = 0; h < a.nb; ++h) {
-          const uint32_t y = __shfl_sync(0xFFFFFFFFu, kb[q], h);
-          rank += (y > kb[q]) | ((y == kb[q]) & (h < lane));
-        }
-        if (lane < a.nb && rank == a.k - 1)
+        if (c < a.Bg && lane < a.nb && rank[q] == a.k - 1)
           s_thv[c] = kb[q] == 0u ? -INFINITY : order_key32_value((int)(kb[q] ^ 0x80000000u));
       }
     };
@@ -430,7 +447,7 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
     auto scan_tile = [&](int step, int lt) {
       const int v = (t_begin + lt) * kTileV + row;
       const uint32_t taddr = tmem + lane_base + col_of(step, lt);
-      for (int c0 = 0; c0 < a.Bg; c0 += 8) {
+      for (int c0 = c0w; c0 < c0w + ncw && c0 < a.Bg; c0 += 8) {
         uint32_t r[8];
         __syncwarp();                                     // (after the divergent appends)
         ptx::tmem_ld_32x32b_x8(taddr + c0, r);
@@ -472,28 +489,37 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
     for (int step = 0; ok && step < a.N; ++step) {
       const int buf = a.dbuf ? (step & 1) : 0;
       const int use = a.dbuf ? (step >> 1) : step;
-      // -------- 3. pass 1: z' = z + m, back into TMEM.  Each chunk of 16 blocks is
-      //            reduced across the warp at once (redux on order keys: the largest value,
-      //            then the lowest row holding it), and lane j keeps the warp's running
-      //            best of block c0 + j in shared memory.  A compact loop: this code runs
-      //            once per tile, so the instruction cache stays warm.
-      if (lane < 32) {
-        s_bv[warp * 32 + lane] = -INFINITY;
-        s_bi[warp * 32 + lane] = 0x7FFFFFFF;
-        if (ZRANK) s_zb[warp * 32 + lane] = -INFINITY;
+      // -------- 3. pass 1: z' = z + m (back into TMEM for the top-k pass).  Every warp
+      //            takes every tile: its TMEM lane quadrant (32 rows) and its half of the
+      //            blocks, so a tile's work is spread over all eight warps.  Each thread
+      //            keeps, per block, the best of its own rows over the slot's tiles (the
+      //            value and the tile); the warp's 32 rows are reduced once, after the
+      //            last tile, so a tile costs no cross-lane work.  (Compared as floats:
+      //            -0 and +0 are equal, as they are as values; the value published is
+      //            canonical.)
+      float bx[16];                                       // best z' of block c0w + j, or -inf
+      uint32_t btile[4];                                  // its tile: byte j % 4 of word j / 4
+#pragma unroll
+      for (int j = 0; j < 16; ++j) bx[j] = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) btile[q] = 0u;
+      if (ZRANK) {
+        if (lane < ncw) s_zb[quad * 32 + c0w + lane] = -INFINITY;
+        __syncwarp();
       }
-      __syncwarp();
-      for (int lt = par; lt < nt; lt += 2) {
+      const bool wide = ncw == 16;                        // (else 8 blocks per warp)
+      for (int lt = 0; lt < nt; ++lt) {
         const int v = (t_begin + lt) * kTileV + row;
         const bool v_ok = v < a.Vh;
         const bool scan_prev = fuse && step > 0;
-        const bool two = a.n_mma > 16;
-        uint32_t rp[32];                                  // the previous slot's z' (fused scan)
+        uint32_t rp[16];                                  // the previous slot's z' (fused scan)
         if (scan_prev) {
-          const uint32_t pa = tmem + lane_base + col_of(step - 1, lt);
+          const uint32_t pa = tmem + lane_base + col_of(step - 1, lt) + c0w;
           __syncwarp();
-          ptx::tmem_ld_32x32b_x16(pa, *reinterpret_cast<uint32_t(*)[16]>(&rp[0]));
-          if (two) ptx::tmem_ld_32x32b_x16(pa + 16, *reinterpret_cast<uint32_t(*)[16]>(&rp[16]));
+          if (wide)
+            ptx::tmem_ld_32x32b_x16(pa, rp);
+          else
+            ptx::tmem_ld_32x32b_x8(pa, *reinterpret_cast<uint32_t(*)[8]>(&rp[0]));
         }
         const uint32_t zit = (uint32_t)(step * nt + lt);
         const uint32_t zs = zit % kZStages, zph = (zit / kZStages) & 1;
@@ -506,16 +532,19 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
           break;
         }
         ptx::tc_fence_after();
+        const uint32_t taddr = tmem + lane_base + col_of(step, lt) + c0w;
+        uint32_t r[16];                                   // this slot's Markov terms
+        if (wide)
+          ptx::tmem_ld_32x32b_x16(taddr, r);
+        else
+          ptx::tmem_ld_32x32b_x8(taddr, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
         const uint8_t* zrow = s_z + (size_t)zs * kZStage + (size_t)row * 128;
-        const uint32_t taddr = tmem + lane_base + col_of(step, lt);
-        uint32_t r[32];                                   // this slot's Markov terms
-        ptx::tmem_ld_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-        if (two) ptx::tmem_ld_32x32b_x16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
-        float zv[32];
+        float zv[16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {                     // 16-byte chunk q of the row, swizzled
-          if (q >= 4 && !two) break;
-          const float4 f = *reinterpret_cast<const float4*>(zrow + ((q ^ (row & 7)) << 4));
+        for (int q = 0; q < 4; ++q) {                     // 16-byte chunk c0w / 4 + q of the
+          if (q >= 2 && !wide) break;                     // row, swizzled
+          const int ch = c0w / 4 + q;
+          const float4 f = *reinterpret_cast<const float4*>(zrow + ((ch ^ (row & 7)) << 4));
           zv[4 * q] = f.x;
           zv[4 * q + 1] = f.y;
           zv[4 * q + 2] = f.z;
@@ -528,85 +557,112 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
         if (scan_prev) {
           uint32_t hit = 0;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 t4 = *reinterpret_cast<const float4*>(s_thv + 4 * q);
+          for (int q = 0; q < 4; ++q) {
+            if (q >= 2 && !wide) break;
+            const float4 t4 = *reinterpret_cast<const float4*>(s_thv + c0w + 4 * q);
             hit |= (__uint_as_float(rp[4 * q]) >= t4.x ? 1u : 0u) << (4 * q);
             hit |= (__uint_as_float(rp[4 * q + 1]) >= t4.y ? 1u : 0u) << (4 * q + 1);
             hit |= (__uint_as_float(rp[4 * q + 2]) >= t4.z ? 1u : 0u) << (4 * q + 2);
             hit |= (__uint_as_float(rp[4 * q + 3]) >= t4.w ? 1u : 0u) << (4 * q + 3);
           }
-          hit &= v_ok ? (a.Bg >= 32 ? 0xFFFFFFFFu : ((1u << a.Bg) - 1u)) : 0u;
+          const int nblk = min(ncw, a.Bg - c0w);          // this warp's blocks in the group
+          hit &= (v_ok && nblk > 0) ? ((1u << nblk) - 1u) : 0u;
           while (hit) {
             const int j = __ffs(hit) - 1;
             hit &= hit - 1;
             uint32_t xb = rp[0];
 #pragma unroll
-            for (int q = 1; q < 32; ++q) xb = j == q ? rp[q] : xb;
-            const int e = atomicAdd(&s_cnt[j], 1);
+            for (int q = 1; q < 16; ++q) xb = j == q ? rp[q] : xb;
+            const int c = c0w + j;
+            const int e = atomicAdd(&s_cnt[c], 1);
             if (e < kDenseLocal) {
               const size_t o =
-                  (((size_t)(step - 1) * a.B + a.b0 + j) * G + blockIdx.x) * kDenseLocal + e;
+                  (((size_t)(step - 1) * a.B + a.b0 + c) * G + blockIdx.x) * kDenseLocal + e;
               a.cand_val[o] = __uint_as_float(xb);
               a.cand_id[o] = v;
             }
           }
         }
         __syncwarp();
-        // z' = z + m (or -inf past the head), back into r for the top-k scan; then each
-        // block's best over the warp's 32 rows: all keys first, then the reductions back
-        // to back (they are independent), lane j keeping block j's result
-        const int ncol = two ? 32 : 16;
-        int kx[32];
+        // z' = z + m (or -inf past the head), back into r for the top-k scan, and the
+        // thread's running best of each block (strict: on equal values the earlier tile,
+        // the lower row, stays)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j >= ncol) break;
+        for (int j = 0; j < 16; ++j) {
+          if (j >= 8 && !wide) break;
           const float x = v_ok ? zv[j] + __uint_as_float(r[j]) : -INFINITY;
-          kx[j] = order_key32(canon(x));
+          if (x > bx[j]) {
+            bx[j] = x;
+            btile[j / 4] = (btile[j / 4] & ~(0xFFu << (8 * (j % 4)))) |
+                           ((uint32_t)lt << (8 * (j % 4)));
+          }
           r[j] = __float_as_uint(ZRANK ? (v_ok ? zv[j] : -INFINITY) : x);
-          if (a.logits && v_ok && j < a.Bg)               // (tests only)
-            a.logits[((size_t)(a.b0 + j) * a.N + step) * a.Vh + v] = x;
+          if (a.logits && v_ok && c0w + j < a.Bg)         // (tests only)
+            a.logits[((size_t)(a.b0 + c0w + j) * a.N + step) * a.Vh + v] = x;
         }
-        int mk = 0;
+        if (ZRANK) {                                      // the largest base logit of each
+          float mzv = -INFINITY;                          // block over the warp's rows
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j >= ncol) break;
-          const int m = __reduce_max_sync(0xFFFFFFFFu, kx[j]);
-          kx[j] = kx[j] == m ? v : 0x7FFFFFFF;            // (now the candidate row)
-          if (lane == j) mk = m;
-        }
-        int mid = 0x7FFFFFFF;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j >= ncol) break;
-          const int id = (int)__reduce_min_sync(0xFFFFFFFFu, (unsigned)kx[j]);
-          if (lane == j) mid = id;
-        }
-        float mzv = -INFINITY;
-        if (ZRANK) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j >= ncol) break;
+          for (int j = 0; j < 16; ++j) {
+            if (j >= 8 && !wide) break;
             const int mz = __reduce_max_sync(0xFFFFFFFFu, order_key32(v_ok ? zv[j] : -INFINITY));
             if (lane == j) mzv = order_key32_value(mz);
           }
-        }
-        if (lane < ncol) {                                 // rows rise with the tiles: on
-          const int c = warp * 32 + lane;                 // equal values the earlier,
-          const float bv = order_key32_value(mk);         // lower row stays
-          if (better(bv, mid, s_bv[c], s_bi[c])) {
-            s_bv[c] = bv;
-            s_bi[c] = mid;
-          }
-          if (ZRANK) s_zb[c] = fmaxf(s_zb[c], mzv);
+          if (lane < ncw)
+            s_zb[quad * 32 + c0w + lane] = fmaxf(s_zb[quad * 32 + c0w + lane], mzv);
         }
         __syncwarp();
         if (TOPK) {
-          ptx::tmem_st_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-          if (two) ptx::tmem_st_32x32b_x16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+          if (wide)
+            ptx::tmem_st_32x32b_x16(taddr, r);
+          else
+            ptx::tmem_st_32x32b_x8(taddr, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
           ptx::tmem_st_wait();
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&zempty[zs]);
+      }
+      // the warp's best of each of its blocks over its 32 rows: a transposing butterfly
+      // on (value, row) pairs over lane bits 3..0, halving the blocks a lane holds at each
+      // step, then one plain step over bit 4; lanes j and j + 16 end with block c0w + j
+      // (on equal values the lower row wins)
+      if (ok) {
+        float key[16];
+        int rw[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int t = (int)((btile[j / 4] >> (8 * (j % 4))) & 0xFFu);
+          key[j] = bx[j];
+          rw[j] = bx[j] == -INFINITY ? 0x7FFFFFFF : (t_begin + t) * kTileV + row;
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < o; ++i) {
+            const float send_k = upper ? key[i] : key[i + o];
+            const int send_r = upper ? rw[i] : rw[i + o];
+            const float keep_k = upper ? key[i + o] : key[i];
+            const int keep_r = upper ? rw[i + o] : rw[i];
+            const float got_k = __shfl_xor_sync(0xFFFFFFFFu, send_k, o);
+            const int got_r = __shfl_xor_sync(0xFFFFFFFFu, send_r, o);
+            const bool take = got_k > keep_k || (got_k == keep_k && got_r < keep_r);
+            key[i] = take ? got_k : keep_k;
+            rw[i] = take ? got_r : keep_r;
+          }
+        }
+        {
+          const float got_k = __shfl_xor_sync(0xFFFFFFFFu, key[0], 16);
+          const int got_r = __shfl_xor_sync(0xFFFFFFFFu, rw[0], 16);
+          if (got_k > key[0] || (got_k == key[0] && got_r < rw[0])) {
+            key[0] = got_k;
+            rw[0] = got_r;
+          }
+        }
+        if (lane < ncw) {
+          s_bv[quad * 32 + c0w + lane] = canon(key[0]);
+          s_bi[quad * 32 + c0w + lane] = rw[0];
+        }
       }
       // a warp that gave up raises the flag; the others then stop waiting, and all take
       // the same decision here (the named barriers below need every epilogue thread)
@@ -628,12 +684,12 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
         int bi = s_bi[tid];
         float bz = ZRANK ? s_zb[tid] : 0.f;
 #pragma unroll
-        for (int w = 1; w < kEpiWarps; ++w) {
-          if (better(s_bv[w * 32 + tid], s_bi[w * 32 + tid], bv, bi)) {
-            bv = s_bv[w * 32 + tid];
-            bi = s_bi[w * 32 + tid];
+        for (int q = 1; q < 4; ++q) {                     // the four lane quadrants
+          if (better(s_bv[q * 32 + tid], s_bi[q * 32 + tid], bv, bi)) {
+            bv = s_bv[q * 32 + tid];
+            bi = s_bi[q * 32 + tid];
           }
-          if (ZRANK) bz = fmaxf(bz, s_zb[w * 32 + tid]);
+          if (ZRANK) bz = fmaxf(bz, s_zb[q * 32 + tid]);
         }
         const size_t sb = (size_t)step * a.B + a.b0 + tid;
         if (bi != 0x7FFFFFFF) atomicMax(&a.keys[sb], order_key(canon(bv), bi));
@@ -644,6 +700,15 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
                     (uint32_t)order_key32(canon(ZRANK ? bz : bv)) ^ 0x80000000u);
         // arrive on the grid barrier; the release orders this thread's atomics first
         red_release_add(a.bar, 1u);
+        // the markov_w1 row of this CTA's best: the next slot gathers one of the G such
+        // rows of the block, so each is brought into L2 while the grid meets
+        if (bi != 0x7FFFFFFF && step + 1 < a.N) {
+          const int p = a.d2t ? __ldg(a.d2t + bi) : bi;
+          if (p >= 0 && p < a.V) {
+            const char* src = reinterpret_cast<const char*>(a.w1 + (size_t)p * a.r);
+            for (int o = 0; o < a.r * 2; o += 128) ptx::prefetch_l2(src + o);
+          }
+        }
       }
       // -------- 5. the grid barrier: every CTA has published this slot's winners.
       //            (Warp 0 polls with all its lanes, in step.)
@@ -674,7 +739,7 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
         rank_bound(kb);
         epi_sync();
         if (!fuse || step + 1 == a.N) {
-          for (int lt = par; lt < nt; lt += 2) scan_tile(step, lt);
+          for (int lt = 0; lt < nt; ++lt) scan_tile(step, lt);
           epi_sync();
           publish_counts(step);
         }
@@ -910,14 +975,10 @@ cudaError_t launch_chain_dense(const ProposePlan& p) {
   // with k = 1 over the corrected logits the top-1 is the argmax: written with the draft
   const bool topk_pass = want_topk && (p.k > 1 || zrank);
 
-  // markov_w2 stages of 256 K-rows (32 KB boxes: a TMA box costs about the same to service
-  // whatever its size, so larger boxes stream faster) when two such stages fit beside the
-  // rest of the shared memory, else 128
-  const int kb_max = ((p.r + 255) / 256) * 4;
-  const int ks = 1024 + (size_t)kZStages * kZStage + (size_t)kb_max * 32 * 128 + 8 * 1024 +
-                             2 * (size_t)(2 * 64 * 256 * 2) <= 225 * 1024
-                     ? 256
-                     : 128;
+  // markov_w2 stages of 256 K-rows (a whole 128-row tile of a rank-256 head: 64 KB), or
+  // 128 when the rank is at most 128.  Each stage costs one mbarrier round trip between
+  // the TMA and the MMA whatever its size, so the stages are as large as the rank allows.
+  const int ks = p.r <= 128 ? 128 : 256;
   CUtensorMap tw, tz;
   {
     cuuint64_t dims[2] = {(cuuint64_t)p.Vh, (cuuint64_t)p.r};

@@ -86,7 +86,7 @@ struct ProposePlan {
   float* z;             // base logits: [N][Vhp][ldb] (slot, head row, block fastest), or
                         // [N][Vhp / 8][ldb][8] when z_octet (see z_octet_index)
   bool z_octet;
-  size_t Vhp, ldb;      // head rows rounded up to whole 128-row tiles; blocks rounded to 4
+  size_t Vhp, ldb;      // head rows rounded up to whole 128-row tiles; blocks rounded to 8
   size_t ldz;           // row stride of zc
   float* zc;            // corrected logits of the current slot [B][ldz]
   int32_t* prev;        // previous tokens [B]
