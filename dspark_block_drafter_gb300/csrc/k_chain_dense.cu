@@ -127,6 +127,19 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// NK MMAs of K = 16 over one markov_w2 stage: A advances 16 K-rows (2048 bytes) per MMA,
+// B 32 bytes inside its 64-K swizzle block and bstep (16-byte units) between blocks.  The
+// descriptors' 14-bit address fields stay below 2^14 (shared memory < 256 KB), so the
+// sums carry into nothing.
+template <int NK>
+__device__ __forceinline__ void mma_run(uint32_t d, uint64_t ad, uint64_t bd, uint32_t bstep,
+                                        uint32_t idesc, bool accumulate_first) {
+#pragma unroll
+  for (int kk = 0; kk < NK; ++kk)
+    ptx::mma_f16(d, ad + (uint64_t)(kk * 128), bd + (uint64_t)((kk / 4) * bstep + (kk % 4) * 2),
+                 idesc, (kk > 0 || accumulate_first) ? 1u : 0u);
+}
+
 template <bool ZRANK, bool TOPK>
 __global__ void __launch_bounds__(kThreads, 1)
 chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_z,
@@ -281,7 +294,8 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
     {
       const uint32_t idesc = ptx::idesc_bf16_f32(kTileV, a.n_mma, /*A MN-major*/ 1, 0);
       const uint32_t u0 = ptx::smem_u32(s_u);
-      uint32_t it = 0;
+      const uint32_t bstep = a.u_kb_bytes >> 4;          // u's 64-K blocks, in 16-byte units
+      uint32_t s_it = 0, ph_it = 0;                      // ring position of the next stage
       bool ok = true;
       for (int step = 0; ok && step < a.N; ++step) {
         if (!__all_sync(0xFFFFFFFFu,
@@ -299,24 +313,31 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
         ptx::tc_fence_after();
         for (int lt = 0; ok && lt < nt; ++lt) {
           const uint32_t d = tmem + col_of(step, lt);
-          for (int kst = 0; kst < a.kstages; ++kst, ++it) {
-            const uint32_t s = it % a.stages, ph = (it / a.stages) & 1;
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait_sleep(&full[s], ph, kWaitBudget, abort_flag))) {
+          for (int kst = 0; kst < a.kstages; ++kst) {
+            if (!__all_sync(0xFFFFFFFFu,
+                            ptx::mbar_wait_sleep(&full[s_it], ph_it, kWaitBudget, abort_flag))) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
             if (lane == 0) {
-              const uint32_t w0 = ptx::smem_u32(s_w2 + (size_t)s * a.stage);
-              for (int kk = 0; kk < a.ks / 16; ++kk) {
-                const uint32_t kb = (uint32_t)(kst * (a.ks / 64) + kk / 4);
-                ptx::mma_f16(d, ptx::desc_mnmajor_sw128(w0 + kk * 2048, a.box, 1024),
-                             ptx::desc_kmajor_sw128(u0 + kb * a.u_kb_bytes + (kk % 4) * 32),
-                             idesc, (kst | kk) != 0);
-              }
-              ptx::mma_commit(&empty[s]);
+              // the stage's MMAs as one straight run from two base descriptors (the tensor
+              // pipe queues only a little ahead of this thread, so per-MMA work idles it)
+              const uint64_t ad = ptx::desc_mnmajor_sw128(
+                  ptx::smem_u32(s_w2 + (size_t)s_it * a.stage), a.box, 1024);
+              const uint64_t bd =
+                  ptx::desc_kmajor_sw128(u0 + (uint32_t)(kst * (a.ks / 64)) * a.u_kb_bytes);
+              if (a.ks == 256)
+                mma_run<16>(d, ad, bd, bstep, idesc, kst != 0);
+              else
+                mma_run<8>(d, ad, bd, bstep, idesc, kst != 0);
+              ptx::mma_commit(&empty[s_it]);
             }
             __syncwarp();
+            if (++s_it == (uint32_t)a.stages) {
+              s_it = 0;
+              ph_it ^= 1u;
+            }
           }
           if (ok && lane == 0) ptx::mma_commit(&acc_full[(a.dbuf ? (step & 1) : 0) * a.tmax + lt]);
           __syncwarp();
@@ -508,6 +529,8 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
         __syncwarp();
       }
       const bool wide = ncw == 16;                        // (else 8 blocks per warp)
+      const int nblk = min(ncw, a.Bg - c0w);              // this warp's blocks in the group
+      const uint32_t blk_mask = nblk > 0 ? (nblk >= 32 ? ~0u : (1u << nblk) - 1u) : 0u;
       for (int lt = 0; lt < nt; ++lt) {
         const int v = (t_begin + lt) * kTileV + row;
         const bool v_ok = v < a.Vh;
@@ -565,8 +588,7 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
             hit |= (__uint_as_float(rp[4 * q + 2]) >= t4.z ? 1u : 0u) << (4 * q + 2);
             hit |= (__uint_as_float(rp[4 * q + 3]) >= t4.w ? 1u : 0u) << (4 * q + 3);
           }
-          const int nblk = min(ncw, a.Bg - c0w);          // this warp's blocks in the group
-          hit &= (v_ok && nblk > 0) ? ((1u << nblk) - 1u) : 0u;
+          hit &= v_ok ? blk_mask : 0u;
           while (hit) {
             const int j = __ffs(hit) - 1;
             hit &= hit - 1;
@@ -584,6 +606,13 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
           }
         }
         __syncwarp();
+        if (a.logits && v_ok) {                           // (tests only)
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < ncw && c0w + j < a.Bg)
+              a.logits[((size_t)(a.b0 + c0w + j) * a.N + step) * a.Vh + v] =
+                  zv[j] + __uint_as_float(r[j]);
+        }
         // z' = z + m (or -inf past the head), back into r for the top-k scan, and the
         // thread's running best of each block (strict: on equal values the earlier tile,
         // the lower row, stays)
@@ -597,8 +626,6 @@ chain_dense(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ C
                            ((uint32_t)lt << (8 * (j % 4)));
           }
           r[j] = __float_as_uint(ZRANK ? (v_ok ? zv[j] : -INFINITY) : x);
-          if (a.logits && v_ok && c0w + j < a.Bg)         // (tests only)
-            a.logits[((size_t)(a.b0 + c0w + j) * a.N + step) * a.Vh + v] = x;
         }
         if (ZRANK) {                                      // the largest base logit of each
           float mzv = -INFINITY;                          // block over the warp's rows
