@@ -84,6 +84,8 @@ SIGNATURES = {
                                    c_ptr, c_ptr, c_ptr]),
     "dspark_device_status": (c_i32, [c_ptr, c_ptr]),
     "dspark_noalloc_device_status": (c_i32, [c_ptr]),
+    "dspark_pass_stats": (c_i32, [c_ptr, c_ptr, ctypes.POINTER(c_i32), ctypes.POINTER(c_i32),
+                                  ctypes.POINTER(c_i32)]),
     "dspark_wait_selftest": (c_i32, [c_ptr, ctypes.c_size_t, ctypes.c_int64, c_i32, c_ptr]),
     "dspark_status_string": (ctypes.c_char_p, [c_i32]),
     "dspark_last_error": (ctypes.c_char_p, []),
@@ -204,6 +206,14 @@ def dspark_device_status(workspace: int, stream: int = 0) -> int:
 
 def dspark_noalloc_device_status(stream: int = 0) -> int:
     return lib().dspark_noalloc_device_status(stream)
+
+
+def dspark_pass_stats(workspace: int, stream: int = 0) -> dict:
+    """Counters of the latest propose call on ``workspace`` (see include/dspark.h)."""
+    a, b, c = c_i32(0), c_i32(0), c_i32(0)
+    check(lib().dspark_pass_stats(workspace, stream, ctypes.byref(a), ctypes.byref(b),
+                                  ctypes.byref(c)))
+    return {"on_the_fly": a.value, "every_row": b.value, "dense_overflow": c.value}
 
 
 def dspark_wait_selftest(workspace: int, workspace_bytes: int, budget_cycles: int,

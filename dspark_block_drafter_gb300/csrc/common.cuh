@@ -15,6 +15,15 @@ enum : uint32_t {
   kErrPrepared = 4u,   // the prepared head buffer was made for other weights or sizes
 };
 
+// Words of the workspace control block after the error word: counters of the latest
+// pass (the block is zeroed at the start of every pass), read by dspark_pass_stats.
+enum : int {
+  kCtrlOnTheFly = 1,   // (slot, block) pairs the pruned walk evaluated without a table
+  kCtrlEveryRow = 2,   //   of those, over every head row (the candidate list overflowed)
+  kCtrlDenseOver = 3,  // (slot, block) top-k lists of the dense chain that overflowed and
+                       //   were recomputed over every head row
+};
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 

@@ -480,6 +480,20 @@ dspark_status dspark_device_status(void* workspace, void* stream) {
   return fail(DSPARK_ERR_DEVICE, "a kernel saw a token outside [0, V)");
 }
 
+dspark_status dspark_pass_stats(void* workspace, void* stream, int32_t* on_the_fly,
+                                int32_t* every_row, int32_t* dense_overflow) {
+  if (!workspace) return fail(DSPARK_ERR_INVALID_ARG, "workspace is NULL");
+  uint32_t w[4] = {0, 0, 0, 0};
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(w, workspace, sizeof(w), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the pass counters");
+  if (on_the_fly) *on_the_fly = (int32_t)w[kCtrlOnTheFly];
+  if (every_row) *every_row = (int32_t)w[kCtrlEveryRow];
+  if (dense_overflow) *dense_overflow = (int32_t)w[kCtrlDenseOver];
+  return DSPARK_OK;
+}
+
 dspark_status dspark_wait_selftest(void* workspace, size_t workspace_bytes,
                                    int64_t budget_cycles, int32_t pre_abort, void* stream) {
   if (!workspace || !aligned(workspace, 256))

@@ -871,6 +871,7 @@ topk_final(const FinalArgs a) {
     return;
   }
   // overflow: every head row of this slot and block, exactly as the chain evaluates it
+  if (tid == 0) atomicAdd(a.err + kCtrlDenseOver, 1u);
   int prev;
   if (i == 0) {
     prev = a.anchors[b];

@@ -448,7 +448,8 @@ struct SelectArgs {
   int32_t* draft;            // [B][N]
   int32_t* topk_ids;         // [B][N][k] or NULL
   float* topk_vals;
-  uint32_t* err;
+  uint32_t* err;             // the control words: [0] error word, [1] slots evaluated on the
+                             // fly (no table), [2] of those, over every head row
   int B, N, V, Vh, r, k, kk, zrank, want_topk;
 };
 
@@ -603,6 +604,7 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
     __syncthreads();
     if (s_pi[step] >= 0) continue;
     // -------- on the fly: u of the previous token, z' of the list (or of every row)
+    if (tid == 0) atomicAdd(a.err + kCtrlOnTheFly, 1u);
     {
       int p;
       if (step == 0) {
@@ -634,7 +636,10 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
       nsel = n;
     } else {
       // the list overflowed: every row, streamed through the buffer
-      if (tid == 0) s_nfull = 0;
+      if (tid == 0) {
+        s_nfull = 0;
+        atomicAdd(a.err + kCtrlEveryRow, 1u);
+      }
       __syncthreads();
       for (int v0 = 0; v0 < a.Vh; v0 += kCand - kMaxKeep) {
         const int cnt = min(kCand - kMaxKeep, a.Vh - v0);

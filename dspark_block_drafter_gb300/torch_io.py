@@ -166,3 +166,7 @@ def tree_verify(topk_ids, n_draft, target, accepted, bonus, emitted=None, path=N
 
 def device_status(workspace: torch.Tensor, stream=None) -> int:
     return _abi.dspark_device_status(workspace.data_ptr(), _stream(stream))
+
+
+def pass_stats(workspace: torch.Tensor, stream=None) -> dict:
+    return _abi.dspark_pass_stats(workspace.data_ptr(), _stream(stream))

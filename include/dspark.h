@@ -334,6 +334,21 @@ dspark_status dspark_propose_noalloc(const dspark_config* cfg, const dspark_head
    otherwise, with the reason in dspark_last_error(). */
 dspark_status dspark_device_status(void* workspace, void* stream);
 
+/* Synchronises `stream` and reads three counters of the latest dspark_propose call on
+   `workspace` (they restart at zero with every call).  Instrumentation of the cost of
+   the two chain forms; the method on the pages has no counterpart.  Any output pointer
+   may be NULL.
+     on_the_fly:     (slot, block) pairs the exact-bound pruned chain could not look up
+                     in its tables and evaluated on the fly (loose Cauchy-Schwarz bounds:
+                     too many candidate rows or possible previous rows);
+     every_row:      of those, the pairs whose candidate list overflowed, so that every
+                     head row was evaluated;
+     dense_overflow: (slot, block) pairs of the dense chain whose top-k candidate lists
+                     overflowed (massive ties) and were recomputed over every head row.
+   DSPARK_ERR_INVALID_ARG for a NULL workspace; DSPARK_ERR_CUDA if the read fails. */
+dspark_status dspark_pass_stats(void* workspace, void* stream, int32_t* on_the_fly,
+                                int32_t* every_row, int32_t* dense_overflow);
+
 /* dspark_device_status() for the built-in scratch of dspark_propose_noalloc() on the
    current device: synchronises `stream`, reads the error word of the latest no-alloc call
    on this device and clears it.  (No counterpart on the pages, like the entry point it

@@ -243,3 +243,10 @@ def test_header_is_plain_c():
                         "-o", os.devnull], input="\n".join(src) + "\n",
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_pass_stats_refuses_null_workspace(lib):
+    import ctypes
+    a = ctypes.c_int32(0)
+    assert lib.dspark_pass_stats(None, None, ctypes.byref(a), None, None) == \
+        _abi.DSPARK_ERR_INVALID_ARG

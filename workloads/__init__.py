@@ -57,6 +57,7 @@ class Workload:
     accept_p: Optional[float] = None  # per-slot mismatch probability of the target;
                                       # None: exactly one mismatch per block
     seed: int = 20260
+    markov_std: Optional[float] = None  # std of markov_w1 and markov_w2 (None: weight_std)
 
     @property
     def N(self) -> int:
@@ -151,8 +152,7 @@ def make_head(wl: Workload, threads: int = 8) -> dict:
       emit_rows [n_emit] int32 sorted, or None
     """
     lm_head = _normal_rows(wl.seed, _S_LM_HEAD, wl.V, wl.H, wl.weight_std, wl.dtype, threads)
-    w1 = _normal_rows(wl.seed, _S_W1, wl.V, wl.r, wl.weight_std, wl.dtype, threads)
-    w2 = _normal_rows(wl.seed, _S_W2, wl.r, wl.V, wl.weight_std, wl.dtype, threads)
+    w1, w2 = make_markov(wl, threads)
     w_conf = _normal_rows(wl.seed, _S_WCONF, 1, wl.H, wl.conf_std, wl.dtype, 1)[0]
     lm_bias = emit = None
     if wl.n_emit is not None:
@@ -162,6 +162,14 @@ def make_head(wl: Workload, threads: int = 8) -> dict:
         lm_bias[emit] = 0.0
     return dict(lm_head=lm_head, markov_w1=w1, markov_w2=w2, w_conf=w_conf,
                 b_conf=float(wl.b_conf), lm_bias=lm_bias, emit_rows=emit)
+
+
+def make_markov(wl: Workload, threads: int = 8):
+    """markov_w1 [V, r] and markov_w2 [r, V] of the head (std markov_std, else weight_std)."""
+    std = wl.weight_std if wl.markov_std is None else wl.markov_std
+    w1 = _normal_rows(wl.seed, _S_W1, wl.V, wl.r, std, wl.dtype, threads)
+    w2 = _normal_rows(wl.seed, _S_W2, wl.r, wl.V, std, wl.dtype, threads)
+    return w1, w2
 
 
 def make_batch(wl: Workload, batch_index: int = 0) -> dict:
