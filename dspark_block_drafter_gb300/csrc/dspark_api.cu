@@ -4,6 +4,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/dspark.h"
 #include "common.cuh"
@@ -26,6 +27,80 @@ static dspark_status cuda_fail(cudaError_t e, const char* where) {
 static constexpr size_t kAlign = 256;
 // the longest wait the self-test may ask for: the budget of the pipelines' own waits
 static constexpr long long kMaxSelftestBudget = 2000000000ll;
+
+cudaError_t device_sms(int* sms) {
+  static std::mutex mu;
+  static int cached[64];                              // 0: not looked up yet
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cached[dev] == 0) {
+    e = cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+      cached[dev] = 0;
+      return e;
+    }
+  }
+  *sms = cached[dev];
+  return cudaSuccess;
+}
+
+cudaError_t raise_smem_limit(const void* fn, size_t smem) {
+  struct Entry {
+    const void* fn;
+    int dev;
+    size_t smem;                                      // the limit set so far
+  };
+  static std::mutex mu;
+  static std::vector<Entry> set;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry* found = nullptr;
+  for (Entry& x : set)
+    if (x.fn == fn && x.dev == dev) found = &x;
+  if (found && found->smem >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (found)
+    found->smem = smem;
+  else if (set.size() < 256)
+    set.push_back({fn, dev, smem});
+  return cudaSuccess;
+}
+
+cudaError_t blocks_per_sm(const void* fn, int threads, size_t smem, int* out) {
+  struct Entry {
+    const void* fn;
+    int dev, threads;
+    size_t smem;
+    int blocks;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;                   // a few kernels x sizes per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& x : cache)
+    if (x.fn == fn && x.dev == dev && x.threads == threads && x.smem == smem) {
+      *out = x.blocks;
+      return cudaSuccess;
+    }
+  if (smem > 48 * 1024) {
+    e = raise_smem_limit(fn, smem);
+    if (e != cudaSuccess) return e;
+  }
+  int blocks = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (cache.size() < 256) cache.push_back({fn, dev, threads, smem, blocks});
+  *out = blocks;
+  return cudaSuccess;
+}
 
 WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool pruned) {
   WorkspaceLayout w{};
@@ -57,8 +132,12 @@ WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool prun
     w.cand = take(plan_pruned_lists(B, N, k).total);
   }
   if (dtype == DSPARK_F32) {          // the CUDA-core chain keeps one corrected row per block
-    w.zc = take(sizeof(float) * (size_t)B * w.ldz);
-    w.prev = take(sizeof(int32_t) * (size_t)B);
+    w.zc = take(sizeof(float) * (size_t)B * w.ldz);   // and each CTA's k best of every slot
+    if ((size_t)B * N <= (size_t)kSimtFusedRows)      // (or every slot's ranked values)
+      w.zk = take(sizeof(float) * (size_t)N * B * w.ldz);
+    const size_t per = (size_t)N * B * simt_chain_ctas_max(Vh) * k;
+    w.dense_val = take(sizeof(float) * per);
+    w.dense_id = take(sizeof(int32_t) * per);
   } else if (!pruned) {               // the dense chain's candidate rows, per CTA
     const size_t per = (size_t)N * B * kChainMaxCtas;
     w.dense_cnt = take(sizeof(int32_t) * per);
@@ -195,7 +274,7 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   p.Vhp = wl.Vhp;
   p.ldb = wl.ldb;
   p.zc = (float*)(ws + wl.zc);
-  p.prev = (int32_t*)(ws + wl.prev);
+  p.zk = wl.zk ? (float*)(ws + wl.zk) : nullptr;
   p.cand_val = (float*)(ws + wl.dense_val);
   p.cand_id = (int32_t*)(ws + wl.dense_id);
   p.cand_cnt = (int32_t*)(ws + wl.dense_cnt);
@@ -250,10 +329,15 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
   if ((e = mark(DSPARK_STAGE_CONF)) != cudaSuccess) return cuda_fail(e, "event record");
   // the pruned chain evaluates the confidence head and truncation in its own kernels,
   // unless the adaptive block length needs the cuts before the GEMM
-  if ((!pruned || p.skip_truncated) && (e = launch_conf(p)) != cudaSuccess)
+  // (small fp32 problems: the confidence head and the base logits run inside the chain's
+  // single launch)
+  const bool simt_one = p.dtype == DSPARK_F32 &&
+                        simt_fused(p.B, p.N, p.H, p.Vh, p.r, p.skip_truncated);
+  if ((!pruned || p.skip_truncated) && !simt_one && (e = launch_conf(p)) != cudaSuccess)
     return cuda_fail(e, "confidence kernel");
   if ((e = mark(DSPARK_STAGE_LOGITS)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = p.dtype == DSPARK_BF16 ? launch_base_logits_tc(p) : launch_base_logits_simt(p);
+  e = p.dtype == DSPARK_BF16 ? launch_base_logits_tc(p)
+                             : (simt_one ? cudaSuccess : launch_base_logits_simt(p));
   if (e != cudaSuccess) return cuda_fail(e, "base logits");
   if ((e = mark(DSPARK_STAGE_CHAIN)) != cudaSuccess) return cuda_fail(e, "event record");
   e = p.dtype == DSPARK_F32 ? launch_chain_simt(p)
@@ -288,13 +372,15 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
                                     const dspark_outputs* out) {
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK || !out) return -1;
-  if (cfg->dtype == DSPARK_F32) return 1 + 1 + 2 * N;   // confidence, GEMM, 2 per slot
+  if (cfg->dtype == DSPARK_F32)                         // confidence, GEMM, chain; or the
+    return simt_fused(cfg->B, N, cfg->H, head->V_head, cfg->r, cfg->skip_truncated != 0)
+               ? 1                                      // chain alone, for small problems
+               : 3;
   if (use_pruned(cfg, head) && !out->logits)            // GEMM; tables with the walk;
     return cfg->skip_truncated ? 3 : 2;                 // confidence first when adaptive
   const bool topk = out->topk_ids || out->topk_vals;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+  int sms = 0;
+  if (device_sms(&sms) != cudaSuccess) {
     cudaGetLastError();
     sms = 152;
   }

@@ -954,11 +954,8 @@ template <bool ZRANK, bool TOPK>
 cudaError_t launch_dense_inst(const CUtensorMap& tw, const CUtensorMap& tz, const DenseArgs& a,
                               int grid, size_t smem, cudaStream_t stream) {
   auto kern = chain_dense<ZRANK, TOPK>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  cudaError_t e = blocks_per_sm(reinterpret_cast<const void*>(kern), kThreads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
   cudaLaunchConfig_t cfg = {};
@@ -990,9 +987,9 @@ int dense_chain_group(int Vh, int sms) {
 cudaError_t launch_chain_dense(const ProposePlan& p) {
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  const cudaError_t es = device_sms(&sms);
+  if (es != cudaSuccess) return es;
   const int tiles = (p.Vh + kTileV - 1) / kTileV;
   const int grid = std::max(1, std::min({sms, tiles, kChainMaxCtas}));
   const int tmax = (tiles + grid - 1) / grid;

@@ -1171,8 +1171,7 @@ cudaError_t launch_chain_pruned(const ProposePlan& p) {
                             sizeof(float) * kCapA * kTabC +
                             sizeof(__nv_bfloat16) * (size_t)(kCapA + kRowsChunk) * p.r;
   const size_t smem = std::max(table_smem, walk_smem_bytes(p.r, p.N));
-  cudaError_t e =
-      cudaFuncSetAttribute(pruned_table, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(pruned_table), smem);
   if (e != cudaSuccess) return e;
   return launch_dependent(pruned_table, dim3(p.B, p.N), dim3(kThreads), smem, p.stream, t, s);
 }

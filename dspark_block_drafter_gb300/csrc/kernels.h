@@ -54,7 +54,8 @@ struct ProposePlan {
   unsigned int* bar;    // grid-barrier counters of the dense chain, one per 16 blocks
   unsigned long long* keys;  // [N][B] order keys of each slot's winner
   float* cand_val;      // dense chain: [N][B][kChainMaxCtas][kDenseLocal] rows of each
-  int32_t* cand_id;     //   CTA that reach the slot's top-k bound, their ranked values
+  int32_t* cand_id;     //   CTA that reach the slot's top-k bound, their ranked values;
+                        //   fp32 chain: [N][B][G][k] each CTA's k best ranked rows
   int32_t* cand_cnt;    //   [N][B][kChainMaxCtas] how many each CTA found
   uint32_t* bucket;     //   [N][B][kDenseBuckets] maxima of the CTAs' best values (order
                         //   keys, zeroed per pass)
@@ -89,7 +90,8 @@ struct ProposePlan {
   size_t Vhp, ldb;      // head rows rounded up to whole 128-row tiles; blocks rounded to 8
   size_t ldz;           // row stride of zc
   float* zc;            // corrected logits of the current slot [B][ldz]
-  int32_t* prev;        // previous tokens [B]
+  float* zk;            // fp32 chain, few prediction rows: every slot's ranked values
+                        //   [N][B][ldz], or NULL
   float* conf_ws;       // confidences when the caller did not ask for them [B][N]
   cudaStream_t stream;
 };
@@ -115,7 +117,7 @@ constexpr int kDenseBuckets = 32;
 // cleared at the start of every call.
 struct WorkspaceLayout {
   size_t ctrl, bar, keys, zbound, walk_done, dense_cnt, dense_bucket, zero_end, z, zmax,
-      zwritten, cand, zc, prev, conf, dense_val, dense_id, total;
+      zwritten, cand, zc, zk, conf, dense_val, dense_id, total;
   size_t Vhp, ldb, ldz;
 };
 WorkspaceLayout plan_workspace(int B, int N, int Vh, int k, int dtype, bool pruned);
@@ -179,10 +181,26 @@ cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, s
 cudaError_t launch_base_logits_tc(const ProposePlan& p);
 cudaError_t launch_base_logits_simt(const ProposePlan& p);
 cudaError_t launch_chain_simt(const ProposePlan& p);
+int simt_chain_ctas_max(int Vh);
+// Whether the fp32 chain of this shape also evaluates the confidence head and the base
+// logits (one launch for the whole proposal).
+bool simt_fused(int B, int N, int H, int Vh, int r, bool skip_truncated);
+constexpr int kSimtFusedRows = 16;   // prediction rows of a problem small enough to fuse
 cudaError_t launch_chain_dense(const ProposePlan& p);
 // Blocks per launch of the dense chain for a head of Vh rows on `sms` SMs (32 or 16), or
 // 0 when its per-CTA share of the Markov terms does not fit TMEM.
 int dense_chain_group(int Vh, int sms);
+
+// Launch facts of the current device, cached across calls (each query costs host time
+// that a small problem would otherwise spend with the GPU idle):
+//   device_sms: its SM count;
+//   blocks_per_sm: resident CTAs per SM of kernel `fn` at `threads` threads and `smem`
+//   bytes of dynamic shared memory, after raising the kernel's dynamic shared memory
+//   limit to `smem` when that is above the default 48 KB;
+//   raise_smem_limit: that limit alone (set only when a larger one is needed).
+cudaError_t device_sms(int* sms);
+cudaError_t blocks_per_sm(const void* fn, int threads, size_t smem, int* out);
+cudaError_t raise_smem_limit(const void* fn, size_t smem);
 cudaError_t launch_verify(int B, int N, const int32_t* draft, const int32_t* n_draft,
                           const int32_t* target, int32_t* accepted, int32_t* bonus,
                           int32_t* emitted, cudaStream_t stream);

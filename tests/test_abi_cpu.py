@@ -195,8 +195,9 @@ def test_timed_and_kernel_count_checked(lib):
     st = ds._abi.dspark_propose_timed(cfg, head, 0x4000, 0x5000, out, 0x10000, need - 1, 0,
                                       [0x10] * n)
     assert st == _abi.DSPARK_ERR_WORKSPACE
-    # launches per pass: confidence, GEMM and two per slot on the fp32 path
-    assert ds._abi.dspark_propose_kernel_count(cfg, head, out) == 2 + 2 * 4
+    # launches per pass on the fp32 path: confidence, GEMM and the one-launch chain; or,
+    # when a GPU says this small shape fits, the chain alone (it evaluates both)
+    assert ds._abi.dspark_propose_kernel_count(cfg, head, out) in (1, 3)
     # bf16, no prepared head: confidence, GEMM, one chain launch per 32 blocks, top-k
     bf = _cfg(dtype=1, B=70)
     topk = _abi.dspark_outputs(draft=0x100, n_draft=0x200, topk_ids=0x300, topk_vals=0x400)
