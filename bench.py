@@ -40,7 +40,9 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "drafted slots/sec (propose+verify) at B=32, V=151936"
+def metric_of(wl) -> str:
+    """The headline metric's name for this workload (the default one: B=32, V=151936)."""
+    return f"drafted slots/sec (propose+verify) at B={wl.B}, V={wl.V}"
 UNIT = "slots/s"
 FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -283,7 +285,7 @@ def run_reference(args):
         times.append(time.perf_counter() - t0)
     t = sum(times) / len(times)
     v = blocks * wl.N / t
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+    line = {"impl": "reference", "metric": metric_of(wl), "value": v, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
@@ -491,7 +493,7 @@ def run_ours(args):
         peak_source = (f"{peaks['_source']} bf16 burst" if wl.dtype == "bf16" else
                        "fp32 lanes x clock (derived)")
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "metric": metric_of(wl), "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": _config(wl, f"flushed: {FLUSH_BYTES >> 20} MB written, then another "
