@@ -203,6 +203,117 @@ static dspark_status validate(const dspark_config* c, const dspark_head* h, int*
   return DSPARK_OK;
 }
 
+// ------------------------------------------------------------------ compact heads
+// A bf16 head in the bias form (full-V lm_head, lm_bias marking the rows the draft cannot
+// emit) whose prepared buffer holds its compact form: every proposal then runs on the
+// emittable rows only (the d2t form), with the same results.
+static bool bias_form(const dspark_config* c, const dspark_head* h) {
+  return c->dtype == DSPARK_BF16 && h->lm_bias && !h->d2t && h->V_head == c->V;
+}
+
+namespace {
+std::mutex g_compact_mu;
+struct CompactEntry {
+  const void* prepared;
+  CompactHeader h;
+};
+std::vector<CompactEntry> g_compact;   // per prepared buffer, what dspark_prepare_head wrote
+}  // namespace
+
+static bool compact_matches(const CompactHeader& h, const dspark_config* c,
+                            const dspark_head* hd) {
+  return h.magic == kCompactMagic && h.V == c->V && h.H == c->H && h.r == c->r &&
+         h.n_emit >= 1 && h.n_pad >= h.n_emit && h.n_pad % 8 == 0 &&
+         h.lm_head == (unsigned long long)(uintptr_t)hd->lm_head &&
+         h.lm_bias == (unsigned long long)(uintptr_t)hd->lm_bias &&
+         h.w1 == (unsigned long long)(uintptr_t)hd->markov_w1 &&
+         h.w2 == (unsigned long long)(uintptr_t)hd->markov_w2;
+}
+
+static void remember_compact(const void* prepared, const CompactHeader& h) {
+  std::lock_guard<std::mutex> lock(g_compact_mu);
+  for (CompactEntry& x : g_compact)
+    if (x.prepared == prepared) {
+      x.h = h;
+      return;
+    }
+  if (g_compact.size() >= 256) g_compact.erase(g_compact.begin());
+  g_compact.push_back({prepared, h});
+}
+
+// For a bias-form head whose prepared buffer holds its compact form: 1 and the compact
+// head in *hc when the call's top_k is within the emittable rows; -1 and, in *hc, the
+// full head without the prepared buffer (the dense chain over every row) when it is not.
+// 0 for any other head (used as given).  A prepared buffer this process has not
+// prepared is read once (synchronously) to learn its row count.
+static int resolve_compact(const dspark_config* cfg, const dspark_head* head, dspark_head* hc) {
+  if (!bias_form(cfg, head) || !head->prepared) return 0;
+  CompactHeader h{};
+  bool found = false;
+  {
+    std::lock_guard<std::mutex> lock(g_compact_mu);
+    for (const CompactEntry& x : g_compact)
+      if (x.prepared == head->prepared) {
+        h = x.h;
+        found = true;
+      }
+  }
+  if (!found) {
+    if (cudaMemcpy(&h, head->prepared, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    if (!compact_matches(h, cfg, head)) return 0;
+    remember_compact(head->prepared, h);
+  }
+  if (!compact_matches(h, cfg, head)) return 0;
+  if (cfg->top_k > h.n_emit) {
+    *hc = *head;
+    hc->prepared = nullptr;
+    return -1;
+  }
+  const CompactLayout l = plan_compact(cfg->V, cfg->H, cfg->r, h.n_pad);
+  const char* base = (const char*)head->prepared;
+  *hc = *head;
+  hc->lm_head = base + l.lm_head;
+  hc->lm_bias = (const float*)(base + l.bias);
+  hc->d2t = (const int32_t*)(base + l.list);
+  hc->V_head = h.n_pad;
+  hc->markov_w2 = base + l.w2;
+  hc->prepared = base + l.prepared;
+  return 1;
+}
+
+// Emittable rows of a bias (bias > -1e8), counted on the device; synchronous.
+static __device__ int g_emit_count;
+static dspark_status count_emittable(const float* bias, int V, cudaStream_t stream, int* n) {
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  void* dev = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&dev, g_emit_count);
+  if (e == cudaSuccess) e = launch_emit_count(bias, V, (int*)dev, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(n, dev, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "counting the emittable rows");
+  return DSPARK_OK;
+}
+
+// Workspace of a proposal with this head: enough for the head as given and for its
+// compact form, so that one size serves both.
+static size_t propose_ws_bytes(const dspark_config* cfg, const dspark_head* head, int N) {
+  // (a prepared head runs the dense chain when the logits output is asked for)
+  auto both = [&](const dspark_head* h) {
+    size_t n = plan_workspace(cfg->B, N, h->V_head, cfg->top_k, cfg->dtype, false).total;
+    if (use_pruned(cfg, h))
+      n = std::max(n, plan_workspace(cfg->B, N, h->V_head, cfg->top_k, cfg->dtype, true).total);
+    return n;
+  };
+  size_t n = both(head);
+  dspark_head hc;
+  if (resolve_compact(cfg, head, &hc) != 0) n = std::max(n, both(&hc));
+  return n;
+}
+
 }  // namespace dspark
 
 using namespace dspark;
@@ -222,22 +333,26 @@ int32_t dspark_num_slots(const dspark_config* cfg) {
 size_t dspark_propose_workspace_size(const dspark_config* cfg, const dspark_head* head) {
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return 0;
-  return plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype, use_pruned(cfg, head))
-      .total;
+  return propose_ws_bytes(cfg, head, N);
 }
 
-static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* head,
+static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* head_in,
                                   const void* hidden, const int32_t* anchors,
                                   const void* conf_hidden, const dspark_outputs* out,
                                   void* workspace,
                                   size_t workspace_bytes, void* stream,
                                   void* const* events) {
   int N, ifp;
-  dspark_status st = validate(cfg, head, &N, &ifp);
+  dspark_status st = validate(cfg, head_in, &N, &ifp);
   if (st != DSPARK_OK) return st;
   if (!hidden || !anchors) return fail(DSPARK_ERR_INVALID_ARG, "hidden and anchors are required");
   if (!out || !out->draft || !out->n_draft)
     return fail(DSPARK_ERR_INVALID_ARG, "outputs draft and n_draft are required");
+  // a bias-form head prepared in its compact form runs on its emittable rows (unless the
+  // logits output, indexed by every head row, is asked for)
+  dspark_head hc;
+  const dspark_head* head =
+      (!out->logits && resolve_compact(cfg, head_in, &hc) != 0) ? &hc : head_in;
   if (cfg->dtype == DSPARK_BF16 && !aligned(hidden, 16))
     return fail(DSPARK_ERR_INVALID_ARG, "bf16 hidden must be 16-byte aligned");
   if (cfg->dtype == DSPARK_BF16 && conf_hidden && !aligned(conf_hidden, 16))
@@ -368,10 +483,13 @@ dspark_status dspark_propose_timed(const dspark_config* cfg, const dspark_head* 
                       workspace_bytes, stream, events);
 }
 
-int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head* head,
+int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head* head_in,
                                     const dspark_outputs* out) {
   int N, ifp;
-  if (validate(cfg, head, &N, &ifp) != DSPARK_OK || !out) return -1;
+  if (validate(cfg, head_in, &N, &ifp) != DSPARK_OK || !out) return -1;
+  dspark_head hc;
+  const dspark_head* head =
+      (!out->logits && resolve_compact(cfg, head_in, &hc) != 0) ? &hc : head_in;
   if (cfg->dtype == DSPARK_F32)                         // confidence, GEMM, chain; or the
     return simt_fused(cfg->B, N, cfg->H, head->V_head, cfg->r, cfg->skip_truncated != 0)
                ? 1                                      // chain alone, for small problems
@@ -418,12 +536,7 @@ size_t dspark_step_host_workspace_size(const dspark_config* cfg, const dspark_he
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK) return 0;
   // (room for a separate confidence input is always planned, so one size fits both)
-  return plan_stage(cfg, N,
-                    plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype,
-                                   use_pruned(cfg, head))
-                        .total,
-                    true)
-      .total;
+  return plan_stage(cfg, N, propose_ws_bytes(cfg, head, N), true).total;
 }
 
 dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head,
@@ -438,8 +551,7 @@ dspark_status dspark_step_host(const dspark_config* cfg, const dspark_head* head
   if (st != DSPARK_OK) return st;
   if (!hidden_h || !anchors_h || !target_h || !draft_h || !n_draft_h || !accepted_h || !bonus_h)
     return fail(DSPARK_ERR_INVALID_ARG, "a required host buffer is NULL");
-  size_t base =
-      plan_workspace(cfg->B, N, head->V_head, cfg->top_k, cfg->dtype, use_pruned(cfg, head)).total;
+  size_t base = propose_ws_bytes(cfg, head, N);
   StageLayout s = plan_stage(cfg, N, base, true);
   if (!workspace || !aligned(workspace, 256))
     return fail(DSPARK_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
@@ -599,6 +711,12 @@ dspark_status dspark_wait_selftest(void* workspace, size_t workspace_bytes,
 size_t dspark_prepare_head_size(const dspark_config* cfg, const dspark_head* head) {
   int N, ifp;
   if (validate(cfg, head, &N, &ifp) != DSPARK_OK || cfg->dtype != DSPARK_BF16) return 0;
+  if (bias_form(cfg, head)) {
+    int n = 0;
+    if (count_emittable(head->lm_bias, cfg->V, 0, &n) != DSPARK_OK) return 0;
+    if (n >= 1 && n < cfg->V)
+      return plan_compact(cfg->V, cfg->H, cfg->r, (int)align_up((size_t)n, 8)).total;
+  }
   return plan_prepared(head->V_head, cfg->r).total;
 }
 
@@ -612,12 +730,51 @@ dspark_status dspark_prepare_head(const dspark_config* cfg, const dspark_head* h
   const PreparedLayout pl = plan_prepared(head->V_head, cfg->r);
   if (!prepared || !aligned(prepared, 256))
     return fail(DSPARK_ERR_WORKSPACE, "prepared buffer must be non-NULL and 256-byte aligned");
+  if (bias_form(cfg, head)) {
+    // the compact form: the emittable rows (counted first, synchronously, to size it)
+    int n = 0;
+    st = count_emittable(head->lm_bias, cfg->V, (cudaStream_t)stream, &n);
+    if (st != DSPARK_OK) return st;
+    if (n >= 1 && n < cfg->V) {
+      const int n_pad = (int)align_up((size_t)n, 8);
+      const CompactLayout cl = plan_compact(cfg->V, cfg->H, cfg->r, n_pad);
+      if (prepared_bytes < cl.total)
+        return fail(DSPARK_ERR_WORKSPACE,
+                    "prepared buffer too small: need " + std::to_string(cl.total) + " bytes");
+      cudaError_t e = launch_prepare_compact(head->lm_head, head->lm_bias, head->markov_w1,
+                                             head->markov_w2, cfg->V, cfg->H, cfg->r, n, n_pad,
+                                             prepared, (cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_fail(e, "head preparation (compact form)");
+      CompactHeader h{};
+      h.magic = kCompactMagic;
+      h.V = cfg->V;
+      h.H = cfg->H;
+      h.r = cfg->r;
+      h.n_emit = n;
+      h.n_pad = n_pad;
+      h.lm_head = (unsigned long long)(uintptr_t)head->lm_head;
+      h.lm_bias = (unsigned long long)(uintptr_t)head->lm_bias;
+      h.w1 = (unsigned long long)(uintptr_t)head->markov_w1;
+      h.w2 = (unsigned long long)(uintptr_t)head->markov_w2;
+      remember_compact(prepared, h);
+      return DSPARK_OK;
+    }
+  }
   if (prepared_bytes < pl.total)
     return fail(DSPARK_ERR_WORKSPACE,
                 "prepared buffer too small: need " + std::to_string(pl.total) + " bytes");
   cudaError_t e = launch_prepare_head(head->markov_w1, head->markov_w2, cfg->V, cfg->r,
                                       head->V_head, prepared, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "head preparation");
+  {
+    // (a buffer prepared in the ordinary form is no longer a compact one)
+    std::lock_guard<std::mutex> lock(g_compact_mu);
+    for (size_t i = 0; i < g_compact.size(); ++i)
+      if (g_compact[i].prepared == prepared) {
+        g_compact.erase(g_compact.begin() + i);
+        break;
+      }
+  }
   return DSPARK_OK;
 }
 

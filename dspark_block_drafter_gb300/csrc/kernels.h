@@ -27,6 +27,27 @@ __device__ __forceinline__ bool prepared_matches(const PreparedHeader* h,
          got.r == want.r && got.w1 == want.w1 && got.w2 == want.w2;
 }
 
+// A head given in the bias form (full-V lm_head, lm_bias marking the rows the draft
+// cannot emit) is prepared as a compact head: the first bytes of its prepared buffer
+// are a CompactHeader, followed by the sorted emittable rows (the compact head's d2t,
+// padded to a multiple of 8), their lm_head rows, markov_w2 columns and biases, and the
+// compact head's own prepared data (a PreparedHeader and the rest).
+constexpr float kEmitMaskLevel = -1e8f;   // a bias at or below it marks a masked row
+struct CompactHeader {
+  uint32_t magic;                         // kCompactMagic once dspark_prepare_head has run
+  int32_t V, H, r, n_emit, n_pad;
+  unsigned long long lm_head, lm_bias, w1, w2;   // the full head's device addresses
+};
+constexpr uint32_t kCompactMagic = 0x4D435044u;
+struct CompactLayout {
+  size_t header, list, chunk_count, lm_head, w2, bias, prepared, total;
+};
+CompactLayout plan_compact(int V, int H, int r, int n_pad);
+cudaError_t launch_emit_count(const float* bias, int V, int* count, cudaStream_t stream);
+cudaError_t launch_prepare_compact(const void* lm_head, const float* bias, const void* w1,
+                                   const void* w2, int V, int H, int r, int n_emit, int n_pad,
+                                   void* prepared, cudaStream_t stream);
+
 // Everything a proposal launch needs, resolved by the ABI layer.
 struct ProposePlan {
   // sizes

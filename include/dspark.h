@@ -216,7 +216,18 @@ dspark_status dspark_tree_verify(int32_t B, int32_t N, int32_t top_k,
    (V, V_head, r and the markov_w1 / markov_w2 addresses), markov_w2 transposed
    [round_up(V_head, 128)][r] bf16, the fp32 Euclidean norm of every markov_w2 column,
    their maximum over each 128-row tile, and the largest Euclidean norm of a markov_w1
-   row. */
+   row.
+   A head in the bias form of a reduced draft vocabulary (lm_bias given, d2t NULL,
+   V_head == V, and 1 <= n_emit < V rows with bias > -1e8) is prepared in its compact
+   form instead (llama.cpp PR #26275, the reduced draft vocabulary as an expanded head
+   and as a d2t map): a 256-byte header (V, H, r, n_emit, the padded row count
+   n_pad = round_up(n_emit, 8) and the lm_head, lm_bias, markov_w1, markov_w2
+   addresses), the emittable rows in increasing order [n_pad] int32 (padded with copies
+   of the last), per-chunk counts, their lm_head rows [n_pad][H] bf16, markov_w2
+   columns [r][n_pad] bf16 and biases [n_pad] fp32 (padding rows: zero weights, bias
+   -1e30), then the layout above for that compact head.  To size it, this call counts
+   the emittable rows on the device and waits for the count (current device, default
+   stream). */
 size_t dspark_prepare_head_size(const dspark_config* cfg, const dspark_head* head);
 
 /*
@@ -235,6 +246,16 @@ size_t dspark_prepare_head_size(const dspark_config* cfg, const dspark_head* hea
  * those the buffer was prepared for reads nothing past the buffer's header: it drafts
  * nothing and dspark_device_status() then reports DSPARK_ERR_DEVICE with that reason.
  * (Contents changed in place at the same addresses cannot be detected; re-prepare.)
+ *
+ * Bias form (see dspark_prepare_head_size): the emittable rows are counted (this call
+ * waits for the count on `stream`), found and gathered on the device into the compact
+ * head; later dspark_propose calls with this head run on those rows only (the GEMM, the
+ * chain and the top-k), with the same outputs as over the full head.  That holds while
+ * top_k <= n_emit and the logits output is not requested; otherwise a call uses the
+ * full head (the dense chain over every row).  It must be prepared again when lm_head or
+ * lm_bias changes too.  A process that did not prepare the buffer itself reads its
+ * header once, synchronously, on first use: make that first call outside stream
+ * capture.
  */
 dspark_status dspark_prepare_head(const dspark_config* cfg, const dspark_head* head,
                                   void* prepared, size_t prepared_bytes, void* stream);
