@@ -33,6 +33,23 @@ def test_tiny_fp32_workload():
 CHAINS = ["dense", "pruned"]
 
 
+@pytest.mark.parametrize("shape", [
+    dict(B=6, L_in=5),                                  # 30 prediction rows: tiled GEMM,
+                                                        # chain in one chunk of 6 blocks
+    dict(B=10, L_in=3, top_k=3),                        # two chunks of blocks
+    dict(B=3, L_in=5, r=48),                            # rank above the register cache
+    dict(B=2, L_in=4, H=1200),                          # 8 rows, hidden past 32 KB: the
+                                                        # few-row GEMM, chain alone
+    dict(B=2, L_in=4, H=64, V=40960, r=16, top_k=8),    # more rows than threads x CTAs:
+                                                        # several rows per thread
+    dict(B=3, L_in=6, sample_from_anchor=False, topk_markov=False),
+])
+def test_fp32_chain_shapes(shape):
+    # the fp32 path's launch forms: one launch (small problems) or GEMM + chain, blocks in
+    # chunks, the markov_w2 column in registers or streamed, one or several rows a thread
+    run_case(_small(dtype="f32", **shape))
+
+
 @pytest.mark.parametrize("sfa", [True, False])
 @pytest.mark.parametrize("topk_markov", [True, False])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
