@@ -749,7 +749,7 @@ __device__ __forceinline__ void table_work(const TableArgs& a, uint8_t* dsm, int
   __nv_bfloat16* s_w1 = (__nv_bfloat16*)(s_x + kCapA * kTabC); // [kCapA][r]
   __nv_bfloat16* s_w2 = s_w1 + (size_t)kCapA * a.r;            // [kRowsChunk][r]
   __shared__ float s_top[kWarps * 32];
-  __shared__ float s_theta, s_red[kWarps];
+  __shared__ float s_theta, s_red[kWarps], s_cpart[kWarps];
   __shared__ int s_ntc, s_nta, s_nc, s_na;
   __shared__ int32_t s_av[kCapA];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -767,14 +767,14 @@ __device__ __forceinline__ void table_work(const TableArgs& a, uint8_t* dsm, int
     s_nc = 0;
     s_na = 0;
   }
-  // ---- bounds of slot i and slot i - 1 (all warps but the last), confidence (the last);
+  // ---- bounds of slot i and slot i - 1, and the confidence, all warps sharing both;
   //      each thread keeps the maxima of the lower bounds / tile maxima it saw
   float mp = -INFINITY;                              // slot i-1's lower bounds
   float mlb = -INFINITY, mzm = -INFINITY;            // slot i's lower bounds, tile maxima
-  if (warp < kWarps - 1) {
+  {
     // loads of up to kBoundsUnroll tiles per thread are issued before any is used
     constexpr int kBoundsUnroll = 8;
-    const int stride = kThreads - 32;
+    const int stride = kThreads;
     for (int t0 = tid; t0 < a.T; t0 += kBoundsUnroll * stride) {
       float c[kBoundsUnroll], z0[kBoundsUnroll], z1[kBoundsUnroll];
       unsigned w0 = 0, w1 = 0;                       // bit u: tile t0 + u * stride stored
@@ -802,35 +802,41 @@ __device__ __forceinline__ void table_work(const TableArgs& a, uint8_t* dsm, int
         }
       }
     }
-  } else if (a.w_conf) {
+  }
+  if (a.w_conf) {
     // sigmoid(h . w_conf + b_conf) (llama.cpp commit 6fed9f6, "spec: add confidence-based
-    // draft pruning for DSpark")
+    // draft pruning for DSpark"): each thread a few 16-byte chunks of the dot product,
+    // summed over the warp here and over the warps after the barrier
     const __nv_bfloat16* h = a.hidden + ((size_t)b * a.L_in + a.ifp + i) * a.H;
     float acc = 0.f;
-    int c0 = 0;
     if ((a.H % 8) == 0 && ((uintptr_t)h % 16) == 0 && ((uintptr_t)a.w_conf % 16) == 0) {
       const uint4* h4 = reinterpret_cast<const uint4*>(h);
       const uint4* w4 = reinterpret_cast<const uint4*>(a.w_conf);
       const int n4 = a.H / 8;
-#pragma unroll 4
-      for (int q = lane; q < n4; q += 32) {
+#pragma unroll 2
+      for (int q = tid; q < n4; q += kThreads) {
         const uint4 hv = h4[q], wv = w4[q];
         const __nv_bfloat16* he = reinterpret_cast<const __nv_bfloat16*>(&hv);
         const __nv_bfloat16* we = reinterpret_cast<const __nv_bfloat16*>(&wv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc = fmaf(to_f32(he[e]), to_f32(we[e]), acc);
       }
-      c0 = a.H;
+    } else {
+      for (int c = tid; c < a.H; c += kThreads) acc = fmaf(to_f32(h[c]), to_f32(a.w_conf[c]), acc);
     }
-    for (int c = c0 + lane; c < a.H; c += 32) acc = fmaf(to_f32(h[c]), to_f32(a.w_conf[c]), acc);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    if (lane == 0) a.conf[(size_t)b * a.N + i] = 1.f / (1.f + expf(-(acc + a.b_conf)));
+    if (lane == 0) s_cpart[warp] = acc;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xFFFFFFFFu, mp, o));
   if (lane == 0) s_red[warp] = mp;
   __syncthreads();
+  if (a.w_conf && tid == 0) {
+    float acc = 0.f;
+    for (int w = 0; w < kWarps; ++w) acc += s_cpart[w];
+    a.conf[(size_t)b * a.N + i] = 1.f / (1.f + expf(-(acc + a.b_conf)));
+  }
   // ---- thresholds: rank kk of slot i's lower bounds (rank 1 when the top-k ranks base
   //      logits, which then take rank kk of the tile maxima); rank 1 of slot i-1's
   const float theta_x = block_kth_of_maxima(mlb, a.zrank ? 1 : a.kk, s_top, &s_theta);
