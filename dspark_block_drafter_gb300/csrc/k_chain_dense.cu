@@ -57,7 +57,6 @@ constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kMmaWarp = 8, kZWarp = 9, kW2Warp = 10;   // two markov_w2 producers: 10, 11
 constexpr int kThreads = 32 * 12;
 constexpr int kZStages = 3;
-constexpr int kMaxRescans = 64;                         // overflow rounds (bounded anyway)
 constexpr long long kWaitBudget = 2000000000ll;         // ~1 s of SM clocks
 
 struct DenseArgs {
@@ -108,16 +107,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 // -0 and +0 are equal values (the lower id decides between them), but not equal keys:
 // keys are taken of x + 0, which is +0 for both.
 __device__ __forceinline__ float canon(float x) { return __fadd_rn(x, 0.0f); }
-
-// Warp-wide best (value, id) under the candidate order, by two reductions: the largest
-// value, then the lowest id among the lanes holding it.
-__device__ __forceinline__ void warp_best_redux(float& v, int& id) {
-  const int kv = order_key32(canon(v));
-  const int m = __reduce_max_sync(0xFFFFFFFFu, kv);
-  const unsigned cand = kv == m ? (unsigned)id : 0xFFFFFFFFu;
-  id = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
-  v = order_key32_value(m);
-}
 
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
