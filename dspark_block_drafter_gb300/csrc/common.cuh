@@ -22,6 +22,7 @@ enum : int {
   kCtrlEveryRow = 2,   //   of those, over every head row (the candidate list overflowed)
   kCtrlDenseOver = 3,  // (slot, block) top-k lists of the dense chain that overflowed and
                        //   were recomputed over every head row
+  kCtrlGemmTiles = 4,  // tiles claimed by the lm_head GEMM's dynamic schedule
 };
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

@@ -439,7 +439,7 @@ static dspark_status propose_impl(const dspark_config* cfg, const dspark_head* h
     return events ? cudaEventRecord((cudaEvent_t)events[s], p.stream) : cudaSuccess;
   };
   // the control words (error word, barrier counters, winner keys) start from zero
-  e = cudaMemsetAsync(ws + wl.ctrl, 0, wl.zero_end - wl.ctrl, p.stream);
+  e = launch_zero_block(ws + wl.ctrl, wl.zero_end - wl.ctrl, p.stream);
   if (e != cudaSuccess) return cuda_fail(e, "control reset");
   if ((e = mark(DSPARK_STAGE_CONF)) != cudaSuccess) return cuda_fail(e, "event record");
   // the pruned chain evaluates the confidence head and truncation in its own kernels,
@@ -490,12 +490,13 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
   dspark_head hc;
   const dspark_head* head =
       (!out->logits && resolve_compact(cfg, head_in, &hc) != 0) ? &hc : head_in;
+  // every pass starts with the kernel that zeroes the control block
   if (cfg->dtype == DSPARK_F32)                         // confidence, GEMM, chain; or the
-    return simt_fused(cfg->B, N, cfg->H, head->V_head, cfg->r, cfg->skip_truncated != 0)
-               ? 1                                      // chain alone, for small problems
-               : 3;
+    return 1 + (simt_fused(cfg->B, N, cfg->H, head->V_head, cfg->r, cfg->skip_truncated != 0)
+                    ? 1                                 // chain alone, for small problems
+                    : 3);
   if (use_pruned(cfg, head) && !out->logits)            // GEMM; tables with the walk;
-    return cfg->skip_truncated ? 3 : 2;                 // confidence first when adaptive
+    return 1 + (cfg->skip_truncated ? 3 : 2);           // confidence first when adaptive
   const bool topk = out->topk_ids || out->topk_vals;
   int sms = 0;
   if (device_sms(&sms) != cudaSuccess) {
@@ -504,7 +505,7 @@ int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head*
   }
   const int group = dense_chain_group(head->V_head, sms);
   const bool merge = topk && (cfg->top_k > 1 || !cfg->topk_markov);
-  return 1 /* confidence */ + 1 /* GEMM */ +
+  return 1 /* control block */ + 1 /* confidence */ + 1 /* GEMM */ +
          (cfg->B + group - 1) / std::max(group, 1) /* chain, one launch per group */ +
          (merge ? 1 : 0);
 }

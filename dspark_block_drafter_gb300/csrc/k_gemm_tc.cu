@@ -20,7 +20,9 @@
 //               per-tile maxima for the pruned chain
 // Two TMEM accumulators alternate so that the epilogue of one tile overlaps the MMAs of
 // the next.  Tiles are ordered vocabulary-major: CTAs that run side by side share the
-// same lm_head tile through L2, so lm_head streams from HBM once.
+// same lm_head tile through L2, so lm_head streams from HBM once.  Single CTAs claim
+// their tiles from a counter as they go (a CTA that streams faster takes more of them);
+// pairs take every units-th tile.
 //
 // When a tile's slots split evenly in two, CTAs run in pairs (a cluster of two on one
 // TPC) on 256-row tiles with M = 256 MMAs (cta_group::2): each CTA stages its own 128
@@ -51,6 +53,8 @@ constexpr int kBlockK = 64;       // one 128-byte swizzle row of bf16
 constexpr uint32_t kStageA = kBlockV * kBlockK * 2;   // 16 KB
 constexpr int kThreads = 192;
 constexpr int kMaxLiveTiles = 64;     // N-tiles the adaptive block length can leave out
+constexpr int kTileRing = 4;          // claimed tile indices in flight (dynamic schedule)
+constexpr int kBarBytes = 512;        // shared memory of the barriers and the tile ring
 #ifndef DSPARK_GEMM_BUCKET_X
 #define DSPARK_GEMM_BUCKET_X 2
 #endif
@@ -77,6 +81,9 @@ struct GemmArgs {
   const PreparedHeader* prep;  // header of the prepared buffer cnmax and w1max lie in
   PreparedHeader prep_want;    // what it must say (otherwise every tile is stored)
   int zbound_k;
+  // Dynamic schedule (CG = 1): after its first tile (unit), a CTA claims tile units + the
+  // old value of *tile_ctr, which starts at 0 for the launch; NULL: tile unit + j units.
+  unsigned* tile_ctr;
   const int32_t* n_draft;  // [B] cuts computed before the GEMM (adaptive block length), or
                            // NULL: every row is drafted
   int octet;       // z layout: [N][Vhp / 8][ldb][8] (1) or [N][Vhp][ldb] (0)
@@ -136,8 +143,12 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
   uint64_t* tile_bar2 = tile_bar + 1;                     // maxima in / maxima out
   uint32_t* tmem_slot = (uint32_t*)(tile_bar2 + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  // the dynamic schedule's mailbox: tile indices posted by the producer, in order
+  uint64_t* ring_full = tile_bar2 + 2;                    // an index is posted
+  uint64_t* ring_free = ring_full + kTileRing;            // every reader has taken it
+  volatile int* s_ring = (volatile int*)(ring_free + kTileRing);
   // column maxima of the tile over the four epilogue warps, as order-preserving keys
-  int* s_cmax = (int*)((uint8_t*)smem + g.stages * (a_stage + b_stage) + 256);   // [256]
+  int* s_cmax = (int*)((uint8_t*)smem + g.stages * (a_stage + b_stage) + kBarBytes);   // [256]
   int* s_live = s_cmax + 256;          // [1 + kMaxLiveTiles]: count, then the live N-tiles
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -157,10 +168,31 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(tile_bar, 128);
     ptx::mbar_init(tile_bar2, 128);
+    for (int j = 0; j < kTileRing; ++j) {
+      ptx::mbar_init(&ring_full[j], 1);           // the producer
+      ptx::mbar_init(&ring_free[j], 1 + 4);       // the MMA thread and the epilogue warps
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
   for (int c = threadIdx.x; c < 256; c += kThreads) s_cmax[c] = INT_MIN;
+  if (warp == 4 && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_w);
+    ptx::tma_prefetch_desc(&tm_h);
+  }
+  if (warp == 0) {
+    if (CG == 2) {
+      ptx::tmem_alloc_pair(tmem_slot, g.tmem_cols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_slot, g.tmem_cols);
+      ptx::tmem_relinquish();
+    }
+  }
+  // Launched as a dependent of the kernel that zeroes the pass's control block: nothing
+  // in global memory is read or written before that kernel (hence every earlier one on
+  // the stream) has finished.
+  pdl_wait();
   // Adaptive block length: an N-tile whose slots all lie at or past every one of its
   // blocks' cuts is not computed (the cuts come from the confidence kernel, launched
   // before this one).  Without cuts, or with more N-tiles than the list holds, all are.
@@ -180,19 +212,6 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       cnt += live;
     }
     if (lane == 0) s_live[0] = cnt;
-  }
-  if (warp == 4 && lane == 0) {
-    ptx::tma_prefetch_desc(&tm_w);
-    ptx::tma_prefetch_desc(&tm_h);
-  }
-  if (warp == 0) {
-    if (CG == 2) {
-      ptx::tmem_alloc_pair(tmem_slot, g.tmem_cols);
-      ptx::tmem_relinquish_pair();
-    } else {
-      ptx::tmem_alloc(tmem_slot, g.tmem_cols);
-      ptx::tmem_relinquish();
-    }
   }
   pdl_signal();                                 // the chain's kernels may be scheduled
   ptx::tc_fence_before();
@@ -214,6 +233,25 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     flag_error(g.err, kErrTimeout);
   };
 
+  // The tile schedule.  Static: CTA (or pair) `unit` takes tiles unit, unit + units, ...
+  // Dynamic (CG = 1 with a claim counter): the producer claims each next tile from the
+  // counter as it starts the current one, so that CTAs that stream faster take more
+  // tiles, and posts the indices in order through the mailbox ring; the MMA thread and
+  // the epilogue warps read them there.  An index past the last tile ends the sequence.
+  const bool dyn = CG == 1 && g.tile_ctr != nullptr;
+  // a reader's local-th tile (false: the wait gave up)
+  auto read_tile = [&](uint32_t local, int& tile) -> bool {
+    if (!dyn) {
+      tile = unit + (int)local * units;
+      return true;
+    }
+    const uint32_t j = local % kTileRing;
+    if (!ptx::mbar_wait(&ring_full[j], (local / kTileRing) & 1, kWaitBudget, abort_flag))
+      return false;
+    tile = s_ring[j];
+    return true;
+  };
+
   if (warp == 4) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
@@ -222,7 +260,22 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       const int num_st = (g.num_kb + g.kpb - 1) / g.kpb;
       uint32_t it = 0, s = 0, ph = 0;          // stages issued; ring slot and phase
       bool ok = true;
-      for (int tile = unit; ok && tile < num_tiles; tile += units) {
+      int tile = unit;
+      for (uint32_t local = 0;; ++local) {
+        if (dyn) {
+          // post the index once every reader has taken the one posted kTileRing ago
+          const uint32_t j = local % kTileRing;
+          if (!ptx::mbar_wait(&ring_free[j], ((local / kTileRing) & 1) ^ 1, kWaitBudget,
+                              abort_flag)) {
+            ok = false;
+            break;
+          }
+          s_ring[j] = tile;
+          ptx::mbar_arrive(&ring_full[j]);
+        }
+        if (tile >= num_tiles) break;
+        // the next claim goes out now; its answer is needed only after this tile's copies
+        const int next = dyn ? units + (int)atomicAdd(g.tile_ctr, 1u) : tile + units;
         const int vt = tile_vt(tile), nt = tile_nt(tile);
         const int row_a = (vt * CG + (int)rank) * kBlockV;
         const int bcol = (nt % g.n_bt) * g.BB;
@@ -262,6 +315,8 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
             ph ^= 1;
           }
         }
+        if (!ok) break;
+        tile = next;
       }
       if (!ok) {
         give_up();
@@ -290,7 +345,14 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
       bool ok = true;
       const int num_st = (g.num_kb + g.kpb - 1) / g.kpb;
       const uint32_t a_base = ptx::smem_u32(sA), b_base = ptx::smem_u32(sB);
-      for (int tile = unit; ok && tile < num_tiles; tile += units, ++local) {
+      for (;; ++local) {
+        int tile;
+        if (!read_tile(local, tile)) {
+          ok = false;
+          break;
+        }
+        if (dyn) ptx::mbar_arrive(&ring_free[local % kTileRing]);
+        if (tile >= num_tiles) break;
         int i0, ni, bb0, nb;
         ntile_extent(g, tile_nt(tile), i0, ni, bb0, nb);
         // rows up to the last valid slot (a pair always covers the full tile)
@@ -341,12 +403,11 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
             ph ^= 1;
           }
         }
-        if (ok) {
-          if (CG == 2)
-            ptx::mma_commit_pair_multicast(&acc_full[acc], 0x3);
-          else
-            ptx::mma_commit(&acc_full[acc]);
-        }
+        if (!ok) break;
+        if (CG == 2)
+          ptx::mma_commit_pair_multicast(&acc_full[acc], 0x3);
+        else
+          ptx::mma_commit(&acc_full[acc]);
       }
       if (!ok) give_up();
       // every MMA issued has finished once this commit lands
@@ -500,9 +561,19 @@ logits_gemm_tc(const __grid_constant__ CUtensorMap tm_w,
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    uint32_t local = 0;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    for (int tile = unit; tile < num_tiles; tile += units, ++local) {
+    for (uint32_t local = 0;; ++local) {
+      int tile;
+      // the warp leaves together (tcgen05.ld below is a warp-collective instruction)
+      if (!__all_sync(0xFFFFFFFFu, read_tile(local, tile))) {
+        give_up();
+        break;
+      }
+      if (dyn) {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ring_free[local % kTileRing]);
+      }
+      if (tile >= num_tiles) break;
       const int vt = tile_vt(tile);
       const int rt = vt * CG + (int)rank;              // this CTA's 128-row tile
       int i0, ni, bb0, nb;
@@ -734,13 +805,16 @@ cudaError_t launch_gemm(const CUtensorMap& tm_w, const CUtensorMap& tm_h, const 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CG;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may be scheduled while the previous kernel runs (the kernel waits for it first)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (PM) {
     // the PM form has the same resources; it needs its own shared-memory opt-in, once
     // per device
@@ -777,6 +851,8 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   g.prep = p.prep;
   g.prep_want = p.prep_want;
   g.zbound_k = p.zbound_k;
+  // single CTAs claim their tiles as they go (the control block is zeroed per pass)
+  g.tile_ctr = CG == 1 ? p.ctrl + kCtrlGemmTiles : nullptr;
   g.n_draft = p.skip_truncated ? p.n_draft : nullptr;
   g.Vhp = p.Vhp;
   g.ldb = p.ldb;
@@ -801,9 +877,9 @@ cudaError_t launch_base_logits_tc(const ProposePlan& p) {
   // (the hidden box must then fill whole 8-row swizzle atoms, so that the second
   // K-block's rows start where the descriptors expect them).  A last stage reaching past
   // H loads zeros there, which add nothing.
-  // shared memory: up to 1023 bytes of alignment, the stages, 256 bytes of barriers and
-  // the column-maximum keys
-  const size_t fixed = 1024 + 256 + (256 + 1 + kMaxLiveTiles) * sizeof(int);
+  // shared memory: up to 1023 bytes of alignment, the stages, the barriers and tile ring,
+  // and the column-maximum keys
+  const size_t fixed = 1024 + kBarBytes + (256 + 1 + kMaxLiveTiles) * sizeof(int);
   const int box_rows = g.BB * g.Ni / CG;
   const uint32_t kblock_bytes = kStageA + (uint32_t)(g.bn_mma / CG) * kBlockK * 2;
   g.kpb = 1;

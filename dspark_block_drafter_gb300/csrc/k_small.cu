@@ -1,5 +1,6 @@
-// Small kernels of the path: the confidence head with the truncation length, the
-// greedy verify/accept step, and the self-test of the bounded device-side wait.
+// Small kernels of the path: the zeroing of a pass's control block, the confidence head
+// with the truncation length, the greedy verify/accept step, and the self-test of the
+// bounded device-side wait.
 #include <algorithm>
 
 #include "common.cuh"
@@ -9,6 +10,17 @@
 namespace dspark {
 
 namespace {
+
+// The control block of a pass (error word, counters, barrier words, winner keys, bound
+// maxima) back to zero.  It lets the kernel after it be scheduled at once: that kernel,
+// launched as a dependent, waits for this one to finish before it reads or writes any of
+// these words.
+__global__ void __launch_bounds__(256) zero_block(uint4* __restrict__ p, size_t n16) {
+  pdl_signal();
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n16;
+       e += (size_t)gridDim.x * blockDim.x)
+    p[e] = make_uint4(0u, 0u, 0u, 0u);
+}
 
 // conf[b, i] = sigmoid(h[b, ifp + i] . w_conf + b_conf) and n_draft[b] = the first slot
 // with conf < conf_min, else N (llama.cpp commit 6fed9f6, "spec: add confidence-based
@@ -169,6 +181,15 @@ wait_selftest(uint32_t* __restrict__ err, long long budget, int pre_abort) {
 cudaError_t launch_wait_selftest(uint32_t* err, long long budget, int pre_abort,
                                  cudaStream_t stream) {
   wait_selftest<<<1, 32, 0, stream>>>(err, budget, pre_abort);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_block(void* p, size_t bytes, cudaStream_t stream) {
+  if (bytes % 16 != 0 || ((uintptr_t)p & 15) != 0) return cudaErrorInvalidValue;
+  const size_t n16 = bytes / 16;
+  if (n16 == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)std::min<size_t>(256, (n16 + 255) / 256);
+  zero_block<<<grid, 256, 0, stream>>>((uint4*)p, n16);
   return cudaGetLastError();
 }
 

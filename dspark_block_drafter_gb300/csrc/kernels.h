@@ -180,6 +180,9 @@ struct GemmTilePlan {
 GemmTilePlan plan_logits_gemm(int B, int N);
 
 cudaError_t launch_conf(const ProposePlan& p);
+// Zeroes `bytes` (a multiple of 16, 16-byte aligned) at p; the next kernel on the stream
+// may be launched as its dependent (launch_dependent, or the lm_head GEMM).
+cudaError_t launch_zero_block(void* p, size_t bytes, cudaStream_t stream);
 
 // Launch `kernel` on `stream` with programmatic stream serialisation, so that it may
 // start before the previous kernel on the stream has finished (it calls pdl_wait()

@@ -280,8 +280,8 @@ dspark_status dspark_propose_timed(const dspark_config* cfg, const dspark_head* 
                                    void* const* events);
 
 /* Number of kernels one dspark_propose call launches for this config, head and set of
-   requested outputs (the workspace reset is a memset node, not counted); -1 on invalid
-   input. */
+   requested outputs, the kernel that resets the workspace's control block included; -1
+   on invalid input. */
 int32_t dspark_propose_kernel_count(const dspark_config* cfg, const dspark_head* head,
                                     const dspark_outputs* out);
 

@@ -195,20 +195,22 @@ def test_timed_and_kernel_count_checked(lib):
     st = ds._abi.dspark_propose_timed(cfg, head, 0x4000, 0x5000, out, 0x10000, need - 1, 0,
                                       [0x10] * n)
     assert st == _abi.DSPARK_ERR_WORKSPACE
-    # launches per pass on the fp32 path: confidence, GEMM and the one-launch chain; or,
-    # when a GPU says this small shape fits, the chain alone (it evaluates both)
-    assert ds._abi.dspark_propose_kernel_count(cfg, head, out) in (1, 3)
-    # bf16, no prepared head: confidence, GEMM, one chain launch per 32 blocks, top-k
+    # launches per pass (each starts with the control-block reset) on the fp32 path:
+    # confidence, GEMM and the one-launch chain; or, when a GPU says this small shape
+    # fits, the chain alone (it evaluates both)
+    assert ds._abi.dspark_propose_kernel_count(cfg, head, out) in (2, 4)
+    # bf16, no prepared head: reset, confidence, GEMM, one chain launch per 32 blocks,
+    # top-k
     bf = _cfg(dtype=1, B=70)
     topk = _abi.dspark_outputs(draft=0x100, n_draft=0x200, topk_ids=0x300, topk_vals=0x400)
-    assert ds._abi.dspark_propose_kernel_count(bf, head, topk) == 1 + 1 + 3 + 1
-    assert ds._abi.dspark_propose_kernel_count(bf, head, out) == 1 + 1 + 3
-    # a prepared head: the GEMM and the tables with the walk; the confidence kernel first
-    # when the block length is adaptive
+    assert ds._abi.dspark_propose_kernel_count(bf, head, topk) == 1 + 1 + 1 + 3 + 1
+    assert ds._abi.dspark_propose_kernel_count(bf, head, out) == 1 + 1 + 1 + 3
+    # a prepared head: reset, the GEMM and the tables with the walk; the confidence kernel
+    # before the GEMM when the block length is adaptive
     prep = _head(prepared=0x9000)
-    assert ds._abi.dspark_propose_kernel_count(bf, prep, topk) == 2
+    assert ds._abi.dspark_propose_kernel_count(bf, prep, topk) == 3
     assert ds._abi.dspark_propose_kernel_count(_cfg(dtype=1, B=70, skip_truncated=1), prep,
-                                               topk) == 3
+                                               topk) == 4
     assert ds._abi.dspark_propose_kernel_count(_cfg(B=0), head, out) == -1
 
 

@@ -87,12 +87,12 @@ def test_kernel_count_follows_the_compact_head():
     cfg = _cfg(wl)
     prepared = tio.head_to_device(hd).prepare(cfg)
     out = tio.Outputs.allocate(wl.B, wl.N, wl.top_k, prepared.V_head)
-    # the compact head, prepared: the pruned chain (GEMM + tables)
-    assert _abi.dspark_propose_kernel_count(cfg, prepared.struct(), out.struct()) == 2
-    # top_k above the emittable rows: the full head's dense chain (confidence, GEMM,
-    # chain and the top-k merge)
+    # the compact head, prepared: the pruned chain (reset, GEMM, tables)
+    assert _abi.dspark_propose_kernel_count(cfg, prepared.struct(), out.struct()) == 3
+    # top_k above the emittable rows: the full head's dense chain (reset, confidence,
+    # GEMM, chain and the top-k merge)
     wl8 = _wl(n_emit=5, top_k=8)
     cfg8 = _cfg(wl8)
     p8 = tio.head_to_device(make_head(wl8)).prepare(cfg8)
     out8 = tio.Outputs.allocate(wl8.B, wl8.N, wl8.top_k, p8.V_head)
-    assert _abi.dspark_propose_kernel_count(cfg8, p8.struct(), out8.struct()) == 4
+    assert _abi.dspark_propose_kernel_count(cfg8, p8.struct(), out8.struct()) == 5
