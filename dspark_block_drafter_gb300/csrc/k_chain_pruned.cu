@@ -498,7 +498,7 @@ __host__ __device__ inline size_t walk_smem_bytes(int r, int N) {
   return sizeof(float) * ((r + 3) & ~3) + sizeof(Cand) * (kCand + kMaxKeep) +
          sizeof(int) * 4 * (size_t)N + sizeof(int32_t) * 2 * (size_t)N * kCapA +
          sizeof(float) * (size_t)N + sizeof(float) * kWarps + sizeof(int) * kWarps +
-         sizeof(int) * (3 + kMaxKeep);
+         sizeof(int) * (3 + kMaxKeep) + sizeof(int8_t) * (size_t)N * kCapA;
 }
 
 // The walk of block b over its N slots, by the whole CTA (the last of the block's table
@@ -523,56 +523,67 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
   int& s_nfull = s_keep[kMaxKeep];
   int& s_prev = s_keep[kMaxKeep + 1];
   int& s_stop = s_keep[kMaxKeep + 2];
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  int8_t (*s_nx)[kCapA] = reinterpret_cast<int8_t (*)[kCapA]>(s_keep + kMaxKeep + 3);   // [N][kCapA]
+  const int tid = threadIdx.x;
   // slots to draft: all, or (adaptive block length) those before the precomputed cut
   const int cut = a.nd_in ? min(max(a.nd_in[b], 0), a.N) : a.N;
 
-  // ---- counts, then the previous rows and argmax rows of every tabulated slot
+  // ---- counts, the previous rows and argmax rows of every slot, and the confidences,
+  //      in one round of copies (entries past a slot's count, or of a slot without a
+  //      table, are copied but never read)
   for (int i = tid; i < cut; i += kThreads) {
-    s_nc[i] = a.cand_n[(size_t)i * a.B + b];
-    s_na[i] = a.prev_n[(size_t)i * a.B + b];
+    cp_async4(&s_nc[i], a.cand_n + (size_t)i * a.B + b);
+    cp_async4(&s_na[i], a.prev_n + (size_t)i * a.B + b);
   }
   if (a.conf && !a.nd_in)
     for (int i = tid; i < a.N; i += kThreads) cp_async4(&s_conf[i], a.conf + (size_t)b * a.N + i);
+  for (int e = tid; e < cut * kCapA; e += kThreads) {
+    const int i = e / kCapA, p = e % kCapA;
+    const size_t o = ((size_t)i * a.B + b) * kCapA + p;
+    cp_async4(&s_av[i][p], a.prev_v + o);
+    cp_async4(&s_am[i][p], a.amax + o);
+  }
+  cp_async_wait_all();
   __syncthreads();
   auto tabulated = [&](int i) {
     return s_nc[i] >= 1 && s_nc[i] <= kTabC && s_na[i] >= 1 && s_na[i] <= kCapA;
   };
+
+  // ---- the links of the walk, all at once: for a tabulated slot i and a possible
+  //      previous row p of it (index into A(i - 1)), nx[i][p] = the index in A(i) of the
+  //      row the table chose for p (its first listing there), or -1 where a walk through p
+  //      stops after slot i: that row is not valid, or slot i + 1 has no table or does not
+  //      list it
   for (int e = tid; e < cut * kCapA; e += kThreads) {
     const int i = e / kCapA, p = e % kCapA;
-    if (tabulated(i) && p < s_na[i]) {
-      const size_t o = ((size_t)i * a.B + b) * kCapA + p;
-      cp_async4(&s_av[i][p], a.prev_v + o);
-      cp_async4(&s_am[i][p], a.amax + o);
+    int nx = -1;
+    if (i + 1 < cut && tabulated(i) && tabulated(i + 1) && p < s_na[i]) {
+      const int row = s_am[i][p];
+      if (row >= 0 && row < a.Vh)
+        for (int q = 0; q < s_na[i + 1]; ++q)
+          if (s_av[i + 1][q] == row) {
+            nx = q;
+            break;
+          }
     }
+    s_nx[i][p] = (int8_t)nx;
   }
-  cp_async_wait_all();
   __syncthreads();
-
-  // ---- warp 0 walks the tabulated slots as far as it can
-  if (warp == 0) {
-    int prev = -1, step = 0;
+  // ---- thread 0 follows the links through the tabulated slots as far as they go (slot
+  //      0's only previous row is the anchor)
+  if (tid == 0) {
+    int prev = -1, step = 0, pi = 0;
     for (; step < cut; ++step) {
-      if (!tabulated(step)) break;
-      int pi = 0;
-      if (step > 0) {
-        const bool hit = lane < s_na[step] && s_av[step][lane] == prev;
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, hit);
-        if (m == 0) break;
-        pi = __ffs(m) - 1;
-      }
+      if (!tabulated(step) || pi < 0) break;
       const int row = s_am[step][pi];
       if (row < 0 || row >= a.Vh) break;
-      if (lane == 0) {
-        s_pi[step] = pi;
-        s_row[step] = row;                           // drafted after the walk
-      }
+      s_pi[step] = pi;
+      s_row[step] = row;                             // drafted after the walk
       prev = row;
+      pi = s_nx[step][pi];
     }
-    if (lane == 0) {
-      s_stop = step;
-      s_prev = prev;
-    }
+    s_stop = step;
+    s_prev = prev;
   }
   __syncthreads();
   for (int step = s_stop; step < cut; ++step) {
@@ -690,30 +701,34 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
     __syncthreads();
   }
 
-  // ---- the draft: every slot's chosen head row as a token
-  for (int i = tid; i < a.N; i += kThreads) {
+  // ---- the draft (every slot's chosen head row as a token) and the top-k of the
+  //      looked-up slots (the entries stored for the chosen previous row): all loads
+  //      first, then the stores
+  for (int e = tid; e < a.N * a.k; e += kThreads) {
     int tok = -1;                                    // past the cut: not drafted
-    if (i < cut) {
-      const int row = s_row[i];
+    if (e < a.N && e < cut) {
+      const int row = s_row[e];
       tok = a.d2t ? a.d2t[row] : row;
     }
-    a.draft[(size_t)b * a.N + i] = tok;
-  }
-  // ---- top-k of the looked-up slots: the entries stored for the chosen previous row
-  if (a.want_topk) {
-    for (int e = tid; e < a.N * a.k; e += kThreads) {
-      const int i = e / a.k, q = e % a.k;
-      const size_t dst = ((size_t)b * a.N + i) * a.k + q;
-      if (i >= cut) {                                // past the cut: not drafted
-        if (a.topk_ids) a.topk_ids[dst] = -1;
-        if (a.topk_vals) a.topk_vals[dst] = NAN;
-        continue;
+    const int i = e / a.k, q = e % a.k;
+    bool put = false;
+    int id = -1;
+    float val = NAN;
+    if (a.want_topk) {
+      if (i >= cut) {
+        put = true;                                  // past the cut: not drafted
+      } else if (s_pi[i] >= 0) {                     // (else written by the on-the-fly step)
+        const size_t src = (((size_t)i * a.B + b) * kCapA + s_pi[i]) * a.k + q;
+        if (a.topk_ids) id = a.tk_id[src];
+        if (a.topk_vals) val = a.tk_val[src];
+        put = true;
       }
-      const int pi = s_pi[i];
-      if (pi < 0) continue;                          // written by the on-the-fly step
-      const size_t src = (((size_t)i * a.B + b) * kCapA + pi) * a.k + q;
-      if (a.topk_ids) a.topk_ids[dst] = a.tk_id[src];
-      if (a.topk_vals) a.topk_vals[dst] = a.tk_val[src];
+    }
+    if (e < a.N) a.draft[(size_t)b * a.N + e] = tok;
+    if (put) {
+      const size_t dst = ((size_t)b * a.N + i) * a.k + q;
+      if (a.topk_ids) a.topk_ids[dst] = id;
+      if (a.topk_vals) a.topk_vals[dst] = val;
     }
   }
   // ---- truncation at the first slot whose confidence is below conf_min (llama.cpp
