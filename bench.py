@@ -49,10 +49,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + written) of one lm_head GEMM launch from an ncu capture of the
 # current kernel, per workload; the summary and the command are in the named file.
 GEMM_TRAFFIC = {
-    "qwen3_8b_b32": (1.283e9 + 0.049e9, "profiles/logits_gemm_qwen3_8b_b32.md"),
-    "qwen3_8b_b1": (1.245e9 + 0.012e9, "profiles/logits_gemm_qwen3_8b_b1.md"),
-    "qwen38_27b_b8": (2.560e9 + 0.123e9, "profiles/logits_gemm_qwen38_27b_b8.md"),
-    "gemma4_bonus_b64": (0.188e9 + 0.026e9, "profiles/logits_gemm_gemma4_bonus_b64.md"),
+    "qwen3_8b_b32": (1.2496e9 + 0.0245e9, "profiles/logits_gemm_qwen3_8b_b32.md"),
+    "qwen3_8b_b1": (1.2449e9 + 0.0042e9, "profiles/logits_gemm_qwen3_8b_b1.md"),
+    "qwen38_27b_b8": (2.5444e9 + 0.0754e9, "profiles/logits_gemm_qwen38_27b_b8.md"),
+    "gemma4_bonus_b64": (0.1870e9 + 0.0071e9, "profiles/logits_gemm_gemma4_bonus_b64.md"),
 }
 # fp32 CUDA-core peak used for the fp32 path: 152 SMs x 128 FP32 lanes x 2 flops (FMA) x
 # 2.07 GHz maximum SM clock
