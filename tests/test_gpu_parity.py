@@ -204,6 +204,30 @@ def test_bonus_layout_six_slots(chain):
              chain=chain)
 
 
+@pytest.mark.parametrize("shape", [
+    # several pair tiles, ragged vocabulary tail, an odd number of K-blocks
+    dict(B=64, L_in=7, sample_from_anchor=False, H=576, V=3000, r=32, top_k=4),
+    # fewer blocks than the tile holds (the hidden box reads zeros past them)
+    dict(B=48, L_in=7, sample_from_anchor=False, H=256, V=2048, r=32, top_k=1),
+    dict(B=40, L_in=6, H=320, V=1504, r=24, top_k=8),
+])
+@pytest.mark.parametrize("chain", CHAINS)
+def test_six_slot_block_tiles(shape, chain):
+    # six slots of 33-64 blocks: pair tiles over two block tiles of 32, the second
+    # partly empty when B < 64
+    run_case(_small(**shape), chain=chain)
+
+
+@pytest.mark.parametrize("chain", CHAINS)
+@pytest.mark.parametrize("form", ["full", "d2t"])
+def test_six_slot_reduced_vocab(form, chain):
+    wl = _small(B=64, L_in=7, sample_from_anchor=False, H=192, V=4096, r=32, top_k=2,
+                n_emit=1000)
+    g, o, rep = run_case(wl, form, chain=chain)
+    emit = set(make_head(wl)["emit_rows"].tolist())
+    assert set(g["draft"].ravel().tolist()) <= emit
+
+
 @pytest.mark.parametrize("chain", CHAINS)
 def test_most_slots(chain):
     # 256 prediction slots: the longest chain the bf16 path takes
