@@ -228,6 +228,21 @@ def test_six_slot_reduced_vocab(form, chain):
     assert set(g["draft"].ravel().tolist()) <= emit
 
 
+@pytest.mark.parametrize("shape", [
+    # two N-tiles of 256 prediction rows (B=32 x 16 slots); H = 320: five K-blocks in
+    # three stages, the last one half past H
+    dict(B=32, L_in=16, H=320, V=152 * 256 + 200, r=24, top_k=8),
+    # one N-tile (B=32 x 8 slots), ragged vocabulary tail
+    dict(B=32, L_in=8, H=320, V=160 * 256 + 64, r=24, top_k=4),
+    # six slots of 64 blocks
+    dict(B=64, L_in=7, sample_from_anchor=False, H=256, V=80 * 256, r=32, top_k=1),
+])
+@pytest.mark.parametrize("chain", CHAINS)
+def test_several_tile_waves(shape, chain):
+    # more 256-row pair tiles than pairs (76 on 152 SMs), not a whole number of waves
+    run_case(_small(**shape), chain=chain)
+
+
 @pytest.mark.parametrize("chain", CHAINS)
 def test_most_slots(chain):
     # 256 prediction slots: the longest chain the bf16 path takes
