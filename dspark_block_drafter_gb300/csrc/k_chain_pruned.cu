@@ -961,7 +961,17 @@ __device__ __forceinline__ void table_work(const TableArgs& a, uint8_t* dsm, int
       if (lane == 0) a.amax[ib * kCapA + p] = (bi >= 0 && bi < a.Vh) ? bi : -1;
       if (!a.want_topk) continue;
       const float* rk = a.zrank ? s_cz : x;
-      if (nc <= 32) {
+      if (a.k == 1 && !a.zrank) {
+        // the top 1 of the corrected logits is the argmax just found (same order)
+        if (lane == 0) {
+          const size_t o = ib * kCapA + p;
+          const int row = (bi >= 0 && bi < a.Vh) ? bi : 0;
+          a.tk_id[o] = a.d2t ? a.d2t[row] : row;
+          a.tk_val[o] = bv;
+        }
+        continue;
+      }
+      if (nc <= 32 && a.k > 1) {
         // one entry per lane: sort the warp, lane q holds the q-th
         float v = lane < nc ? rk[lane] : -INFINITY;
         int id = lane < nc ? s_cv[lane] : 0x7FFFFFFF;
