@@ -498,7 +498,7 @@ __host__ __device__ inline size_t walk_smem_bytes(int r, int N) {
   return sizeof(float) * ((r + 3) & ~3) + sizeof(Cand) * (kCand + kMaxKeep) +
          sizeof(int) * 4 * (size_t)N + sizeof(int32_t) * 2 * (size_t)N * kCapA +
          sizeof(float) * (size_t)N + sizeof(float) * kWarps + sizeof(int) * kWarps +
-         sizeof(int) * (3 + kMaxKeep) + sizeof(int8_t) * (size_t)N * kCapA;
+         sizeof(int) * (3 + kMaxKeep) + 8 + sizeof(int2) * (size_t)N * kCapA;
 }
 
 // The walk of block b over its N slots, by the whole CTA (the last of the block's table
@@ -523,7 +523,8 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
   int& s_nfull = s_keep[kMaxKeep];
   int& s_prev = s_keep[kMaxKeep + 1];
   int& s_stop = s_keep[kMaxKeep + 2];
-  int8_t (*s_nx)[kCapA] = reinterpret_cast<int8_t (*)[kCapA]>(s_keep + kMaxKeep + 3);   // [N][kCapA]
+  int2 (*s_step)[kCapA] = reinterpret_cast<int2 (*)[kCapA]>(
+      ((uintptr_t)(s_keep + kMaxKeep + 3) + 7) & ~(uintptr_t)7);                  // [N][kCapA]
   const int tid = threadIdx.x;
   // slots to draft: all, or (adaptive block length) those before the precomputed cut
   const int cut = a.nd_in ? min(max(a.nd_in[b], 0), a.N) : a.N;
@@ -549,38 +550,40 @@ __device__ void walk_block(const SelectArgs& a, int b, uint8_t* dsm) {
     return s_nc[i] >= 1 && s_nc[i] <= kTabC && s_na[i] >= 1 && s_na[i] <= kCapA;
   };
 
-  // ---- the links of the walk, all at once: for a tabulated slot i and a possible
-  //      previous row p of it (index into A(i - 1)), nx[i][p] = the index in A(i) of the
-  //      row the table chose for p (its first listing there), or -1 where a walk through p
-  //      stops after slot i: that row is not valid, or slot i + 1 has no table or does not
-  //      list it
+  // ---- the steps of the walk, all at once: for a tabulated slot i and a possible
+  //      previous row p of it (index into A(i - 1)), step[i][p] = {the row the table
+  //      chose for p, the index in A(i) of that row (its first listing there)}; the row
+  //      is -1 where the walk stops at slot i (it is not valid), the index -1 where it
+  //      stops after slot i (slot i + 1 has no table or does not list the row)
   for (int e = tid; e < cut * kCapA; e += kThreads) {
     const int i = e / kCapA, p = e % kCapA;
-    int nx = -1;
-    if (i + 1 < cut && tabulated(i) && tabulated(i + 1) && p < s_na[i]) {
+    int2 st = make_int2(-1, -1);
+    if (tabulated(i) && p < s_na[i]) {
       const int row = s_am[i][p];
-      if (row >= 0 && row < a.Vh)
-        for (int q = 0; q < s_na[i + 1]; ++q)
-          if (s_av[i + 1][q] == row) {
-            nx = q;
-            break;
-          }
+      if (row >= 0 && row < a.Vh) {
+        st.x = row;
+        if (i + 1 < cut && tabulated(i + 1))
+          for (int q = 0; q < s_na[i + 1]; ++q)
+            if (s_av[i + 1][q] == row) {
+              st.y = q;
+              break;
+            }
+      }
     }
-    s_nx[i][p] = (int8_t)nx;
+    s_step[i][p] = st;
   }
   __syncthreads();
-  // ---- thread 0 follows the links through the tabulated slots as far as they go (slot
-  //      0's only previous row is the anchor)
+  // ---- thread 0 follows the steps through the tabulated slots as far as they go (slot
+  //      0's only previous row is the anchor): one shared-memory load per slot
   if (tid == 0) {
     int prev = -1, step = 0, pi = 0;
-    for (; step < cut; ++step) {
-      if (!tabulated(step) || pi < 0) break;
-      const int row = s_am[step][pi];
-      if (row < 0 || row >= a.Vh) break;
+    for (; step < cut && pi >= 0; ++step) {
+      const int2 st = s_step[step][pi];
+      if (st.x < 0) break;
       s_pi[step] = pi;
-      s_row[step] = row;                             // drafted after the walk
-      prev = row;
-      pi = s_nx[step][pi];
+      s_row[step] = st.x;                            // drafted after the walk
+      prev = st.x;
+      pi = st.y;
     }
     s_stop = step;
     s_prev = prev;
