@@ -308,29 +308,38 @@ def _config(wl, l2):
 
 # ------------------------------------------------------------------ GPU arm
 def _time_steps(tio, _abi, cfg, head, ws, hidden, anchors, out, target, acc, bonus,
-                emitted, stream, flush, K, W, world):
+                emitted, stream, flush, K, W, world, graph=False):
     """W warm-up steps, then K timed steps (L2 flushed before each, untimed): device time
     per step from CUDA events on the launching stream around dspark_propose +
-    dspark_verify.  Then K more steps through dspark_propose_timed for the per-stage
-    breakdown (its stage events add a little time of their own, so the step time comes
-    from the first set)."""
+    dspark_verify, called directly or (graph=True) replayed from a CUDA graph of one
+    pass captured after the warm-up.  Then K more direct steps through
+    dspark_propose_timed for the per-stage breakdown (its stage events add a little time
+    of their own, so the step time comes from the first set)."""
     import torch
     ns = _abi.DSPARK_NUM_STAGES
 
-    def step(events=None):
+    def step(events=None, s=None):
+        s = stream if s is None else s
         if events is None:
-            tio.propose(cfg, head, hidden, anchors, out, ws, stream)
+            tio.propose(cfg, head, hidden, anchors, out, ws, s)
         else:
             _abi.check(_abi.dspark_propose_timed(
                 cfg, head.struct(), hidden.data_ptr(), anchors.data_ptr(), out.struct(),
-                ws.data_ptr(), ws.numel(), stream.cuda_stream, [e.cuda_event for e in events]))
-        tio.verify(out.draft, out.n_draft, target, acc, bonus, emitted, stream)
+                ws.data_ptr(), ws.numel(), s.cuda_stream, [e.cuda_event for e in events]))
+        tio.verify(out.draft, out.n_draft, target, acc, bonus, emitted, s)
 
     for _ in range(W):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     assert tio.device_status(ws, stream) == 0
+    g = None
+    if graph:
+        # one pass captured as it is replayed by a decoding loop (same buffers)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(s=torch.cuda.current_stream())
+        torch.cuda.synchronize()
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)]
     torch.cuda.synchronize()
@@ -341,7 +350,10 @@ def _time_steps(tio, _abi, cfg, head, ws, hidden, anchors, out, target, acc, bon
     for s_ in range(K):
         flush.zero_()                                   # untimed L2 flush
         ev_step[s_][0].record(stream)
-        step()
+        if g is not None:
+            g.replay()
+        else:
+            step()
         ev_step[s_][1].record(stream)
     torch.cuda.synchronize()
     _barrier(world)
@@ -349,6 +361,7 @@ def _time_steps(tio, _abi, cfg, head, ws, hidden, anchors, out, target, acc, bon
     window = (t_begin, datetime.datetime.now())
     assert tio.device_status(ws, stream) == 0
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    del g
 
     # per-stage breakdown
     ev_stage = [[torch.cuda.Event(enable_timing=True) for _ in range(ns + 1)] for _ in range(K)]
@@ -422,8 +435,9 @@ def run_ours(args):
     clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     clocks.start()
+    # t_pass: the pass replayed from a CUDA graph, as a decoding loop runs it
     ms, stage_ms, t_wall, window = _time_steps(tio, _abi, cfg, head, ws, *common, K,
-                                               args.warmup, world)
+                                               args.warmup, world, graph=True)
     clk = clocks.stop(window)
     if clk and set(clk["reasons"]) & set(BAD_CLOCK_REASONS):
         # a run the GPU throttled for heat or a hardware slowdown is no measurement:
@@ -431,11 +445,14 @@ def run_ours(args):
         first = clk["reasons"]
         clocks.start()
         ms, stage_ms, t_wall, window = _time_steps(tio, _abi, cfg, head, ws, *common, K,
-                                                   args.warmup, world)
+                                                   args.warmup, world, graph=True)
         clk = clocks.stop(window)
         if clk:
             clk["remeasured_after"] = first
     ms_max, value = job_throughput(ms, wl.B * wl.N, world, dev)
+    # the same pass through direct calls, beside it
+    ms_d, _, _, _ = _time_steps(tio, _abi, cfg, head, ws, *common, K, args.warmup, world)
+    ms_direct, _ = job_throughput(ms_d, wl.B * wl.N, world, dev)
     slots = wl.B * wl.N * world
     launches = _abi.dspark_propose_kernel_count(cfg, head.struct(), out.struct()) + 1
 
@@ -511,6 +528,8 @@ def run_ours(args):
                               "step (untimed)"),
         "verified_blocks_per_s": wl.B * world / (ms_max / 1e3),
         "t_pass_us": ms_max * 1e3,
+        "timing": "CUDA-graph replay of one pass (dspark_propose + dspark_verify)",
+        "t_pass_direct_us": ms_direct * 1e3,
         "stage_us": {k: v * 1e3 for k, v in stage_ms.items()},
         "chain": "pruned" if head is not dense_head else "dense",
         "head_prepare_ms": None if t_prep is None else t_prep * 1e3,
